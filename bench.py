@@ -1,0 +1,537 @@
+#!/usr/bin/env python3
+"""Benchmark of the ring AllReduce library on synthetic rank buffers.
+
+One step is one ra_allreduce call over R rank buffers resident in HBM: the
+chunk plan, every ReduceScatter and AllGather round of the ring (done by the
+selected variant; the default carries every element's ring fold out in one
+launch).  Prints one JSON line.
+
+  value     algbw = n * bytes_per_element / time per step (the per-rank
+            payload over time, the usual AllReduce convention), summed over
+            replicas when run on several GPUs (each GPU runs its own R-rank
+            ring: the collective does not span GPUs)
+  busbw     algbw * 2(R-1)/R: what every rank of a real ring sends, section
+            13 of the ring page ("Why AllReduce = ReduceScatter + AllGather --
+            NCCL Ring AllReduce"), 2N(k-1)/k per rank
+  roofline  the dominant kernel's compulsory HBM bytes (read every input
+            once, write every output once: 2 R n b) over its CUDA-event
+            launch time, against the measured device copy bandwidth
+
+--impl reference times the CPU oracle instead (host cores, bounded sample
+of the same workload).  --sweep prints one line per size / rank count of the
+sweep workloads (not the headline).
+"""
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ring allreduce algbw GB/s and % of GB300 HBM roofline (R ranks on 1 GPU)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "r8_f32": "ring allreduce, R=8 ranks x n=2^24 fp32 per rank (64 MiB/rank), N(0,1), sum, seed 1",
+    "r8_bf16": "ring allreduce, R=8 ranks x n=2^26+3 bf16 per rank (ragged), grad-like N(0,1e-3) with 1% x100, "
+               "sum with bf16 rounding per hop, seed 2",
+    "r16_i32": "ring allreduce, R=16 ranks x n=2^24 int32 per rank, uniform [-2^20,2^20], sum, seed 3",
+    "r4_small": "ring allreduce, R=4 ranks x n=4096 fp32 per rank, integers in [-8,8], sum, seed 0",
+}
+
+
+# ------------------------------------------------------------------ helpers
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _init_pg(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    # the harness only needs a barrier and a max over ranks: gloo on the host
+    dist.init_process_group("gloo")
+    return dist
+
+
+def aggregate(local_seconds, local_units, dist):
+    """Max of the per-rank times and sum of the per-rank work over the
+    process group (identity without one)."""
+    if dist is None:
+        return local_seconds, local_units
+    import torch
+    t = torch.tensor([local_seconds], dtype=torch.float64)
+    u = torch.tensor([local_units], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(workload, units_full):
+    """Traffic per launch of the direct kernel from the committed ncu
+    summary, scaled to the full workload, or None when the summary was
+    taken on other kernel sources."""
+    from ring_allreduce_gb300 import build
+    path = os.path.join(ROOT, "profiles", f"direct_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
+    m_units = re.search(r"units_per_launch:\s*(\d+)", text)
+    if not (m_hash and m_bytes and m_units):
+        return None, path
+    if m_hash.group(1) != build.kernel_source_hash():
+        return None, path
+    return int(m_bytes.group(1)) * units_full / int(m_units.group(1)), path
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while a region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=50):
+        self.idx = gpu_index
+        self.period = period_ms
+        self.lines = []
+        self.proc = None
+        self.t_begin = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_begin <= r[0] <= self.t_end + 0.05]
+        note = "samples inside the timed region"
+        if not inside:
+            mid = (self.t_begin + self.t_end) / 2
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+            note = "timed region shorter than the sampling period: nearest samples"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------- GPU arm
+
+def _device_ranks(torch, R, n, np_dtype, host=None):
+    """R rank buffers as rows of one device tensor; rows padded so every
+    rank's base is 16-byte aligned."""
+    import numpy as np
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.uint16): torch.int16,
+           np.dtype(np.int32): torch.int32}[np.dtype(np_dtype)]
+    stride = ((n + 63) // 64) * 64
+    big = torch.empty((R, stride), dtype=tdt, device="cuda")
+    if host is not None:
+        for r in range(R):
+            a = host[r].view(np.int16) if np.dtype(np_dtype) == np.uint16 else host[r]
+            big[r, :n].copy_(torch.from_numpy(a))
+    return big, [big[r, :n] for r in range(R)]
+
+
+def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        h.allreduce(ins, outs, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+        if per_launch else []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        if per_launch:
+            ev[i][0].record(stream)
+        h.allreduce(ins, outs, stream)
+        if per_launch:
+            ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev] if per_launch else []
+    return total_ms, launch_ms
+
+
+def run_gpu_arm(args):
+    import numpy as np
+    import torch
+
+    from ring_allreduce_gb300 import build, inputs
+    build.build()
+    from ring_allreduce_gb300 import binding as ra
+
+    ws, rank, local = _dist_env()
+    dist = _init_pg(ws)
+    torch.cuda.set_device(local)
+    w = dict(inputs.WORKLOADS[args.workload])
+    R = w["R"]
+    n = args.n or w["n"]
+    dtype, op = w["dtype"], w["ops"][0]
+    b = inputs.itemsize(dtype)
+    st_dtype = inputs.storage_dtype(dtype)
+
+    host = inputs.generate(R, n, dtype, w["dist"], w["seed"])
+    big_in, ins = _device_ranks(torch, R, n, st_dtype, host)
+    big_out, outs = _device_ranks(torch, R, n, st_dtype)
+    h = ra.RingAllReduce(R, n, dtype, op, variant=args.variant)
+    variant_name = args.variant
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    gpu_id = str(local)
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id).start() if (rank == 0 and not args.no_clocks) else None
+    for _ in range(args.warmup):
+        h.allreduce(ins, outs)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.begin()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        h.allreduce(ins, outs, stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.end()
+    if dist:
+        dist.barrier()
+    total_s = t0.elapsed_time(t1) / 1e3
+    launch_ms = [a.elapsed_time(bb) for a, bb in ev]
+    clk = clocks.stop() if clocks else None
+    st_code, err = h.device_status()
+    if st_code != ra.Status.OK:
+        raise RuntimeError(f"device status {st_code.name}: {err.as_dict()}")
+
+    t_step, total_units = aggregate(total_s / args.steps, float(n * b), dist)
+    algbw = total_units / t_step / 1e9
+    busbw = algbw * 2 * (R - 1) / R if R > 1 else algbw
+
+    # dominant kernel: the one launch per step of the direct variant
+    compulsory = 2 * R * n * b
+    ring_bytes = 5 * (R - 1) * n * b
+    launch_avg_s = statistics.mean(launch_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = compulsory / launch_avg_s / 1e9
+    traffic, prof_path = profile_traffic(args.workload, n) if args.n is None else (None, None)
+
+    result = {
+        "metric": METRIC,
+        "value": round(algbw, 3),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step * 1e3, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD_TEXT.get(args.workload, args.workload) if args.n is None
+            else f"{args.workload} with n={n}",
+            "R": R, "n_per_rank": n, "op": op, "variant": variant_name,
+            "l2": f"inputs larger than L2: {R * n * b / 2**20:.0f} MiB of inputs, "
+                  f"{R * n * b / 2**20:.0f} MiB of outputs per step, no flush",
+            "parallelism": f"replicas x{ws} (each GPU runs its own {R}-rank ring)",
+        },
+        "busbw": round(busbw, 3),
+        "hbm_frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "ra::direct_kernel" if variant_name in ("auto", "direct") else f"{variant_name} step",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "bytes_per_launch": compulsory,
+            "bytes_model": "compulsory 2*R*n*b (each input read once, each output written once)",
+            "launch_ms_avg": round(launch_avg_s * 1e3, 6),
+            "traffic": traffic,
+            "traffic_source": os.path.relpath(prof_path, ROOT) if prof_path else None,
+        },
+        "gpu_launches": args.steps * (1 if variant_name in ("auto", "direct", "persistent") else 2 * (R - 1)),
+    }
+    if clk is not None:
+        result["clocks"] = clk
+
+    # ---- other variants, same workload (fewer steps)
+    if not args.no_variants and rank == 0:
+        var = {}
+        for v in ("direct", "ring", "persistent"):
+            hv = ra.RingAllReduce(R, n, dtype, op, variant=v)
+            steps_v = max(5, min(args.steps, 100))
+            total_ms, lm = _time_variant(torch, ra, hv, ins, outs, steps_v, max(3, args.warmup // 4 or 3))
+            assert hv.device_status()[0] == ra.Status.OK
+            hv.close()
+            t = statistics.mean(lm) / 1e3
+            by = compulsory if v == "direct" else (ring_bytes if v == "ring" else ring_bytes)
+            var[v] = {"algbw": round(n * b / t / 1e9, 3),
+                      "us_per_call": round(t * 1e6, 2),
+                      "frac_compulsory": round(compulsory / t / 1e9 / peak, 4),
+                      "frac_own_bytes": round(by / t / 1e9 / peak, 4),
+                      "own_bytes": by}
+        result["variants"] = var
+
+    # ---- end to end through the public API, host buffers
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        pin_in = torch.empty(big_in.shape, dtype=big_in.dtype, pin_memory=True)
+        pin_in.copy_(big_in)
+        pin_out = torch.empty(big_out.shape, dtype=big_out.dtype, pin_memory=True)
+        h.allreduce(ins, outs)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            big_in.copy_(pin_in, non_blocking=True)
+            h.allreduce(ins, outs, stream)
+            pin_out.copy_(big_out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        te, units = aggregate(e0.elapsed_time(e1) / 1e3 / e2e_steps, float(n * b), dist)
+        result["e2e"] = {"value": round(units / te / 1e9, 3), "unit": "GB/s",
+                         "h2d_bytes_per_step": big_in.numel() * big_in.element_size(),
+                         "d2h_bytes_per_step": big_out.numel() * big_out.element_size(),
+                         "steps": e2e_steps,
+                         "note": "pinned host inputs copied in, ra_allreduce, all R outputs copied out, every step"}
+        if True:
+            got = pin_out[0, :n].numpy()
+            if not np.array_equal(got.view(np.uint8), big_out[0, :n].cpu().numpy().view(np.uint8)):
+                raise RuntimeError("e2e read-back differs from the device result")
+
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+
+    h.close()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def _oracle_step_seconds(workload, n_sample):
+    from oracle import elementops, ring
+    from ring_allreduce_gb300 import inputs
+    w = inputs.WORKLOADS[workload]
+    x = inputs.generate(w["R"], n_sample, w["dtype"], w["dist"], w["seed"])
+    op = elementops.get_op(w["dtype"], w["ops"][0])
+    t = time.perf_counter()
+    ring.ring_allreduce(x, op)
+    return time.perf_counter() - t, x, op
+
+
+def cpu_baseline(workload, budget_s=15.0, n_sample=None):
+    """Time the oracle, as it stands, on R ranks of a sample of the
+    workload; value is algbw on the sample."""
+    from oracle import ring
+    from ring_allreduce_gb300 import inputs
+    w = inputs.WORKLOADS[workload]
+    b = inputs.itemsize(w["dtype"])
+    n_sample = n_sample or min(w["n"], 2**20)
+    _, x, op = _oracle_step_seconds(workload, n_sample)      # warm-up call, not timed
+    times = []
+    t_start = time.perf_counter()
+    while (time.perf_counter() - t_start < budget_s and len(times) < 200) or len(times) < 2:
+        t = time.perf_counter()
+        ring.ring_allreduce(x, op)
+        times.append(time.perf_counter() - t)
+    t_mean = statistics.mean(times)
+    return {"value": round(n_sample * b / t_mean / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"R={w['R']} ranks x n={n_sample} per rank (same recipe and seed as the workload), "
+                      f"{len(times)} oracle calls, {sum(times):.1f} s; numpy, one thread",
+            "ms_per_call": round(t_mean * 1e3, 3)}
+
+
+def run_reference_arm(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    from ring_allreduce_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    b = inputs.itemsize(w["dtype"])
+    # size the sample so warm-up + K steps take about a minute
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n_sample = 2**12
+    while n_sample * 2 <= min(w["n"], 2**22):
+        t, _, _ = _oracle_step_seconds(args.workload, n_sample * 2)
+        if t > budget:
+            break
+        n_sample *= 2
+    from oracle import ring
+    _, x, op = _oracle_step_seconds(args.workload, n_sample)
+    for _ in range(args.warmup):
+        ring.ring_allreduce(x, op)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        ring.ring_allreduce(x, op)
+        times.append(time.perf_counter() - t)
+    t_step = statistics.mean(times)
+    value = n_sample * b / t_step / 1e9
+    sample = (f"R={w['R']} ranks x n={n_sample} per rank (same recipe and seed as the workload) per step; "
+              f"numpy oracle, one thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload), "R": w["R"],
+                   "n_per_rank": w["n"], "op": w["ops"][0], "variant": "cpu oracle",
+                   "parallelism": "host, one thread"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ sweep
+
+def run_sweep(args):
+    """Latency/bandwidth sweep (R=8 fp32 sum over n, and R over 2..32 at
+    n=2^24), every variant; one JSON line per point on stdout."""
+    import torch
+    from ring_allreduce_gb300 import build, inputs
+    build.build()
+    from ring_allreduce_gb300 import binding as ra
+    peak, _ = measured_peaks()
+    points = [(8, n) for n in inputs.SWEEP_N] + [(R, 2**24) for R in inputs.SWEEP_R if R != 8]
+    for R, n in points:
+        host = inputs.generate(R, n, "f32", "normal", inputs.SWEEP_SEED)
+        _, ins = _device_ranks(torch, R, n, inputs.storage_dtype("f32"), host)
+        _, outs = _device_ranks(torch, R, n, inputs.storage_dtype("f32"))
+        line = {"sweep": "r8_f32_n" if R == 8 else "f32_R", "R": R, "n_per_rank": n}
+        for v in ("direct", "ring", "persistent"):
+            h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
+            steps = 200 if n <= 2**20 else 30
+            _, lm = _time_variant(torch, ra, h, ins, outs, steps, 10)
+            assert h.device_status()[0] == ra.Status.OK
+            h.close()
+            t = statistics.median(lm) / 1e3
+            line[v] = {"us": round(t * 1e6, 2), "algbw": round(n * 4 / t / 1e9, 2),
+                       "busbw": round(n * 4 / t / 1e9 * 2 * (R - 1) / R, 2),
+                       "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
+        print(json.dumps(line), flush=True)
+        del ins, outs
+        torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="r8_f32", choices=["r8_f32", "r8_bf16", "r16_i32", "r4_small"])
+    ap.add_argument("--n", type=int, default=None, help="override n per rank (profiling of a smaller case)")
+    ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws != args.gpus and ws > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
+    if args.impl == "reference":
+        run_reference_arm(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * ra.h -- ring AllReduce, ReduceScatter and AllGather over R ranks that are
+ * held as R buffers in the HBM of one GPU (GB300, sm_103a).
+ *
+ * What the calls compute follows the web page "Why AllReduce =
+ * ReduceScatter + AllGather -- NCCL Ring AllReduce":
+ *
+ *   section 1   every rank r holds x_r[0..n); afterwards every rank holds
+ *               S[i] = x_0[i] (+) x_1[i] (+) ... (+) x_{R-1}[i] for all i;
+ *   section 12  the n elements are cut into R chunks; here chunk k is
+ *               [k*C, min((k+1)*C, n)) with C = ceil(n/R), so the last
+ *               chunks are the short ones and may be empty;
+ *   section 4   the ring is rank 0 -> 1 -> ... -> R-1 -> 0;
+ *   section 5   ReduceScatter: in round 1 rank r sends its chunk r to r+1,
+ *               which adds its own chunk; the partial travels on, and after
+ *               R-1 rounds rank r holds the complete S of chunk (r+1) mod R
+ *               (GPU0:S1, GPU1:S2, GPU2:S3, GPU3:S0 for R=4).  Chunk k is
+ *               therefore folded in ring order x_k, x_{k+1}, ..., x_{k-1},
+ *               each hop computing  incoming (+) local;
+ *   section 6   AllGather: the complete chunks travel on for R-1 more
+ *               rounds, copied, never reduced;
+ *   sections 8, 9  the boundary step recvReduceCopySend: the last reduction
+ *               of a chunk writes it to the rank's output and is the first
+ *               AllGather send.
+ *
+ * Results are bitwise the ones of that ring for every dtype: the fold order
+ * of each element is fixed, bf16 partials are rounded to bf16
+ * (round-to-nearest-even) at every hop, as a ring carrying bf16 messages
+ * would store them, fp32 additions are single IEEE binary32 additions with
+ * no contraction and no flush to zero, int32 sums wrap.  MAX keeps the
+ * incoming partial unless the local value is strictly greater.
+ *
+ * Buffers and ownership
+ *   - The caller owns every buffer.  in[r] and out[r] (r = 0..R-1) are
+ *     device pointers to n elements, in memory of the device that was
+ *     current at ra_create, each 16-byte aligned.  The pointer arrays
+ *     themselves are host arrays of R entries, read during the call only.
+ *   - out[r] == in[r] (in place) is allowed.  Any other overlap between the
+ *     2R ranges, or between two outputs, is RA_ERR_INVALID.
+ *   - The handle owns only what it allocates at ra_create: the barrier
+ *     signal slots and a device error record.
+ *
+ * Asynchrony and errors
+ *   - Every compute call is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns once enqueued.  Host-side argument
+ *     errors return a status and enqueue nothing.
+ *   - No device wait is unbounded: the persistent kernel's barrier polls and
+ *     the AllGather kernel's copy waits give up after RA_OPT_TIMEOUT_NS, note
+ *     what they waited for in the handle's error record and return.  That
+ *     record is read by ra_get_device_status.  No kernel traps.
+ *   - ra_last_error() gives a text for the calling thread's last failure.
+ *   - Calls on one handle must be ordered (one stream, or synchronised by the
+ *     caller): the persistent variant's signal slots are per handle.
+ *
+ * Edge cases: n == 0 is a no-op returning RA_OK.  R == 1 copies in[0] to
+ * out[0].  R outside [1, 32], a NULL or misaligned pointer, an unknown dtype
+ * or op return RA_ERR_INVALID.
+ */
+#ifndef RING_ALLREDUCE_GB300_RA_H
+#define RING_ALLREDUCE_GB300_RA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ra_status {
+  RA_OK = 0,
+  RA_ERR_INVALID = 1,      /* bad argument; nothing was enqueued */
+  RA_ERR_CUDA = 2,         /* a CUDA runtime call failed (no device, launch error, ...) */
+  RA_ERR_OOM = 3,          /* device allocation of the handle's state failed */
+  RA_ERR_UNSUPPORTED = 4,  /* e.g. the persistent grid cannot be co-resident */
+  RA_ERR_TIMEOUT = 5       /* a device-side wait gave up (see ra_get_device_status) */
+} ra_status;
+
+typedef enum ra_dtype { RA_F32 = 0, RA_BF16 = 1, RA_I32 = 2 } ra_dtype;
+typedef enum ra_op { RA_SUM = 0, RA_MAX = 1 } ra_op;
+
+/* Which kernels carry out a call.  All give bitwise the same result. */
+typedef enum ra_variant {
+  RA_VARIANT_AUTO = 0,        /* currently DIRECT */
+  RA_VARIANT_DIRECT = 1,      /* one launch: every element's ring fold done in
+                                 registers; reads each input once, writes each
+                                 output once */
+  RA_VARIANT_RING = 2,        /* one launch per ring round: R-1 reduce rounds
+                                 (recvReduceSend ... recvReduceCopySend), then
+                                 R-1 AllGather rounds done with TMA bulk copies */
+  RA_VARIANT_PERSISTENT = 3   /* one cooperative launch running every round;
+                                 simulated ranks meet at a counting barrier
+                                 between rounds */
+} ra_variant;
+
+typedef enum ra_option {
+  RA_OPT_VARIANT = 1,        /* ra_variant, default RA_VARIANT_AUTO */
+  RA_OPT_TIMEOUT_NS = 2,     /* limit of every device-side wait in ns, default 1e9 */
+  RA_OPT_CTAS = 3,           /* CTAs per rank (ring, persistent) or per chunk
+                                (direct); 0 = chosen from the SM count */
+  RA_OPT_CHECK_POINTERS = 4, /* 1 (default): each call checks with
+                                cudaPointerGetAttributes that every buffer is
+                                device memory of the handle's device */
+  RA_OPT_SKIP_ARRIVAL = 5    /* failure injection for tests, persistent
+                                variant: (rank << 16) | barrier_round names a
+                                rank whose arrival at that barrier is withheld
+                                in every channel; -1 (default) = off.  The
+                                peers' waits then run out after
+                                RA_OPT_TIMEOUT_NS and the call reports
+                                RA_ERR_TIMEOUT through ra_get_device_status. */
+} ra_option;
+
+/* Device error record, filled by the first wait that gives up. */
+typedef struct ra_device_error {
+  uint32_t code;      /* 0 = none, 1 = barrier wait ran out, 2 = copy wait ran out */
+  int32_t round;      /* barrier round (0-based) or tile index */
+  int32_t rank;       /* waiting rank */
+  int32_t channel;    /* channel: the CTA index within its rank */
+  uint64_t observed;  /* signal value seen last */
+  uint64_t expected;  /* value waited for; expected - observed arrivals were missing */
+} ra_device_error;
+
+typedef struct ra_ctx* ra_handle;
+
+/* Create a handle for R ranks of n elements of `dtype`, reduced with `op`,
+ * on the current CUDA device.  Allocates the barrier signal slots (zeroed)
+ * and the error record.  *out is set only on RA_OK. */
+ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out);
+
+/* Free the handle's device state after synchronising the device.  NULL is
+ * a no-op. */
+ra_status ra_destroy(ra_handle h);
+
+/* Ring ReduceScatter (section 5 of the ring page).  On completion chunk
+ * (r+1) mod R of out[r] holds the complete S of that chunk; the other chunks
+ * of out[r] hold unspecified values (partials of the ring). */
+ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out, void* stream);
+
+/* Ring AllGather (section 6), in place: buf[r] must hold in its chunk
+ * (r+1) mod R the complete value of that chunk (the layout ra_reduce_scatter
+ * leaves); afterwards every buf[r] holds all R chunks. */
+ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream);
+
+/* Ring AllReduce (sections 4-9): out[r] = S for every r. */
+ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, void* stream);
+
+/* Host only, needs no device: the chunk plan of section 12 as read here.
+ * off[k], len[k] for k < R (arrays of R entries owned by the caller). */
+ra_status ra_chunk_plan(int R, size_t n, size_t* off, size_t* len);
+
+/* The chunk rank r holds complete after ReduceScatter: (r+1) mod R. */
+ra_status ra_owned_chunk(ra_handle h, int r, size_t* off, size_t* len);
+
+ra_status ra_set_option(ra_handle h, int key, long long value);
+ra_status ra_get_option(ra_handle h, int key, long long* value);
+
+/* Synchronise `stream`, then read the device error record into *err (may
+ * be NULL).  Returns RA_ERR_TIMEOUT when a wait gave up since the last
+ * read; the record and the handle's signal slots are then reset, so the
+ * handle can be used again. */
+ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
+
+/* Synchronise the device and copy the persistent variant's signal slots of
+ * the last launch's kind into dst (host array of cap entries), laid out
+ * [channel][barrier round][waiter rank].  With dst == NULL only the sizes
+ * are returned.  *count, *channels, *rounds get
+ * the sizes used; *calls gets how many calls of that kind ran since the
+ * slots were last reset, so every slot must equal calls * (R - 1). */
+ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
+                          int* channels, int* rounds, long long* calls);
+
+/* Text of the calling thread's last error ("" if none). */
+const char* ra_last_error(void);
+
+/* Name of a status code. */
+const char* ra_status_string(ra_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ALLREDUCE_GB300_RA_H */

@@ -1,0 +1,293 @@
+"""Thin Python binding of libra_gb300.so (include/ra.h) over ctypes.
+
+Argument marshalling only: rank buffers are torch CUDA tensors (or raw
+device addresses), their addresses go into C pointer arrays, the stream is a
+torch stream (or a raw cudaStream_t).  Every step of the collective runs in
+the library's kernels.  Importing this module loads the library and raises
+ImportError when it has not been built -- there is no fallback.
+"""
+
+import ctypes
+import enum
+import os
+
+from . import build as _build
+
+__all__ = [
+    "Status", "DType", "Op", "Variant", "Option", "DeviceError", "RAError",
+    "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
+    "ra_all_gather", "ra_allreduce", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
+    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_last_error",
+    "ra_status_string", "RingAllReduce", "EXPORTED",
+]
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID = 1
+    ERR_CUDA = 2
+    ERR_OOM = 3
+    ERR_UNSUPPORTED = 4
+    ERR_TIMEOUT = 5
+
+
+class DType(enum.IntEnum):
+    F32 = 0
+    BF16 = 1
+    I32 = 2
+
+
+class Op(enum.IntEnum):
+    SUM = 0
+    MAX = 1
+
+
+class Variant(enum.IntEnum):
+    AUTO = 0
+    DIRECT = 1
+    RING = 2
+    PERSISTENT = 3
+
+
+class Option(enum.IntEnum):
+    VARIANT = 1
+    TIMEOUT_NS = 2
+    CTAS = 3
+    CHECK_POINTERS = 4
+    SKIP_ARRIVAL = 5
+
+
+class DeviceError(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_uint32), ("round", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("channel", ctypes.c_int32), ("observed", ctypes.c_uint64), ("expected", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class RAError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = Status(status)
+        super().__init__(f"{self.status.name}: {message}")
+
+
+_P = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+_ST = ctypes.c_int
+# name -> (restype, argtypes); every function include/ra.h declares
+EXPORTED = {
+    "ra_create": (_ST, [ctypes.c_int, _SZ, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P)]),
+    "ra_destroy": (_ST, [_P]),
+    "ra_reduce_scatter": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "ra_all_gather": (_ST, [_P, ctypes.POINTER(_P), _P]),
+    "ra_allreduce": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "ra_chunk_plan": (_ST, [ctypes.c_int, _SZ, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "ra_owned_chunk": (_ST, [_P, ctypes.c_int, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "ra_set_option": (_ST, [_P, ctypes.c_int, ctypes.c_longlong]),
+    "ra_get_option": (_ST, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]),
+    "ra_get_device_status": (_ST, [_P, _P, ctypes.POINTER(DeviceError)]),
+    "ra_read_signals": (_ST, [_P, ctypes.POINTER(ctypes.c_uint64), _SZ, ctypes.POINTER(_SZ),
+                              ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                              ctypes.POINTER(ctypes.c_longlong)]),
+    "ra_last_error": (ctypes.c_char_p, []),
+    "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_LIB = None
+
+
+def library_path():
+    return _build.LIB_PATH
+
+
+def load_library(path=None):
+    """Load libra_gb300.so once and declare its C signatures."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"libra_gb300.so is not built ({path}); run "
+                          "`python -m ring_allreduce_gb300.build` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTED.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+_lib = load_library()
+
+
+def ra_last_error():
+    return _lib.ra_last_error().decode()
+
+
+def ra_status_string(status):
+    return _lib.ra_status_string(int(status)).decode()
+
+
+def _check(status):
+    if status != Status.OK:
+        raise RAError(status, ra_last_error())
+
+
+def _addr(x):
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(bufs):
+    arr = (_P * len(bufs))()
+    for i, b in enumerate(bufs):
+        arr[i] = _addr(b)
+    return arr
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def ra_create(R, n, dtype, op):
+    h = _P()
+    _check(_lib.ra_create(int(R), int(n), int(dtype), int(op), ctypes.byref(h)))
+    return h
+
+
+def ra_destroy(h):
+    _check(_lib.ra_destroy(h))
+
+
+def ra_allreduce(h, ins, outs, stream=None):
+    _check(_lib.ra_allreduce(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
+def ra_reduce_scatter(h, ins, outs, stream=None):
+    _check(_lib.ra_reduce_scatter(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
+def ra_all_gather(h, bufs, stream=None):
+    _check(_lib.ra_all_gather(h, _ptr_array(bufs), _stream(stream)))
+
+
+def ra_chunk_plan(R, n):
+    off = (_SZ * max(R, 1))()
+    ln = (_SZ * max(R, 1))()
+    _check(_lib.ra_chunk_plan(int(R), int(n), off, ln))
+    return [(off[k], ln[k]) for k in range(R)]
+
+
+def ra_owned_chunk(h, r):
+    off, ln = _SZ(), _SZ()
+    _check(_lib.ra_owned_chunk(h, int(r), ctypes.byref(off), ctypes.byref(ln)))
+    return off.value, ln.value
+
+
+def ra_set_option(h, key, value):
+    _check(_lib.ra_set_option(h, int(key), int(value)))
+
+
+def ra_get_option(h, key):
+    v = ctypes.c_longlong()
+    _check(_lib.ra_get_option(h, int(key), ctypes.byref(v)))
+    return v.value
+
+
+def ra_get_device_status(h, stream=None):
+    """Synchronise the stream and return (status, DeviceError); does not
+    raise on RA_ERR_TIMEOUT, which it reports."""
+    err = DeviceError()
+    st = _lib.ra_get_device_status(h, _stream(stream), ctypes.byref(err))
+    if st not in (Status.OK, Status.ERR_TIMEOUT):
+        _check(st)
+    return Status(st), err
+
+
+def ra_read_signals(h):
+    """Signal slots of the last persistent call's kind, as a list laid out
+    [channel][round][rank], plus (channels, rounds, calls)."""
+    count, ch, rd, calls = _SZ(), ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+    _check(_lib.ra_read_signals(h, None, 0, ctypes.byref(count), ctypes.byref(ch), ctypes.byref(rd),
+                                ctypes.byref(calls)))
+    buf = (ctypes.c_uint64 * max(count.value, 1))()
+    _check(_lib.ra_read_signals(h, buf, count.value, ctypes.byref(count), ctypes.byref(ch),
+                                ctypes.byref(rd), ctypes.byref(calls)))
+    flat = list(buf)[:count.value]
+    R = count.value // (ch.value * rd.value) if ch.value and rd.value else 0
+    nested = [[flat[(g * rd.value + t) * R:(g * rd.value + t + 1) * R] for t in range(rd.value)]
+              for g in range(ch.value)]
+    return nested, ch.value, rd.value, calls.value
+
+
+_DTYPES = {"f32": DType.F32, "bf16": DType.BF16, "i32": DType.I32}
+_OPS = {"sum": Op.SUM, "max": Op.MAX}
+
+
+class RingAllReduce:
+    """A handle for R ranks of n elements; buffers are passed per call."""
+
+    def __init__(self, R, n, dtype="f32", op="sum", variant=None):
+        self.R, self.n = int(R), int(n)
+        self.dtype = _DTYPES[dtype] if isinstance(dtype, str) else DType(dtype)
+        self.op = _OPS[op] if isinstance(op, str) else Op(op)
+        self.h = ra_create(self.R, self.n, self.dtype, self.op)
+        if variant is not None:
+            self.set_option(Option.VARIANT, Variant[variant.upper()] if isinstance(variant, str) else variant)
+
+    def _ranks(self, *lists):
+        # the C side reads exactly R pointers from each array
+        for lst in lists:
+            if len(lst) != self.R:
+                raise ValueError(f"expected {self.R} rank buffers, got {len(lst)}")
+
+    def allreduce(self, ins, outs, stream=None):
+        self._ranks(ins, outs)
+        ra_allreduce(self.h, ins, outs, stream)
+
+    def reduce_scatter(self, ins, outs, stream=None):
+        self._ranks(ins, outs)
+        ra_reduce_scatter(self.h, ins, outs, stream)
+
+    def all_gather(self, bufs, stream=None):
+        self._ranks(bufs)
+        ra_all_gather(self.h, bufs, stream)
+
+    def owned_chunk(self, r):
+        return ra_owned_chunk(self.h, r)
+
+    def set_option(self, key, value):
+        ra_set_option(self.h, key, value)
+
+    def get_option(self, key):
+        return ra_get_option(self.h, key)
+
+    def device_status(self, stream=None):
+        return ra_get_device_status(self.h, stream)
+
+    def read_signals(self):
+        return ra_read_signals(self.h)
+
+    def close(self):
+        if self.h:
+            ra_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,108 @@
+"""Build the CUDA library libra_gb300.so in-tree, for sm_103a only.
+
+``python -m ring_allreduce_gb300.build`` (or ``build()``) compiles every
+translation unit under ``csrc/`` with nvcc in parallel into ``_build/`` and
+links ``libra_gb300.so`` next to this file.  Nothing is rebuilt when the
+library is newer than every source and header and the flags are unchanged.
+Set RA_PTXAS_VERBOSE=1 to print ptxas register / spill / shared-memory use.
+"""
+
+import hashlib
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_NAME = "libra_gb300.so"
+LIB_PATH = os.path.join(HERE, LIB_NAME)
+
+SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# IEEE arithmetic throughout: no fast-math, no flush to zero, no contraction.
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-ftz=false",
+         "-prec-div=true", "-prec-sqrt=true", "-fmad=false"]
+
+
+def _nvcc():
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libra_gb300.so")
+    return cand
+
+
+def _inputs():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "ra.h"))
+    files.append(os.path.abspath(__file__))
+    return sorted(f for f in files if os.path.isfile(f))
+
+
+def kernel_source_hash():
+    """Short hash of the CUDA / C++ sources and the public header: a
+    profile summary taken on another hash describes a different kernel."""
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(INCLUDE, "ra.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _stamp(extra):
+    h = hashlib.sha256(" ".join(ARCH + FLAGS + extra).encode())
+    for f in _inputs():
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def build(force=False, verbose=None, jobs=None):
+    """Compile and link the library; returns its path."""
+    verbose = os.environ.get("RA_PTXAS_VERBOSE") == "1" if verbose is None else verbose
+    extra = ["-Xptxas", "-v"] if verbose else []
+    stamp = _stamp(extra)
+    stamp_file = os.path.join(BUILD_DIR, "stamp")
+    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+        with open(stamp_file) as f:
+            if f.read().strip() == stamp:
+                return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    nvcc = _nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
+               os.path.join(CSRC, src), "-o", obj]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, res
+
+    with ThreadPoolExecutor(max_workers=jobs or len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    failed = [(s, r) for s, _, r in results if r.returncode != 0]
+    for s, _, r in results:
+        if verbose or r.returncode != 0:
+            sys.stderr.write(f"--- {s}\n{r.stdout}{r.stderr}")
+    if failed:
+        raise RuntimeError("nvcc failed for " + ", ".join(s for s, _ in failed))
+    objs = [o for _, o, _ in results]
+    tmp = LIB_PATH + ".tmp"
+    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        sys.stderr.write(res.stdout + res.stderr)
+        raise RuntimeError("link of libra_gb300.so failed")
+    os.replace(tmp, LIB_PATH)
+    with open(stamp_file, "w") as f:
+        f.write(stamp)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,261 @@
+// ra_device.cuh -- device building blocks shared by the ring kernels:
+// the reduction applied at a ring hop, 16-byte vector I/O, the counting
+// barrier's signal operations, and the TMA bulk-copy / mbarrier primitives.
+//
+// The reduction follows "Why AllReduce = ReduceScatter + AllGather -- NCCL
+// Ring AllReduce", sections 5 and 7: the receiver computes
+// new_partial = incoming_partial (+) local_chunk, elementwise.
+//   fp32 SUM  one binary32 addition, __fadd_rn (never contracted, no FTZ);
+//   bf16 SUM  both operands widened to binary32 exactly, one binary32
+//             addition, then round-to-nearest-even to bf16: the partial is
+//             kept in bf16 at every hop, as a ring shipping bf16 would;
+//   int32 SUM two's-complement wrap;
+//   MAX       local if local > incoming, else incoming.
+//
+// The signal operations follow the counting barrier of "comm: lift the GIN
+// scale-out ceiling by making the rail barrier a counting barrier" (section
+// "Fix": every peer adds 1, the waiter moves its shadow by R-1 and polls)
+// with the 64-bit rolling comparison of the NCCL Device API GIN article
+// (section on signals and counters).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ra_internal.h"
+
+namespace ra {
+
+enum : int { kOpSum = 0, kOpMax = 1 };
+
+// Element storage types.  kVec elements make one 16-byte vector.
+struct DF32 { using T = float;    static constexpr int kVec = 4; };
+struct DBF16 { using T = uint16_t; static constexpr int kVec = 8; };
+struct DI32 { using T = int32_t;  static constexpr int kVec = 4; };
+
+// ------------------------------------------------------------ reduction
+
+__device__ __forceinline__ float bf16_widen(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ uint16_t bf16_round(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <class D, int OP> struct Op;
+
+template <> struct Op<DF32, kOpSum> {
+  static __device__ __forceinline__ float apply(float inc, float loc) { return __fadd_rn(inc, loc); }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    return __float_as_uint(__fadd_rn(__uint_as_float(inc), __uint_as_float(loc)));
+  }
+};
+
+template <> struct Op<DF32, kOpMax> {
+  static __device__ __forceinline__ float apply(float inc, float loc) { return loc > inc ? loc : inc; }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    return __uint_as_float(loc) > __uint_as_float(inc) ? loc : inc;
+  }
+};
+
+template <> struct Op<DI32, kOpSum> {
+  static __device__ __forceinline__ int32_t apply(int32_t inc, int32_t loc) {
+    return (int32_t)((uint32_t)inc + (uint32_t)loc);
+  }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) { return inc + loc; }
+};
+
+template <> struct Op<DI32, kOpMax> {
+  static __device__ __forceinline__ int32_t apply(int32_t inc, int32_t loc) { return loc > inc ? loc : inc; }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    return (int32_t)loc > (int32_t)inc ? loc : inc;
+  }
+};
+
+// bf16: one 32-bit word holds elements 2j (low half) and 2j+1 (high half).
+template <> struct Op<DBF16, kOpSum> {
+  static __device__ __forceinline__ uint16_t apply(uint16_t inc, uint16_t loc) {
+    return bf16_round(__fadd_rn(bf16_widen(inc), bf16_widen(loc)));
+  }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    float lo = __fadd_rn(__uint_as_float(inc << 16), __uint_as_float(loc << 16));
+    float hi = __fadd_rn(__uint_as_float(inc & 0xFFFF0000u), __uint_as_float(loc & 0xFFFF0000u));
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half), .y = hi
+    return *reinterpret_cast<uint32_t*>(&p);
+  }
+};
+
+template <> struct Op<DBF16, kOpMax> {
+  static __device__ __forceinline__ uint16_t apply(uint16_t inc, uint16_t loc) {
+    return bf16_widen(loc) > bf16_widen(inc) ? loc : inc;
+  }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    uint32_t lo = __uint_as_float(loc << 16) > __uint_as_float(inc << 16) ? (loc & 0xFFFFu) : (inc & 0xFFFFu);
+    uint32_t hi = __uint_as_float(loc & 0xFFFF0000u) > __uint_as_float(inc & 0xFFFF0000u)
+                      ? (loc & 0xFFFF0000u) : (inc & 0xFFFF0000u);
+    return lo | hi;
+  }
+};
+
+template <class D, int OP>
+__device__ __forceinline__ uint4 combine_vec(uint4 inc, uint4 loc) {
+  uint4 r;
+  r.x = Op<D, OP>::word(inc.x, loc.x);
+  r.y = Op<D, OP>::word(inc.y, loc.y);
+  r.z = Op<D, OP>::word(inc.z, loc.z);
+  r.w = Op<D, OP>::word(inc.w, loc.w);
+  return r;
+}
+
+// ------------------------------------------------------------ vector I/O
+// Streaming loads/stores for data touched once per launch (evict-first in
+// L2), and L2-only (.cg) accesses for data another CTA of the same launch
+// wrote or will read (the persistent kernel), which must not come from a
+// stale L1 line.
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
+__device__ __forceinline__ uint4 ld_l2(const uint4* p) { return __ldcg(p); }
+__device__ __forceinline__ void st_l2(uint4* p, uint4 v) { __stcg(p, v); }
+
+template <class T> __device__ __forceinline__ T ld_l2_scalar(const T* p);
+template <> __device__ __forceinline__ float ld_l2_scalar<float>(const float* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ int32_t ld_l2_scalar<int32_t>(const int32_t* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ uint16_t ld_l2_scalar<uint16_t>(const uint16_t* p) {
+  return __ldcg(reinterpret_cast<const unsigned short*>(p));
+}
+
+// Split [off, end) (element indices, buffers 16-byte aligned) into a scalar
+// head, whole 16-byte vectors [vb, ve) (vector indices) and a scalar tail.
+template <int V>
+struct Span {
+  int64_t off, end, vb, ve;
+  __device__ __forceinline__ Span(int64_t o, int64_t e) : off(o), end(e) {
+    vb = (o + V - 1) / V;
+    ve = e / V;
+    if (vb > ve) { vb = ve = 0; }   // no whole vector: all scalar
+  }
+  __device__ __forceinline__ bool has_vectors() const { return ve > vb; }
+  // scalar elements: [off, head_end) and [tail_begin, end)
+  __device__ __forceinline__ int64_t head_end() const { return has_vectors() ? vb * V : end; }
+  __device__ __forceinline__ int64_t tail_begin() const { return has_vectors() ? ve * V : end; }
+  __device__ __forceinline__ int64_t scalar_count() const {
+    return (head_end() - off) + (end - tail_begin());
+  }
+  // i-th scalar element (i < scalar_count())
+  __device__ __forceinline__ int64_t scalar_at(int64_t i) const {
+    int64_t h = head_end() - off;
+    return i < h ? off + i : tail_begin() + (i - h);
+  }
+};
+
+// Part `part` of `parts` of a vector range [vb, ve): contiguous, whole vectors.
+__device__ __forceinline__ void split_vectors(int64_t vb, int64_t ve, int part, int parts,
+                                              int64_t* pb, int64_t* pe) {
+  int64_t nv = ve - vb;
+  int64_t per = (nv + parts - 1) / parts;
+  int64_t b = vb + per * part;
+  int64_t e = b + per;
+  if (b > ve) b = ve;
+  if (e > ve) e = ve;
+  *pb = b;
+  *pe = e;
+}
+
+// ----------------------------------------------------- signals / barrier
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// SignalAdd: release at GPU scope, so everything this thread has ordered
+// before it (including other threads' writes it synchronised with) is
+// visible to whoever acquires the count.
+__device__ __forceinline__ void signal_add_release(uint64_t* p, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t signal_load_acquire(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t load_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Rolling comparison: observed has reached target even across wrap-around.
+__device__ __forceinline__ bool rolling_reached(uint64_t observed, uint64_t target) {
+  return (int64_t)(observed - target) >= 0;
+}
+
+// ------------------------------------------------- TMA bulk copy, mbarrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// global -> shared (this CTA), completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// shared (this CTA) -> global, tracked by bulk async-groups.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(gmem_dst), "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N committed bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every committed bulk group has completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+}  // namespace ra

@@ -1,0 +1,583 @@
+// ra_host.cpp -- host runtime behind the C ABI of include/ra.h: handles,
+// argument checks, the chunk plan, variant selection, launches and errors.
+//
+// The chunk plan is the ring page's section 12 ("Why AllReduce =
+// ReduceScatter + AllGather -- NCCL Ring AllReduce": N elements cut into k
+// chunks of about N/k), read as C = ceil(n/R), chunk k = [kC, min((k+1)C, n)).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "ra.h"
+#include "ra_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ra_status fail(ra_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+ra_status cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear a non-sticky error so the next call starts clean
+  ra_status s = RA_ERR_CUDA;
+  if (e == cudaErrorMemoryAllocation) s = RA_ERR_OOM;
+  if (e == cudaErrorCooperativeLaunchTooLarge) s = RA_ERR_UNSUPPORTED;
+  return fail(s, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t elem_bytes(ra_dtype d) { return d == RA_BF16 ? 2 : 4; }
+
+// Switch to the handle's device for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Signal slots of one kind of call (AllReduce, ReduceScatter, AllGather).
+struct SlotRegion {
+  uint64_t* d = nullptr;
+  size_t cap = 0;       // entries
+  int G = 0;            // channel count the slots were last used with
+  int rounds = 0;       // ring rounds of this kind
+  long long calls = 0;  // completed-or-enqueued calls since the last reset
+};
+
+enum Kind { kKindAllReduce = 0, kKindReduceScatter = 1, kKindAllGather = 2 };
+
+}  // namespace
+
+struct ra_ctx {
+  int R = 0;
+  size_t n = 0;
+  ra_dtype dtype = RA_F32;
+  ra_op op = RA_SUM;
+  int device = 0;
+  int num_sms = 0;
+  int persist_blocks_per_sm = 0;
+  int variant = RA_VARIANT_AUTO;
+  long long timeout_ns = 1000000000LL;
+  int ctas = 0;
+  int check_pointers = 1;
+  long long skip = -1;
+  uint64_t* d_slots = nullptr;
+  ra_device_error* d_err = nullptr;
+  SlotRegion region[3];
+  int last_kind = -1;
+};
+
+namespace {
+
+bool valid_dtype(int d) { return d == RA_F32 || d == RA_BF16 || d == RA_I32; }
+bool valid_op(int o) { return o == RA_SUM || o == RA_MAX; }
+
+ra::Plan make_plan(int R, size_t n) {
+  ra::Plan p;
+  p.n = (int64_t)n;
+  p.C = (int64_t)((n + (size_t)R - 1) / (size_t)R);
+  return p;
+}
+
+bool overlap(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + bytes && y < x + bytes;
+}
+
+ra_status check_device_pointer(const ra_ctx* h, const void* p, const char* name, int r) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_INVALID, "%s[%d]=%p: not a CUDA pointer (%s)", name, r, p, cudaGetErrorName(e));
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return fail(RA_ERR_INVALID, "%s[%d]=%p: not device memory", name, r, p);
+  if (at.type == cudaMemoryTypeDevice && at.device != h->device)
+    return fail(RA_ERR_INVALID, "%s[%d]=%p: memory of device %d, handle is on device %d", name, r, p,
+                at.device, h->device);
+  return RA_OK;
+}
+
+// in may equal out (then only `out` is checked); in == nullptr means an
+// in-place AllGather over out.
+ra_status check_buffers(const ra_ctx* h, const void* const* in, void* const* out) {
+  const int R = h->R;
+  const size_t bytes = h->n * elem_bytes(h->dtype);
+  if (!out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  for (int r = 0; r < R; ++r) {
+    if (in && !in[r]) return fail(RA_ERR_INVALID, "in[%d] is NULL", r);
+    if (!out[r]) return fail(RA_ERR_INVALID, "%s[%d] is NULL", in ? "out" : "buf", r);
+    if (in && ((uintptr_t)in[r] & 15u)) return fail(RA_ERR_INVALID, "in[%d]=%p is not 16-byte aligned", r, in[r]);
+    if ((uintptr_t)out[r] & 15u)
+      return fail(RA_ERR_INVALID, "%s[%d]=%p is not 16-byte aligned", in ? "out" : "buf", r, out[r]);
+  }
+  if (bytes == 0) return RA_OK;
+  for (int r = 0; r < R; ++r) {
+    for (int q = 0; q < R; ++q) {
+      if (q != r && overlap(out[r], out[q], bytes))
+        return fail(RA_ERR_INVALID, "output buffers %d and %d overlap", r, q);
+      if (in) {
+        const bool same = (q == r) && (in[q] == out[r]);
+        if (!same && overlap(out[r], in[q], bytes))
+          return fail(RA_ERR_INVALID, "out[%d] overlaps in[%d] (only out[r] == in[r] is allowed)", r, q);
+      }
+    }
+  }
+  if (h->check_pointers) {
+    for (int r = 0; r < R; ++r) {
+      if (in && in[r] != out[r]) {
+        ra_status s = check_device_pointer(h, in[r], "in", r);
+        if (s != RA_OK) return s;
+      }
+      ra_status s = check_device_pointer(h, out[r], in ? "out" : "buf", r);
+      if (s != RA_OK) return s;
+    }
+  }
+  return RA_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int vec_elems(ra_dtype d) { return d == RA_BF16 ? 8 : 4; }
+
+int direct_ctas_per_chunk(const ra_ctx* h, const ra::Plan& pl) {
+  if (h->ctas > 0) return h->ctas;
+  const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
+  const int64_t need = ceil_div(vecs, ra::kDirectThreads);
+  const int64_t target = ceil_div((int64_t)h->num_sms * 8, h->R);
+  int64_t c = need < target ? need : target;
+  return (int)(c < 1 ? 1 : c);
+}
+
+int round_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
+  if (h->ctas > 0) return h->ctas;
+  const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
+  const int64_t need = ceil_div(vecs, ra::kRoundThreads);
+  const int64_t target = ceil_div((int64_t)h->num_sms * 8, h->R);
+  int64_t c = need < target ? need : target;
+  return (int)(c < 1 ? 1 : c);
+}
+
+int copy_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
+  if (h->ctas > 0) return h->ctas;
+  const int64_t tiles = ceil_div(pl.C * (int64_t)elem_bytes(h->dtype), 16384) + 1;
+  const int64_t target = ceil_div((int64_t)h->num_sms * 3, h->R);
+  int64_t c = tiles < target ? tiles : target;
+  return (int)(c < 1 ? 1 : c);
+}
+
+int persistent_channels(const ra_ctx* h, const ra::Plan& pl) {
+  const int cap = h->persist_blocks_per_sm * h->num_sms / h->R;
+  int G;
+  if (h->ctas > 0) {
+    G = h->ctas;
+  } else {
+    const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
+    const int64_t need = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
+    G = (int)(need < cap ? need : cap);
+  }
+  if (G < 1) G = 1;
+  return G;
+}
+
+ra::Ptrs make_ptrs(const ra_ctx* h, const void* const* in, void* const* out) {
+  ra::Ptrs p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < h->R; ++r) {
+    p.in[r] = in ? in[r] : out[r];
+    p.out[r] = out[r];
+  }
+  return p;
+}
+
+ra_status run_direct(ra_ctx* h, int mode, const void* const* in, void* const* out, cudaStream_t st) {
+  ra::DirectArgs a;
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  cudaError_t e = ra::launch_direct(h->dtype, h->op, a, direct_ctas_per_chunk(h, a.plan), st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "direct kernel launch");
+}
+
+ra_status run_ring_reduce(ra_ctx* h, const void* const* in, void* const* out, cudaStream_t st) {
+  ra::RoundArgs a;
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  const int ctas = round_ctas_per_rank(h, a.plan);
+  for (int s = 1; s < h->R; ++s) {
+    a.s = s;
+    cudaError_t e = ra::launch_rs_round(h->dtype, h->op, a, ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce round launch");
+  }
+  return RA_OK;
+}
+
+ra_status run_ring_gather(ra_ctx* h, void* const* buf, cudaStream_t st) {
+  ra::CopyArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < h->R; ++r) a.buf[r] = buf[r];
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.elem_bytes = (int)elem_bytes(h->dtype);
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  const int ctas = copy_ctas_per_rank(h, a.plan);
+  for (int s = 1; s < h->R; ++s) {
+    a.s = s;
+    cudaError_t e = ra::launch_ag_round(a, ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e, "AllGather round launch");
+  }
+  return RA_OK;
+}
+
+ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
+                         cudaStream_t st) {
+  SlotRegion& reg = h->region[kind];
+  ra::PersistArgs a;
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.rounds = reg.rounds;
+  a.G = persistent_channels(h, a.plan);
+  const int cap = h->persist_blocks_per_sm * h->num_sms;
+  if ((long long)a.G * h->R > cap)
+    return fail(RA_ERR_UNSUPPORTED, "persistent grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
+  const size_t need = (size_t)a.G * (size_t)(reg.rounds > 1 ? reg.rounds - 1 : 0) * (size_t)h->R;
+  if (need > reg.cap) return fail(RA_ERR_UNSUPPORTED, "too many channels for the signal slots");
+  if (reg.G != a.G) {
+    cudaError_t e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
+    reg.G = a.G;
+    reg.calls = 0;
+  }
+  a.slots = reg.d;
+  a.epoch = (uint64_t)(reg.calls + 1);
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
+  a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
+  cudaError_t e = ra::launch_persistent(h->dtype, h->op, a, ra::kPersistThreads, st);
+  if (e != cudaSuccess) return cuda_fail(e, "persistent kernel launch");
+  reg.calls += 1;
+  h->last_kind = kind;
+  return RA_OK;
+}
+
+ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(h->d_err, 0, sizeof(ra_device_error), st);
+  if (e == cudaSuccess && h->d_slots) {
+    size_t total = 0;
+    for (auto& r : h->region) total += r.cap;
+    e = cudaMemsetAsync(h->d_slots, 0, total * sizeof(uint64_t), st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "device state reset");
+  for (auto& r : h->region) r.calls = 0;
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_chunk_plan(int R, size_t n, size_t* off, size_t* len) {
+  if (R < 1 || R > ra::kMaxRanks) return fail(RA_ERR_INVALID, "R=%d outside [1, %d]", R, ra::kMaxRanks);
+  if (!off || !len) return fail(RA_ERR_INVALID, "NULL output array");
+  const size_t C = (n + (size_t)R - 1) / (size_t)R;
+  for (int k = 0; k < R; ++k) {
+    size_t lo = (size_t)k * C;
+    size_t hi = lo + C;
+    if (lo > n) lo = n;
+    if (hi > n) hi = n;
+    off[k] = lo;
+    len[k] = hi - lo;
+  }
+  return RA_OK;
+}
+
+ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
+  if (!out) return fail(RA_ERR_INVALID, "NULL handle pointer");
+  if (R < 1 || R > ra::kMaxRanks) return fail(RA_ERR_INVALID, "R=%d outside [1, %d]", R, ra::kMaxRanks);
+  if (!valid_dtype(dtype)) return fail(RA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (!valid_op(op)) return fail(RA_ERR_INVALID, "unknown op %d", (int)op);
+  if (n > ((size_t)1 << 40)) return fail(RA_ERR_INVALID, "n=%zu too large", n);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  int coop = 0;
+  e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  int bps = 0;
+  e = ra::persistent_blocks_per_sm(dtype, op, ra::kPersistThreads, &bps);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  e = ra::prepare_ag_round();
+  if (e != cudaSuccess) return cuda_fail(e, "AllGather kernel set-up");
+
+  ra_ctx* h = new (std::nothrow) ra_ctx();
+  if (!h) return fail(RA_ERR_OOM, "host allocation failed");
+  h->R = R;
+  h->n = n;
+  h->dtype = dtype;
+  h->op = op;
+  h->device = dev;
+  h->num_sms = sms;
+  h->persist_blocks_per_sm = coop ? bps : 0;
+
+  // signal slots: per kind, the most channels that can be co-resident x
+  // barrier rounds x waiters
+  const size_t gmax = (size_t)(bps > 0 ? bps : 1) * (size_t)sms / (size_t)R + 1;
+  const int rounds[3] = {2 * (R - 1), R - 1, R - 1};
+  size_t total = 0;
+  for (int k = 0; k < 3; ++k) {
+    h->region[k].rounds = rounds[k];
+    h->region[k].cap = gmax * (size_t)(rounds[k] > 1 ? rounds[k] - 1 : 0) * (size_t)R;
+    total += h->region[k].cap;
+  }
+  if (total > 0) {
+    e = cudaMalloc(&h->d_slots, total * sizeof(uint64_t));
+    if (e != cudaSuccess) {
+      delete h;
+      return cuda_fail(e, "signal slot allocation");
+    }
+    e = cudaMemset(h->d_slots, 0, total * sizeof(uint64_t));
+    if (e != cudaSuccess) {
+      cudaFree(h->d_slots);
+      delete h;
+      return cuda_fail(e, "signal slot init");
+    }
+    size_t o = 0;
+    for (auto& r : h->region) {
+      r.d = h->d_slots + o;
+      o += r.cap;
+    }
+  }
+  e = cudaMalloc(&h->d_err, sizeof(ra_device_error));
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(ra_device_error));
+  if (e != cudaSuccess) {
+    if (h->d_slots) cudaFree(h->d_slots);
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return cuda_fail(e, "error record allocation");
+  }
+  *out = h;
+  return RA_OK;
+}
+
+ra_status ra_destroy(ra_handle h) {
+  if (!h) return RA_OK;
+  DeviceGuard g(h->device);
+  ra_status s = RA_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) s = cuda_fail(e, "synchronise before destroy");
+  if (h->d_slots) cudaFree(h->d_slots);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+  return s;
+}
+
+ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!in || !out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  ra_status s = check_buffers(h, in, out);
+  if (s != RA_OK) return s;
+  if (h->n == 0) return RA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->R == 1) {
+    if (in[0] == out[0]) return RA_OK;
+    return run_direct(h, ra::kModeAllReduce, in, out, st);
+  }
+  switch (h->variant) {
+    case RA_VARIANT_RING:
+      s = run_ring_reduce(h, in, out, st);
+      return s != RA_OK ? s : run_ring_gather(h, out, st);
+    case RA_VARIANT_PERSISTENT:
+      return run_persistent(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
+    default:
+      return run_direct(h, ra::kModeAllReduce, in, out, st);
+  }
+}
+
+ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!in || !out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  ra_status s = check_buffers(h, in, out);
+  if (s != RA_OK) return s;
+  if (h->n == 0) return RA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->R == 1) {
+    if (in[0] == out[0]) return RA_OK;
+    return run_direct(h, ra::kModeAllReduce, in, out, st);
+  }
+  switch (h->variant) {
+    case RA_VARIANT_RING:
+      return run_ring_reduce(h, in, out, st);
+    case RA_VARIANT_PERSISTENT:
+      return run_persistent(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
+    default:
+      return run_direct(h, ra::kModeReduceScatter, in, out, st);
+  }
+}
+
+ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!buf) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  ra_status s = check_buffers(h, nullptr, buf);
+  if (s != RA_OK) return s;
+  if (h->n == 0 || h->R == 1) return RA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (h->variant) {
+    case RA_VARIANT_RING:
+      return run_ring_gather(h, buf, st);
+    case RA_VARIANT_PERSISTENT:
+      return run_persistent(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
+    default:
+      return run_direct(h, ra::kModeAllGather, buf, buf, st);
+  }
+}
+
+ra_status ra_owned_chunk(ra_handle h, int r, size_t* off, size_t* len) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (r < 0 || r >= h->R) return fail(RA_ERR_INVALID, "rank %d outside [0, %d)", r, h->R);
+  if (!off || !len) return fail(RA_ERR_INVALID, "NULL output pointer");
+  size_t o[ra::kMaxRanks], l[ra::kMaxRanks];
+  ra_chunk_plan(h->R, h->n, o, l);
+  const int k = (r + 1) % h->R;
+  *off = o[k];
+  *len = l[k];
+  return RA_OK;
+}
+
+ra_status ra_set_option(ra_handle h, int key, long long value) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  switch (key) {
+    case RA_OPT_VARIANT:
+      if (value < RA_VARIANT_AUTO || value > RA_VARIANT_PERSISTENT)
+        return fail(RA_ERR_INVALID, "unknown variant %lld", value);
+      if (value == RA_VARIANT_PERSISTENT && h->persist_blocks_per_sm == 0)
+        return fail(RA_ERR_UNSUPPORTED, "device has no cooperative launch");
+      h->variant = (int)value;
+      return RA_OK;
+    case RA_OPT_TIMEOUT_NS:
+      if (value < 1000) return fail(RA_ERR_INVALID, "timeout %lld ns below 1 us", value);
+      h->timeout_ns = value;
+      return RA_OK;
+    case RA_OPT_CTAS:
+      if (value < 0 || value > 65535) return fail(RA_ERR_INVALID, "CTA count %lld outside [0, 65535]", value);
+      h->ctas = (int)value;
+      return RA_OK;
+    case RA_OPT_CHECK_POINTERS:
+      h->check_pointers = value != 0;
+      return RA_OK;
+    case RA_OPT_SKIP_ARRIVAL:
+      if (value < -1 || (value >= 0 && ((value >> 16) >= h->R))) return fail(RA_ERR_INVALID, "bad skip %lld", value);
+      h->skip = value;
+      return RA_OK;
+    default:
+      return fail(RA_ERR_INVALID, "unknown option %d", key);
+  }
+}
+
+ra_status ra_get_option(ra_handle h, int key, long long* value) {
+  if (!h || !value) return fail(RA_ERR_INVALID, "NULL argument");
+  switch (key) {
+    case RA_OPT_VARIANT: *value = h->variant; return RA_OK;
+    case RA_OPT_TIMEOUT_NS: *value = h->timeout_ns; return RA_OK;
+    case RA_OPT_CTAS: *value = h->ctas; return RA_OK;
+    case RA_OPT_CHECK_POINTERS: *value = h->check_pointers; return RA_OK;
+    case RA_OPT_SKIP_ARRIVAL: *value = h->skip; return RA_OK;
+    default: return fail(RA_ERR_INVALID, "unknown option %d", key);
+  }
+}
+
+ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  DeviceGuard g(h->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  ra_device_error rec;
+  e = cudaMemcpy(&rec, h->d_err, sizeof(rec), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error record read");
+  if (err) *err = rec;
+  if (rec.code == 0) return RA_OK;
+  ra_status s = reset_device_state(h, st);
+  if (s != RA_OK) return s;
+  return fail(RA_ERR_TIMEOUT,
+              "device wait gave up: %s, round %d, rank %d, channel %d, observed %llu of %llu (%llu missing)",
+              rec.code == 1 ? "barrier" : "bulk copy", rec.round, rec.rank, rec.channel,
+              (unsigned long long)rec.observed, (unsigned long long)rec.expected,
+              (unsigned long long)(rec.expected - rec.observed));
+}
+
+ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count, int* channels, int* rounds,
+                          long long* calls) {
+  if (!h || !count) return fail(RA_ERR_INVALID, "NULL argument");
+  DeviceGuard g(h->device);
+  if (h->last_kind < 0) {
+    *count = 0;
+    if (channels) *channels = 0;
+    if (rounds) *rounds = 0;
+    if (calls) *calls = 0;
+    return RA_OK;
+  }
+  const SlotRegion& reg = h->region[h->last_kind];
+  const int br = reg.rounds > 1 ? reg.rounds - 1 : 0;
+  const size_t need = (size_t)reg.G * (size_t)br * (size_t)h->R;
+  *count = need;
+  if (channels) *channels = reg.G;
+  if (rounds) *rounds = br;
+  if (calls) *calls = reg.calls;
+  if (!dst || need == 0) return RA_OK;  // sizes only
+  if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess && need) e = cudaMemcpy(dst, reg.d, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "signal read");
+  return RA_OK;
+}
+
+const char* ra_last_error(void) { return g_last_error.c_str(); }
+
+const char* ra_status_string(ra_status s) {
+  switch (s) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID: return "RA_ERR_INVALID";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_OOM: return "RA_ERR_OOM";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+    default: return "RA_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// ra_internal.h -- what the host runtime (ra_host.cpp) and the kernel
+// translation units share: kernel argument blocks and launch functions.
+// Nothing here is part of the public C ABI (include/ra.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra.h"
+
+namespace ra {
+
+constexpr int kMaxRanks = 32;
+
+// Which collective a launch carries out.
+enum Mode : int { kModeAllReduce = 0, kModeReduceScatter = 1, kModeAllGather = 2 };
+
+// Rank buffers, copied by value into the kernel parameters.
+struct Ptrs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+};
+
+// Chunk k of a rank buffer is [k*C, min((k+1)*C, n)).
+struct Plan {
+  int64_t n;
+  int64_t C;
+};
+
+// Direct variant: one launch, grid.y = chunk.
+struct DirectArgs {
+  Ptrs p;
+  Plan plan;
+  int R;
+  int mode;
+};
+
+// Ring variant, one reduce round s (1..R-1), grid.y = rank.
+struct RoundArgs {
+  Ptrs p;
+  Plan plan;
+  int R;
+  int s;
+};
+
+// Ring variant, one AllGather round s (1..R-1) on out[]; grid.y = rank.
+struct CopyArgs {
+  void* buf[kMaxRanks];
+  Plan plan;
+  int R;
+  int s;
+  int elem_bytes;
+  int64_t timeout_ns;
+  ra_device_error* err;
+};
+
+// Persistent variant: one cooperative launch of R*G CTAs (G channels).
+struct PersistArgs {
+  Ptrs p;
+  Plan plan;
+  int R;
+  int G;
+  int mode;
+  int rounds;           // ring rounds this call runs
+  uint64_t* slots;      // [G][rounds-1][R] signal slots of this call's kind
+  uint64_t epoch;       // calls of this kind since the slots were zeroed, this one included
+  int64_t timeout_ns;
+  ra_device_error* err;
+  int skip_rank;        // failure injection: rank withholding one arrival, -1 = none
+  int skip_round;
+};
+
+cudaError_t launch_direct(int dtype, int op, const DirectArgs& a, int ctas_per_chunk, cudaStream_t st);
+cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st);
+cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st);
+// Per-device set-up of the AllGather kernel (its shared-memory opt-in);
+// call with the device current before its first launch there.
+cudaError_t prepare_ag_round();
+cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
+// Co-resident CTAs per SM of the persistent kernel for `threads` threads.
+cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks);
+
+constexpr int kDirectThreads = 256;
+constexpr int kRoundThreads = 256;
+constexpr int kCopyThreads = 32;
+constexpr int kPersistThreads = 512;
+
+}  // namespace ra

@@ -1,0 +1,187 @@
+// ra_persistent.cu -- the persistent variant: every ring round in one
+// cooperative launch, simulated ranks meeting at a counting barrier
+// between rounds.
+//
+// Rounds ("Why AllReduce = ReduceScatter + AllGather -- NCCL Ring
+// AllReduce", sections 5 and 6): ReduceScatter round s computes, on every
+// rank r, P_r[c] = P_{r-1}[c] (+) x_r[c] with c = (r - s) mod R; AllGather
+// round s copies chunk (r + 1 - s) mod R from rank r-1.  The partial a rank
+// passes on is what it stored in its output buffer.
+//
+// Ranks and channels: the launch has R x G CTAs.  CTA (r, g) is rank r's
+// channel g: in every round it handles the g-th slice of its rank's chunk.
+// Slices are cut from the chunk alone, so channel g of rank r only ever
+// reads what channel g of rank r-1 wrote: each channel is a ring of its own,
+// as NCCL runs several rings side by side.
+//
+// Barrier between rounds ("comm: lift the GIN scale-out ceiling by making
+// the rail barrier a counting barrier", section "Fix"): after a round each
+// CTA adds 1 to one signal of every peer of its channel (release, so its
+// round's stores are visible with the count), then polls its own signal
+// (acquire) until the shadow target is reached, and a __syncthreads lets
+// the rest of the CTA on.  The page's section "Scoped to the rail team,
+// deliberately" explains that a single counter reused across rounds lets a
+// peer a round ahead stand in for a late one; here every (channel, round,
+// waiter) has its own 64-bit slot, so a count comes only from its round.
+// Slots are never cleared between calls: the k-th call on a slot array
+// waits for k * (R - 1), compared in 64-bit rolling order (NCCL Device API
+// GIN article, signals and counters).
+//
+// No wait is unbounded: a poll that passes the time limit records
+// (round, rank, channel, observed, expected) in the handle's error record and
+// the CTA returns; every other CTA sees the record at its next poll and
+// returns as well.  Data produced by another CTA of the launch is read
+// through L2 (ld.global.cg), never from a possibly stale L1 line.
+#include "ra_device.cuh"
+
+namespace ra {
+
+// One counting-barrier round.  Returns false when this CTA must stop.
+__device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int abort = 0;
+    uint64_t* row = a.slots + ((int64_t)g * (a.rounds - 1) + t) * a.R;
+    __threadfence();
+    if (!(r == a.skip_rank && t == a.skip_round)) {
+      for (int q = 0; q < a.R; ++q)
+        if (q != r) signal_add_release(row + q, 1);
+    }
+    const uint64_t target = a.epoch * (uint64_t)(a.R - 1);
+    const uint64_t t0 = globaltimer_ns();
+    // an iteration bound on top of the clock: every poll costs far more than 1 ns
+    const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+    uint64_t seen = 0;
+    for (uint64_t it = 0;; ++it) {
+      seen = signal_load_acquire(row + r);
+      if (rolling_reached(seen, target)) break;
+      if (load_relaxed_u32(&a.err->code) != 0u) { abort = 1; break; }
+      if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
+        if (atomicCAS(&a.err->code, 0u, 1u) == 0u) {
+          a.err->round = t;
+          a.err->rank = r;
+          a.err->channel = g;
+          a.err->observed = seen;
+          a.err->expected = target;
+          __threadfence();
+        }
+        abort = 1;
+        break;
+      }
+      if (it > 32) __nanosleep(100);
+    }
+    *s_abort = abort;
+  }
+  __syncthreads();
+  return *s_abort == 0;
+}
+
+template <class D, int OP>
+__device__ __forceinline__ void reduce_slice(const typename D::T* inc, const typename D::T* loc,
+                                             typename D::T* dst, int64_t off, int64_t end, int g, int G) {
+  constexpr int V = D::kVec;
+  const Span<V> sp(off, end);
+  int64_t pb, pe;
+  split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
+  for (int64_t v = pb + threadIdx.x; v < pe; v += blockDim.x) {
+    const uint4 x = ld_l2(reinterpret_cast<const uint4*>(inc) + v);
+    const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
+    st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+  }
+  if (g == 0) {
+    const int64_t ns = sp.scalar_count();
+    for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
+      const int64_t i = sp.scalar_at(t);
+      dst[i] = Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i));
+    }
+  }
+}
+
+template <class D>
+__device__ __forceinline__ void copy_slice(const typename D::T* src, typename D::T* dst, int64_t off,
+                                           int64_t end, int g, int G) {
+  constexpr int V = D::kVec;
+  const Span<V> sp(off, end);
+  int64_t pb, pe;
+  split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
+  for (int64_t v = pb + threadIdx.x; v < pe; v += blockDim.x)
+    st_l2(reinterpret_cast<uint4*>(dst) + v, ld_l2(reinterpret_cast<const uint4*>(src) + v));
+  if (g == 0) {
+    const int64_t ns = sp.scalar_count();
+    for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
+      const int64_t i = sp.scalar_at(t);
+      dst[i] = ld_l2_scalar(src + i);
+    }
+  }
+}
+
+template <class D, int OP>
+__global__ void __launch_bounds__(kPersistThreads)
+persistent_kernel(const PersistArgs a) {
+  using T = typename D::T;
+  __shared__ int s_abort;
+  const int R = a.R, G = a.G;
+  const int r = blockIdx.x % R;
+  const int g = blockIdx.x / R;
+  const int p = (r == 0) ? R - 1 : r - 1;
+  for (int t = 0; t < a.rounds; ++t) {
+    bool reduce;
+    int s;
+    if (a.mode == kModeAllGather) {
+      reduce = false;
+      s = t + 1;
+    } else if (t < R - 1) {
+      reduce = true;
+      s = t + 1;
+    } else {
+      reduce = false;
+      s = t - (R - 1) + 1;
+    }
+    int c = reduce ? (r - s) : (r + 1 - s);
+    c %= R;
+    if (c < 0) c += R;
+    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
+    const int64_t end = min(off + a.plan.C, a.plan.n);
+    if (off < end) {
+      if (reduce) {
+        const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
+        reduce_slice<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), off, end, g, G);
+      } else {
+        copy_slice<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), off, end, g, G);
+      }
+    }
+    if (t + 1 < a.rounds && !counting_barrier(a, g, t, r, &s_abort)) return;
+  }
+}
+
+template <class D, int OP>
+static const void* persistent_fn() {
+  return reinterpret_cast<const void*>(&persistent_kernel<D, OP>);
+}
+
+static const void* persistent_select(int dtype, int op) {
+  switch (dtype * 2 + op) {
+    case RA_F32 * 2 + RA_SUM: return persistent_fn<DF32, kOpSum>();
+    case RA_F32 * 2 + RA_MAX: return persistent_fn<DF32, kOpMax>();
+    case RA_BF16 * 2 + RA_SUM: return persistent_fn<DBF16, kOpSum>();
+    case RA_BF16 * 2 + RA_MAX: return persistent_fn<DBF16, kOpMax>();
+    case RA_I32 * 2 + RA_SUM: return persistent_fn<DI32, kOpSum>();
+    case RA_I32 * 2 + RA_MAX: return persistent_fn<DI32, kOpMax>();
+    default: return nullptr;
+  }
+}
+
+cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
+  const void* fn = persistent_select(dtype, op);
+  if (!fn) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
+}
+
+cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
+  const void* fn = persistent_select(dtype, op);
+  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<PersistArgs*>(&a)};
+  return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
+}
+
+}  // namespace ra

@@ -1,0 +1,181 @@
+// ra_round.cu -- the ring variant: one launch per ring round.
+//
+// "Why AllReduce = ReduceScatter + AllGather -- NCCL Ring AllReduce":
+//   section 5, ReduceScatter round s (1..R-1): every rank r at once receives
+//     from r-1 the partial of chunk c = (r - s) mod R and adds its own copy:
+//       P_r[c] = P_{r-1}[c] (+) x_r[c],   P_{r-1}[c] = x_{r-1}[c] when s = 1.
+//     The partial a rank "sends" is what it stored in its output buffer; its
+//     successor reads it there in the next round.  After round R-1, chunk
+//     (r+1) mod R of out[r] is complete -- the final reduce of section 9's
+//     recvReduceCopySend already lands in the rank's output, and the
+//     AllGather's first send reads it from there, so no copy pass is needed.
+//   section 6, AllGather round s (1..R-1): rank r copies chunk
+//     c = (r + 1 - s) mod R from out[r-1] into out[r]: receive + copy, no
+//     reduce.  The copy runs on the Tensor Memory Accelerator: 16-byte
+//     aligned tiles go global -> shared -> global with cp.async.bulk, a few
+//     tiles in flight per CTA; the unaligned head and tail bytes of a chunk
+//     are copied by the CTA's threads.
+// One launch covers all R ranks of a round (grid.y = rank); the stream
+// order between launches is the round order of the ring.
+#include "ra_device.cuh"
+
+namespace ra {
+
+// ------------------------------------------------------------ reduce round
+
+template <class D, int OP>
+__global__ void __launch_bounds__(kRoundThreads)
+rs_round_kernel(const RoundArgs a) {
+  using T = typename D::T;
+  constexpr int V = D::kVec;
+  const int R = a.R, s = a.s, r = blockIdx.y;
+  int c = r - s;
+  if (c < 0) c += R;
+  const int p = (r == 0) ? R - 1 : r - 1;
+  const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
+  const int64_t end = min(off + a.plan.C, a.plan.n);
+  if (off >= end) return;
+  const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
+  const T* loc = static_cast<const T*>(a.p.in[r]);
+  T* dst = static_cast<T*>(a.p.out[r]);
+  const Span<V> sp(off, end);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t v = sp.vb + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < sp.ve; v += stride) {
+    const uint4 x = reinterpret_cast<const uint4*>(inc)[v];
+    const uint4 y = ld_stream(reinterpret_cast<const uint4*>(loc) + v);
+    // plain store: the next round reads this partial, possibly from L2
+    reinterpret_cast<uint4*>(dst)[v] = combine_vec<D, OP>(x, y);
+  }
+  if (blockIdx.x == 0) {
+    const int64_t ns = sp.scalar_count();
+    for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
+      const int64_t i = sp.scalar_at(t);
+      dst[i] = Op<D, OP>::apply(inc[i], loc[i]);
+    }
+  }
+}
+
+cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st) {
+  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
+  dim3 grid(ctas_per_rank, a.R);
+  switch (dtype * 2 + op) {
+    case RA_F32 * 2 + RA_SUM: rs_round_kernel<DF32, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
+    case RA_F32 * 2 + RA_MAX: rs_round_kernel<DF32, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
+    case RA_BF16 * 2 + RA_SUM: rs_round_kernel<DBF16, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
+    case RA_BF16 * 2 + RA_MAX: rs_round_kernel<DBF16, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
+    case RA_I32 * 2 + RA_SUM: rs_round_kernel<DI32, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
+    case RA_I32 * 2 + RA_MAX: rs_round_kernel<DI32, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------- AllGather round, TMA
+
+constexpr int kTileBytes = 16384;
+constexpr int kStages = 4;
+constexpr int kCopySmem = kTileBytes * kStages;
+
+// Bounded wait for a bulk load; false when the limit ran out.
+__device__ __forceinline__ bool wait_tile(uint64_t* bar, uint32_t parity, int64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((int64_t)(globaltimer_ns() - t0) > timeout_ns) return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kCopyThreads)
+ag_round_kernel(const CopyArgs a) {
+  extern __shared__ __align__(128) uint8_t tiles[];
+  __shared__ __align__(8) uint64_t bars[kStages];
+  const int R = a.R, s = a.s, r = blockIdx.y;
+  int c = (r + 1 - s) % R;
+  if (c < 0) c += R;
+  const int p = (r == 0) ? R - 1 : r - 1;
+  const int64_t eb = a.elem_bytes;
+  const int64_t b0 = min((int64_t)c * a.plan.C, a.plan.n) * eb;
+  const int64_t b1 = min((int64_t)c * a.plan.C + a.plan.C, a.plan.n) * eb;
+  if (b0 >= b1) return;
+  const uint8_t* src = static_cast<const uint8_t*>(a.buf[p]);
+  uint8_t* dst = static_cast<uint8_t*>(a.buf[r]);
+
+  // 16-byte aligned body [a0, a1); the rest is copied byte by byte
+  int64_t a0 = (b0 + 15) & ~int64_t(15);
+  int64_t a1 = b1 & ~int64_t(15);
+  if (a0 >= a1) { a0 = b1; a1 = b1; }
+  if (blockIdx.x == 0) {
+    for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) dst[i] = src[i];
+    for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) dst[i] = src[i];
+  }
+  const int64_t body = a1 - a0;
+  const int64_t ntiles = (body + kTileBytes - 1) / kTileBytes;
+  if ((int64_t)blockIdx.x >= ntiles || threadIdx.x != 0) return;
+  const int count = (int)((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  auto tile_of = [&](int i) -> int64_t { return blockIdx.x + (int64_t)i * gridDim.x; };
+  auto bytes_of = [&](int64_t t) -> uint32_t {
+    int64_t b = body - t * kTileBytes;
+    return (uint32_t)(b < kTileBytes ? b : kTileBytes);
+  };
+  auto issue_load = [&](int i) {
+    const int st = i % kStages;
+    const int64_t t = tile_of(i);
+    const uint32_t nb = bytes_of(t);
+    mbar_arrive_expect_tx(&bars[st], nb);
+    bulk_load(tiles + st * kTileBytes, src + a0 + t * kTileBytes, nb, &bars[st]);
+  };
+
+  for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+  fence_mbar_init();
+  const int pro = count < kStages ? count : kStages;
+  for (int i = 0; i < pro; ++i) issue_load(i);
+  int issued = pro;   // loads issued so far
+  bool ok = true;
+  for (int i = 0; i < count; ++i) {
+    const int st = i % kStages;
+    if (!wait_tile(&bars[st], (uint32_t)((i / kStages) & 1), a.timeout_ns)) {
+      if (atomicCAS(&a.err->code, 0u, 2u) == 0u) {
+        a.err->round = s;
+        a.err->rank = r;
+        a.err->channel = blockIdx.x;
+        a.err->observed = (uint64_t)i;
+        a.err->expected = (uint64_t)count;
+        __threadfence();
+      }
+      ok = false;
+      break;
+    }
+    fence_proxy_async_smem();
+    const int64_t t = tile_of(i);
+    bulk_store(dst + a0 + t * kTileBytes, tiles + st * kTileBytes, bytes_of(t));
+    bulk_commit();
+    // refill the stage of tile i-1 once its store has read shared memory
+    if (i >= 1 && issued < count) {
+      bulk_wait_read<1>();
+      issue_load(issued);
+      ++issued;
+    }
+  }
+  if (!ok) {
+    // drain: give every load that may still be in flight one more bounded wait
+    for (int i = 0; i < issued; ++i) {
+      const int st = i % kStages;
+      wait_tile(&bars[st], (uint32_t)((i / kStages) & 1), a.timeout_ns);
+    }
+  }
+  bulk_wait_all();
+}
+
+cudaError_t prepare_ag_round() {
+  return cudaFuncSetAttribute(ag_round_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCopySmem);
+}
+
+cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st) {
+  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
+  dim3 grid(ctas_per_rank, a.R);
+  ag_round_kernel<<<grid, kCopyThreads, kCopySmem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

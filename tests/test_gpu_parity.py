@@ -1,0 +1,260 @@
+"""Parity of the CUDA library with the oracle, element by element and
+bitwise (the fold order is fixed, so the tolerance is 0 ulp), through the
+C ABI, for every variant, dtype and op, on seeded inputs; plus guard bands
+around every buffer, in-place calls, the barrier's arrival count, the
+timeout path and argument checks on a real device."""
+
+import numpy as np
+import pytest
+
+from oracle import barrier, elementops, ring
+from ring_allreduce_gb300 import inputs
+from rahelpers import DeviceRanks, assert_bitwise_equal
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+VARIANTS = ["direct", "ring", "persistent"]
+DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
+             ("i32", "sum"), ("i32", "max")]
+# (R, n): degenerate, n < R, ragged, several tiles per chunk with a ragged tail
+SHAPES = [(2, 1), (3, 2), (4, 4096), (5, 1001), (8, 8 * 1024 + 13), (2, 2**20 + 7),
+          (8, 2**20 + 7), (13, 77777), (16, 2**16 + 3), (32, 2**16 + 1)]
+
+
+@pytest.fixture(scope="module")
+def ra():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_allreduce_gb300 import build
+    build.build()
+    from ring_allreduce_gb300 import binding
+    return binding
+
+
+def _dist(dtype):
+    return {"f32": "normal", "bf16": "grad", "i32": "int20"}[dtype]
+
+
+def run_gpu(ra, x, dtype, op, variant, kind="allreduce", inplace=False, ctas=0, repeat=1):
+    R, n = len(x), len(x[0])
+    st = inputs.storage_dtype(dtype)
+    inp = DeviceRanks(R, n, st, host=x)
+    out = inp if inplace else DeviceRanks(R, n, st)
+    with ra.RingAllReduce(R, n, dtype, op, variant=variant) as h:
+        if ctas:
+            h.set_option(ra.Option.CTAS, ctas)
+        for _ in range(repeat):
+            if kind == "allreduce":
+                h.allreduce(inp.views, out.views)
+            elif kind == "reduce_scatter":
+                h.reduce_scatter(inp.views, out.views)
+            else:
+                h.all_gather(inp.views)
+        status, err = h.device_status()
+        assert status == ra.Status.OK, err.as_dict()
+    torch.cuda.synchronize()
+    assert inp.guards_intact(), "write outside an input buffer"
+    assert out.guards_intact(), "write outside an output buffer"
+    return out.host()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dtype,op", DTYPE_OPS)
+def test_allreduce_matches_oracle(ra, variant, dtype, op):
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=100 + i)
+        want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, dtype, op, variant)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"{variant} {dtype}/{op} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "sum"), ("i32", "max")])
+def test_reduce_scatter_owned_chunk(ra, variant, dtype, op):
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=200 + i)
+        want = ring.ring_reduce_scatter(x, o)
+        got = run_gpu(ra, x, dtype, op, variant, kind="reduce_scatter")
+        plan = ring.chunk_plan(R, n)
+        for r in range(R):
+            off, L = plan[ring.owned_chunk(R, r)]
+            assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"{variant} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_all_gather_from_reduce_scatter_layout(ra, variant, dtype):
+    """AllGather takes the layout ReduceScatter leaves: only chunk (r+1) of
+    buf[r] matters; the other chunks hold junk that must be overwritten."""
+    o = elementops.get_op(dtype, "sum")
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=300 + i)
+        rs = ring.ring_reduce_scatter(x, o)
+        junk = inputs.generate(R, n, dtype, _dist(dtype), seed=999)
+        plan = ring.chunk_plan(R, n)
+        buf = []
+        for r in range(R):
+            b = junk[r].copy()
+            off, L = plan[ring.owned_chunk(R, r)]
+            b[off:off + L] = rs[r][off:off + L]
+            buf.append(b)
+        want = ring.ring_all_gather(buf, o)
+        got = run_gpu(ra, buf, dtype, "sum", variant, kind="all_gather", inplace=True)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"{variant} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter"])
+def test_in_place(ra, variant, kind):
+    o = elementops.get_op("f32", "sum")
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, "f32", "normal", seed=400 + i)
+        got = run_gpu(ra, x, "f32", "sum", variant, kind=kind, inplace=True)
+        if kind == "allreduce":
+            want = ring.ring_allreduce(x, o)
+            for r in range(R):
+                assert_bitwise_equal(got[r], want[r], f"{variant} R={R} n={n}")
+        else:
+            want = ring.ring_reduce_scatter(x, o)
+            plan = ring.chunk_plan(R, n)
+            for r in range(R):
+                off, L = plan[ring.owned_chunk(R, r)]
+                assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"{variant} R={R} n={n}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("ctas", [1, 3, 64])
+def test_launch_shapes(ra, variant, ctas):
+    """Odd CTA counts still cover every element exactly once."""
+    o = elementops.get_op("bf16", "sum")
+    for R, n in ((8, 2**20 + 7), (3, 100003)):
+        x = inputs.generate(R, n, "bf16", "grad", seed=ctas)
+        want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, "bf16", "sum", variant, ctas=ctas)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"{variant} ctas={ctas} R={R}")
+
+
+def test_single_rank_and_empty(ra):
+    x = inputs.generate(1, 1000, "f32", "normal", 5)
+    for v in VARIANTS:
+        got = run_gpu(ra, x, "f32", "sum", v)
+        assert_bitwise_equal(got[0], x[0])
+    for v in VARIANTS:
+        got = run_gpu(ra, [np.zeros(0, np.float32)] * 4, "f32", "sum", v)
+        assert all(len(g) == 0 for g in got)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dtype,big", [("f32", 2.0**24), ("bf16", 256.0)])
+def test_ring_start_rank_pin_on_gpu(ra, variant, dtype, big):
+    """Chunk k holds big, 1, 1, -big on ranks k..k+3: the ring's fold from
+    rank k gives 0, any other start gives 2."""
+    R, per = 4, 1000
+    vals = [np.zeros(R * per, dtype=np.float32) for _ in range(R)]
+    pattern = [big, 1.0, 1.0, -big]
+    for k in range(R):
+        for j in range(R):
+            vals[(k + j) % R][k * per:(k + 1) * per] = pattern[j]
+    if dtype == "bf16":
+        x = [torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for v in vals]
+    else:
+        x = vals
+    got = run_gpu(ra, x, dtype, "sum", variant)
+    for r in range(R):
+        g = elementops.bf16_bits_to_f32(got[r]) if dtype == "bf16" else got[r]
+        assert (g == 0).all()
+
+
+@pytest.mark.parametrize("R,G", [(2, 1), (4, 3), (8, 5), (32, 2)])
+def test_barrier_exactly_r_minus_1_arrivals(ra, R, G):
+    """After k persistent calls every signal slot holds k (R-1): each of the
+    R-1 peers arrived exactly once per round and call."""
+    n = R * 5000 + 3
+    x = inputs.generate(R, n, "f32", "normal", 7)
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    out = DeviceRanks(R, n, np.float32)
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="persistent") as h:
+        h.set_option(ra.Option.CTAS, G)
+        for k in range(1, 4):
+            h.allreduce(inp.views, out.views)
+            slots, ch, rounds, calls = h.read_signals()
+            assert (ch, rounds, calls) == (G, barrier.barrier_rounds(R), k)
+            exp = barrier.expected_slot_value(R, k)
+            assert all(v == exp for g in slots for t in g for v in t), slots
+        status, _ = h.device_status()
+        assert status == ra.Status.OK
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
+
+
+def test_barrier_timeout_reports_missing_arrival(ra):
+    """A rank that withholds its arrival makes its peers' waits run out:
+    the call reports RA_ERR_TIMEOUT with one arrival missing, nothing
+    faults, and the handle works again afterwards."""
+    R, n = 4, 4 * 4096
+    x = inputs.generate(R, n, "f32", "normal", 8)
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    out = DeviceRanks(R, n, np.float32)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="persistent") as h:
+        h.set_option(ra.Option.TIMEOUT_NS, 20_000_000)   # 20 ms
+        # rank 2 withholds its arrival at the last barrier (round 4 of 5), so
+        # it finishes while its three peers wait for it
+        last = barrier.barrier_rounds(R) - 1
+        h.set_option(ra.Option.SKIP_ARRIVAL, (2 << 16) | last)
+        h.allreduce(inp.views, out.views)
+        status, err = h.device_status()
+        assert status == ra.Status.ERR_TIMEOUT
+        assert err.code == 1 and err.round == last and err.rank != 2
+        assert err.expected - err.observed == 1
+        assert "missing" in ra.ra_last_error()
+        # recovers: failure injection off, next call is correct
+        h.set_option(ra.Option.SKIP_ARRIVAL, -1)
+        h.set_option(ra.Option.TIMEOUT_NS, 1_000_000_000)
+        h.allreduce(inp.views, out.views)
+        status, err = h.device_status()
+        assert status == ra.Status.OK
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
+
+
+def test_argument_checks_on_device(ra):
+    R, n = 4, 1024
+    inp = DeviceRanks(R, n, np.float32, host=inputs.generate(R, n, "f32", "normal", 1))
+    out = DeviceRanks(R, n, np.float32)
+    h = ra.RingAllReduce(R, n, "f32", "sum")
+    try:
+        bad = [p + 4 for p in out.ptrs()]                     # misaligned
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.ptrs(), bad)
+        assert e.value.status == ra.Status.ERR_INVALID
+        ov = out.ptrs()
+        ov[1] = ov[0] + 256                                   # outputs overlap
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.ptrs(), ov)
+        assert e.value.status == ra.Status.ERR_INVALID
+        cpu = [torch.zeros(n, dtype=torch.float32) for _ in range(R)]   # host memory
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.ptrs(), cpu)
+        assert e.value.status == ra.Status.ERR_INVALID
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.ptrs(), [0] * R)
+        assert e.value.status == ra.Status.ERR_INVALID
+        mixed = out.ptrs()
+        mixed[2] = inp.ptrs()[1]                              # out[2] is another rank's input
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.ptrs(), mixed)
+        assert e.value.status == ra.Status.ERR_INVALID
+        # nothing was enqueued: the device is fine and a good call works
+        h.allreduce(inp.ptrs(), out.ptrs())
+        assert h.device_status()[0] == ra.Status.OK
+    finally:
+        h.close()
