@@ -417,17 +417,18 @@ def cpu_baseline(workload, budget_s=15.0, n_sample=None):
     from ring_allreduce_gb300 import inputs
     w = inputs.WORKLOADS[workload]
     b = inputs.itemsize(w["dtype"])
-    n_sample = n_sample or min(w["n"], 2**20)
+    n_sample = n_sample or w["n"]
     _, x, op = _oracle_step_seconds(workload, n_sample)      # warm-up call, not timed
     times = []
     t_start = time.perf_counter()
-    while (time.perf_counter() - t_start < budget_s and len(times) < 200) or len(times) < 2:
+    while (time.perf_counter() - t_start < budget_s and len(times) < 1000) or len(times) < 2:
         t = time.perf_counter()
         ring.ring_allreduce(x, op)
         times.append(time.perf_counter() - t)
     t_mean = statistics.mean(times)
     return {"value": round(n_sample * b / t_mean / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"R={w['R']} ranks x n={n_sample} per rank (same recipe and seed as the workload), "
+            "sample": f"R={w['R']} ranks x n={n_sample} per rank ("
+                      f"{'the full workload' if n_sample == w['n'] else 'same recipe and seed as the workload'}), "
                       f"{len(times)} oracle calls, {sum(times):.1f} s; numpy, one thread",
             "ms_per_call": round(t_mean * 1e3, 3)}
 

@@ -52,7 +52,8 @@
  *   - Calls on one handle must be ordered (one stream, or synchronised by the
  *     caller): the persistent variant's signal slots are per handle.
  *
- * Edge cases: n == 0 is a no-op returning RA_OK.  R == 1 copies in[0] to
+ * Edge cases: n == 0 is a no-op returning RA_OK (the buffer pointers are not
+ * looked at, NULL included).  R == 1 copies in[0] to
  * out[0].  R outside [1, 32], a NULL or misaligned pointer, an unknown dtype
  * or op return RA_ERR_INVALID.
  */

@@ -131,8 +131,15 @@ def test_in_place(ra, variant, kind):
 def test_launch_shapes(ra, variant, ctas):
     """Odd CTA counts still cover every element exactly once."""
     o = elementops.get_op("bf16", "sum")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for R, n in ((8, 2**20 + 7), (3, 100003)):
         x = inputs.generate(R, n, "bf16", "grad", seed=ctas)
+        if variant == "persistent" and R * ctas > sms:
+            # more channels than can be co-resident: refused on the host
+            with pytest.raises(ra.RAError) as e:
+                run_gpu(ra, x, "bf16", "sum", variant, ctas=4 * sms)
+            assert e.value.status == ra.Status.ERR_UNSUPPORTED
+            continue
         want = ring.ring_allreduce(x, o)
         got = run_gpu(ra, x, "bf16", "sum", variant, ctas=ctas)
         for r in range(R):
