@@ -169,6 +169,40 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
 ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
                           int* channels, int* rounds, long long* calls);
 
+/* AllReduce that allocates nothing.  The pages have no counterpart: this
+ * is a library convenience, not a step of the ring.
+ *
+ * For callers that may not allocate device memory: code whose device memory
+ * belongs to another allocator (a framework's caching allocator, a host
+ * process that gives plug-ins a fixed memory budget) and may not call
+ * cudaMalloc, and code that cannot accept the device-wide synchronisation of
+ * cudaFree.  ra_create allocates the persistent variant's scratch (signal
+ * slots, error record); this call needs no handle and takes that scratch from
+ * a fixed array inside the library instead: 256 KiB of signal slots plus a
+ * 256-byte error record, held on every GPU that loads the library until the
+ * process exits.  It runs the persistent variant (one cooperative launch,
+ * counting barrier between rounds) with results bitwise equal to
+ * ra_allreduce's.
+ *
+ * Arguments as for ra_allreduce, with R in [2, 32]; the scratch a call
+ * needs, (2R-3) * R slots per channel, always fits for one channel, and the
+ * channel count is limited to what fits.  Host-side argument errors return
+ * RA_ERR_INVALID and enqueue nothing.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call clears the part of the array it uses (an async memset
+ * on `stream`) before its kernel, so nothing carries over from the previous
+ * call.  All calls share the one array: calls that overlap on the GPU (other
+ * streams, other threads) race on it and give wrong results.  A barrier wait
+ * that runs out (1 s) ends the kernel early, records the fact in the array's
+ * error record and leaves the outputs undefined; this entry point does not
+ * report it -- callers that need that report use a handle and
+ * ra_get_device_status. */
+ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op op, const void* const* in,
+                               void* const* out, void* stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char* ra_last_error(void);
 

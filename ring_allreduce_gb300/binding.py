@@ -17,7 +17,7 @@ __all__ = [
     "Status", "DType", "Op", "Variant", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
-    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_last_error",
+    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error",
     "ra_status_string", "RingAllReduce", "EXPORTED",
 ]
 
@@ -89,6 +89,8 @@ EXPORTED = {
     "ra_read_signals": (_ST, [_P, ctypes.POINTER(ctypes.c_uint64), _SZ, ctypes.POINTER(_SZ),
                               ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                               ctypes.POINTER(ctypes.c_longlong)]),
+    "ra_allreduce_noalloc": (_ST, [ctypes.c_int, _SZ, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
+                                   ctypes.POINTER(_P), _P]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -176,6 +178,15 @@ def ra_reduce_scatter(h, ins, outs, stream=None):
 
 def ra_all_gather(h, bufs, stream=None):
     _check(_lib.ra_all_gather(h, _ptr_array(bufs), _stream(stream)))
+
+
+def ra_allreduce_noalloc(R, n, dtype, op, ins, outs, stream=None):
+    """AllReduce with the library's fixed scratch array: no handle, no
+    device allocation (for callers that may not allocate device memory)."""
+    if len(ins) != R or len(outs) != R:
+        raise ValueError(f"expected {R} rank buffers")
+    _check(_lib.ra_allreduce_noalloc(int(R), int(n), int(dtype), int(op), _ptr_array(ins),
+                                     _ptr_array(outs), _stream(stream)))
 
 
 def ra_chunk_plan(R, n):

@@ -300,6 +300,21 @@ ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
 
 }  // namespace
 
+namespace ra {
+
+// Error text for entry points defined in other translation units.
+ra_status record_error(ra_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+}  // namespace ra
+
 extern "C" {
 
 ra_status ra_chunk_plan(int R, size_t n, size_t* off, size_t* len) {
