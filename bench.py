@@ -105,7 +105,7 @@ def profile_traffic(workload, units_full):
     m_units = re.search(r"units_per_launch:\s*(\d+)", text)
     if not (m_hash and m_bytes and m_units):
         return None, path
-    if m_hash.group(1) != build.kernel_source_hash():
+    if m_hash.group(1) != build.kernel_source_hash("direct"):
         return None, path
     return int(m_bytes.group(1)) * units_full / int(m_units.group(1)), path
 

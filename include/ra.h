@@ -98,9 +98,11 @@ typedef enum ra_option {
   RA_OPT_TIMEOUT_NS = 2,     /* limit of every device-side wait in ns, default 1e9 */
   RA_OPT_CTAS = 3,           /* CTAs per rank (ring, persistent) or per chunk
                                 (direct); 0 = chosen from the SM count */
-  RA_OPT_CHECK_POINTERS = 4, /* 1 (default): each call checks with
+  RA_OPT_CHECK_POINTERS = 4, /* 1 (default): a call checks with
                                 cudaPointerGetAttributes that every buffer is
-                                device memory of the handle's device */
+                                device memory of the handle's device; a call
+                                with the same pointers as the last call that
+                                passed is not checked again */
   RA_OPT_SKIP_ARRIVAL = 5    /* failure injection for tests, persistent
                                 variant: (rank << 16) | barrier_round names a
                                 rank whose arrival at that barrier is withheld

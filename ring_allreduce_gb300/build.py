@@ -43,15 +43,26 @@ def _inputs():
     return sorted(f for f in files if os.path.isfile(f))
 
 
-def kernel_source_hash():
-    """Short hash of the CUDA / C++ sources and the public header: a
-    profile summary taken on another hash describes a different kernel."""
+# The files each kernel's device code is built from.
+KERNEL_SOURCES = {
+    "direct": ["ra_direct.cu", "ra_device.cuh", "ra_internal.h"],
+    "round": ["ra_round.cu", "ra_device.cuh", "ra_internal.h"],
+    "persistent": ["ra_persistent.cu", "ra_device.cuh", "ra_internal.h"],
+}
+
+
+def kernel_source_hash(kernel=None):
+    """Short hash of the sources of one kernel (``KERNEL_SOURCES``), or of
+    every CUDA / C++ source and the public header when ``kernel`` is None.
+    A profile summary taken on another hash describes a different kernel."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    files = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(CSRC))
+    for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
-    with open(os.path.join(INCLUDE, "ra.h"), "rb") as fh:
-        h.update(fh.read())
+    if kernel is None:
+        with open(os.path.join(INCLUDE, "ra.h"), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

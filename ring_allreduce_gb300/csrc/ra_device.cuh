@@ -172,16 +172,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// SignalAdd: release at GPU scope, so everything this thread has ordered
-// before it (including other threads' writes it synchronised with) is
-// visible to whoever acquires the count.
-__device__ __forceinline__ void signal_add_release(uint64_t* p, uint64_t v) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// Release / acquire in the fence form: one fence.acq_rel.gpu before a
+// batch of relaxed SignalAdds makes everything ordered before the fence
+// (this thread's writes and those of the CTA it synchronised with) visible
+// to whoever observes any of the adds and then runs the acquire fence.
+// One fence for the R-1 adds of a barrier round instead of a release per add.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void signal_add_relaxed(uint64_t* p, uint64_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint64_t signal_load_acquire(const uint64_t* p) {
+__device__ __forceinline__ uint64_t signal_load_relaxed(const uint64_t* p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 

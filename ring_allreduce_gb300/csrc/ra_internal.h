@@ -71,6 +71,8 @@ struct PersistArgs {
 };
 
 cudaError_t launch_direct(int dtype, int op, const DirectArgs& a, int ctas_per_chunk, cudaStream_t st);
+// 16-byte vectors a thread of the direct kernel takes per step.
+int direct_vectors_per_thread(int R, int mode);
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st);
 cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st);
 // Per-device set-up of the AllGather kernel (its shared-memory opt-in);

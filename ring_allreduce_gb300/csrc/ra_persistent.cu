@@ -23,6 +23,8 @@
 // deliberately" explains that a single counter reused across rounds lets a
 // peer a round ahead stand in for a late one; here every (channel, round,
 // waiter) has its own 64-bit slot, so a count comes only from its round.
+// Release and acquire take the fence form: one fence.acq_rel.gpu before the
+// R-1 relaxed adds, one after the poll has seen its target.
 // Slots are never cleared between calls: the k-th call on a slot array
 // waits for k * (R - 1), compared in 64-bit rolling order (NCCL Device API
 // GIN article, signals and counters).
@@ -42,10 +44,10 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
   if (threadIdx.x == 0) {
     int abort = 0;
     uint64_t* row = a.slots + ((int64_t)g * (a.rounds - 1) + t) * a.R;
-    __threadfence();
+    fence_acq_rel_gpu();   // release: this round's stores of the whole CTA
     if (!(r == a.skip_rank && t == a.skip_round)) {
       for (int q = 0; q < a.R; ++q)
-        if (q != r) signal_add_release(row + q, 1);
+        if (q != r) signal_add_relaxed(row + q, 1);
     }
     const uint64_t target = a.epoch * (uint64_t)(a.R - 1);
     const uint64_t t0 = globaltimer_ns();
@@ -53,8 +55,11 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
     const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
     uint64_t seen = 0;
     for (uint64_t it = 0;; ++it) {
-      seen = signal_load_acquire(row + r);
-      if (rolling_reached(seen, target)) break;
+      seen = signal_load_relaxed(row + r);
+      if (rolling_reached(seen, target)) {
+        fence_acq_rel_gpu();   // acquire: the peers' round is visible to this CTA
+        break;
+      }
       if (load_relaxed_u32(&a.err->code) != 0u) { abort = 1; break; }
       if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
         if (atomicCAS(&a.err->code, 0u, 1u) == 0u) {
