@@ -103,13 +103,21 @@ typedef enum ra_option {
                                 device memory of the handle's device; a call
                                 with the same pointers as the last call that
                                 passed is not checked again */
-  RA_OPT_SKIP_ARRIVAL = 5    /* failure injection for tests, persistent
+  RA_OPT_SKIP_ARRIVAL = 5,   /* failure injection for tests, persistent
                                 variant: (rank << 16) | barrier_round names a
                                 rank whose arrival at that barrier is withheld
                                 in every channel; -1 (default) = off.  The
                                 peers' waits then run out after
                                 RA_OPT_TIMEOUT_NS and the call reports
                                 RA_ERR_TIMEOUT through ra_get_device_status. */
+  RA_OPT_GRAPHS = 6          /* 1 (default): the ring variant captures its
+                                2(R-1) launches in a CUDA graph the first time
+                                it meets a set of buffers and replays the graph
+                                on later calls with the same buffers (one host
+                                launch instead of 2(R-1)); when the caller's
+                                stream is itself being captured it launches
+                                directly.  0: always launch directly.  Any
+                                ra_set_option drops the cached graph. */
 } ra_option;
 
 /* Device error record, filled by the first wait that gives up. */

@@ -55,6 +55,7 @@ class Option(enum.IntEnum):
     CTAS = 3
     CHECK_POINTERS = 4
     SKIP_ARRIVAL = 5
+    GRAPHS = 6
 
 
 class DeviceError(ctypes.Structure):

@@ -89,6 +89,14 @@ struct ra_ctx {
   bool checked_has_in = false;
   const void* checked_in[ra::kMaxRanks] = {};
   void* checked_out[ra::kMaxRanks] = {};
+  // the ring variant's 2(R-1) launches, captured once per buffer set and
+  // replayed as one CUDA graph
+  int use_graphs = 1;
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t ring_exec = nullptr;
+  int ring_kind = -1;
+  const void* ring_in[ra::kMaxRanks] = {};
+  void* ring_out[ra::kMaxRanks] = {};
 };
 
 namespace {
@@ -274,6 +282,61 @@ ra_status run_ring_gather(ra_ctx* h, void* const* buf, cudaStream_t st) {
   return RA_OK;
 }
 
+void drop_ring_graph(ra_ctx* h) {
+  if (h->ring_exec) cudaGraphExecDestroy(h->ring_exec);
+  h->ring_exec = nullptr;
+  h->ring_kind = -1;
+}
+
+ra_status run_ring_launches(ra_ctx* h, int kind, const void* const* in, void* const* out, cudaStream_t st) {
+  if (kind == kKindAllGather) return run_ring_gather(h, out, st);
+  ra_status s = run_ring_reduce(h, in, out, st);
+  if (s != RA_OK || kind == kKindReduceScatter) return s;
+  return run_ring_gather(h, out, st);
+}
+
+// Ring variant: replay the cached graph of this call's launches when the
+// buffers are those it was captured with; otherwise capture it first.  When
+// the caller's own stream is being captured, or graphs are off, launch
+// directly (the launches then join the caller's graph).
+ra_status run_ring(ra_ctx* h, int kind, const void* const* in, void* const* out, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (!h->use_graphs || !h->capture_stream || cudaStreamIsCapturing(st, &cs) != cudaSuccess ||
+      cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return run_ring_launches(h, kind, in, out, st);
+  }
+  bool same = h->ring_exec && h->ring_kind == kind;
+  for (int r = 0; same && r < h->R; ++r)
+    same = h->ring_out[r] == out[r] && h->ring_in[r] == (in ? in[r] : nullptr);
+  if (!same) {
+    drop_ring_graph(h);
+    cudaError_t e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "ring graph capture");
+    ra_status s = run_ring_launches(h, kind, in, out, h->capture_stream);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(h->capture_stream, &g);
+    if (s != RA_OK) {
+      if (g) cudaGraphDestroy(g);
+      return s;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring graph capture");
+    e = cudaGraphInstantiate(&h->ring_exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      h->ring_exec = nullptr;
+      return cuda_fail(e, "ring graph instantiation");
+    }
+    h->ring_kind = kind;
+    for (int r = 0; r < h->R; ++r) {
+      h->ring_in[r] = in ? in[r] : nullptr;
+      h->ring_out[r] = out[r];
+    }
+  }
+  cudaError_t e = cudaGraphLaunch(h->ring_exec, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "ring graph launch");
+}
+
 ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                          cudaStream_t st) {
   SlotRegion& reg = h->region[kind];
@@ -416,11 +479,12 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   }
   e = cudaMalloc(&h->d_err, sizeof(ra_device_error));
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(ra_device_error));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     if (h->d_slots) cudaFree(h->d_slots);
     if (h->d_err) cudaFree(h->d_err);
     delete h;
-    return cuda_fail(e, "error record allocation");
+    return cuda_fail(e, "handle set-up");
   }
   *out = h;
   return RA_OK;
@@ -432,6 +496,8 @@ ra_status ra_destroy(ra_handle h) {
   ra_status s = RA_OK;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) s = cuda_fail(e, "synchronise before destroy");
+  drop_ring_graph(h);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->d_slots) cudaFree(h->d_slots);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
@@ -453,8 +519,7 @@ ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, voi
   }
   switch (h->variant) {
     case RA_VARIANT_RING:
-      s = run_ring_reduce(h, in, out, st);
-      return s != RA_OK ? s : run_ring_gather(h, out, st);
+      return run_ring(h, kKindAllReduce, in, out, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
     default:
@@ -477,7 +542,7 @@ ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out
   }
   switch (h->variant) {
     case RA_VARIANT_RING:
-      return run_ring_reduce(h, in, out, st);
+      return run_ring(h, kKindReduceScatter, in, out, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
     default:
@@ -496,7 +561,7 @@ ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (h->variant) {
     case RA_VARIANT_RING:
-      return run_ring_gather(h, buf, st);
+      return run_ring(h, kKindAllGather, nullptr, buf, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
     default:
@@ -518,7 +583,15 @@ ra_status ra_owned_chunk(ra_handle h, int r, size_t* off, size_t* len) {
 
 ra_status ra_set_option(ra_handle h, int key, long long value) {
   if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  {
+    // launch shapes and limits are baked into a captured ring graph
+    DeviceGuard g(h->device);
+    drop_ring_graph(h);
+  }
   switch (key) {
+    case RA_OPT_GRAPHS:
+      h->use_graphs = value != 0;
+      return RA_OK;
     case RA_OPT_VARIANT:
       if (value < RA_VARIANT_AUTO || value > RA_VARIANT_PERSISTENT)
         return fail(RA_ERR_INVALID, "unknown variant %lld", value);
@@ -554,6 +627,7 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_CTAS: *value = h->ctas; return RA_OK;
     case RA_OPT_CHECK_POINTERS: *value = h->check_pointers; return RA_OK;
     case RA_OPT_SKIP_ARRIVAL: *value = h->skip; return RA_OK;
+    case RA_OPT_GRAPHS: *value = h->use_graphs; return RA_OK;
     default: return fail(RA_ERR_INVALID, "unknown option %d", key);
   }
 }

@@ -265,3 +265,74 @@ def test_argument_checks_on_device(ra):
         assert h.device_status()[0] == ra.Status.OK
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "all_gather"])
+def test_ring_graph_replay_and_rebuild(ra, kind):
+    """The ring variant replays its captured graph on repeated calls with the
+    same buffers (reading the data they hold now), captures a new one when
+    the buffers change, and gives the same bits with graphs switched off."""
+    R, n = 8, 2**18 + 5
+    o = elementops.get_op("f32", "sum")
+    plan = ring.chunk_plan(R, n)
+    bufs = [DeviceRanks(R, n, np.float32) for _ in range(2)]
+    outs = [DeviceRanks(R, n, np.float32) for _ in range(2)]
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="ring") as h:
+        for step, (b, out, graphs) in enumerate([(0, 0, 1), (0, 0, 1), (1, 1, 1), (0, 1, 1), (1, 0, 0)]):
+            if step == 4:
+                h.set_option(ra.Option.GRAPHS, graphs)
+            x = inputs.generate(R, n, "f32", "normal", seed=50 + step)
+            if kind == "all_gather":
+                rs = ring.ring_reduce_scatter(x, o, fill=np.float32(0))
+                want = ring.ring_all_gather(rs, o)
+                src = DeviceRanks(R, n, np.float32, host=rs)
+                outs[out].big.copy_(src.big)
+                h.all_gather(outs[out].views)
+            else:
+                bufs[b].big.copy_(DeviceRanks(R, n, np.float32, host=x).big)
+                if kind == "allreduce":
+                    want = ring.ring_allreduce(x, o)
+                    h.allreduce(bufs[b].views, outs[out].views)
+                else:
+                    want = ring.ring_reduce_scatter(x, o)
+                    h.reduce_scatter(bufs[b].views, outs[out].views)
+            assert h.device_status()[0] == ra.Status.OK
+            got = outs[out].host()
+            for r in range(R):
+                if kind == "reduce_scatter":
+                    off, L = plan[ring.owned_chunk(R, r)]
+                    assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"step {step}")
+                else:
+                    assert_bitwise_equal(got[r], want[r], f"step {step} rank {r}")
+            assert outs[out].guards_intact()
+
+
+@pytest.mark.parametrize("variant", ["direct", "ring"])
+def test_calls_inside_a_caller_graph(ra, variant):
+    """A caller may capture ra_allreduce into its own CUDA graph (after one
+    call on the same buffers outside it) and replay it on new data."""
+    R, n = 4, 100003
+    o = elementops.get_op("f32", "sum")
+    inp = DeviceRanks(R, n, np.float32, host=inputs.generate(R, n, "f32", "normal", 1))
+    out = DeviceRanks(R, n, np.float32)
+    h = ra.RingAllReduce(R, n, "f32", "sum", variant=variant)
+    try:
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            h.allreduce(inp.views, out.views, side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            h.allreduce(inp.views, out.views, side)
+        for seed in (7, 8):
+            x = inputs.generate(R, n, "f32", "normal", seed)
+            inp.big.copy_(DeviceRanks(R, n, np.float32, host=x).big)
+            g.replay()
+            torch.cuda.synchronize()
+            want = ring.ring_allreduce(x, o)
+            got = out.host()
+            for r in range(R):
+                assert_bitwise_equal(got[r], want[r], f"{variant} seed {seed}")
+        assert h.device_status()[0] == ra.Status.OK
+    finally:
+        h.close()
