@@ -332,7 +332,7 @@ def run_gpu_arm(args):
             "traffic": traffic,
             "traffic_source": os.path.relpath(prof_path, ROOT) if prof_path else None,
         },
-        "gpu_launches": args.steps * (1 if variant_name in ("auto", "direct", "persistent") else 2 * (R - 1)),
+        "gpu_launches": args.steps * (2 * (R - 1) if variant_name == "ring" else 1),
     }
     if clk is not None:
         result["clocks"] = clk
@@ -340,14 +340,14 @@ def run_gpu_arm(args):
     # ---- other variants, same workload (fewer steps)
     if not args.no_variants and rank == 0:
         var = {}
-        for v in ("direct", "ring", "persistent"):
+        for v in ("direct", "ring", "persistent", "pipelined"):
             hv = ra.RingAllReduce(R, n, dtype, op, variant=v)
             steps_v = max(5, min(args.steps, 100))
             total_ms, lm = _time_variant(torch, ra, hv, ins, outs, steps_v, max(3, args.warmup // 4 or 3))
             assert hv.device_status()[0] == ra.Status.OK
             hv.close()
             t = statistics.mean(lm) / 1e3
-            by = compulsory if v == "direct" else (ring_bytes if v == "ring" else ring_bytes)
+            by = compulsory if v == "direct" else ring_bytes
             var[v] = {"algbw": round(n * b / t / 1e9, 3),
                       "us_per_call": round(t * 1e6, 2),
                       "frac_compulsory": round(compulsory / t / 1e9 / peak, 4),
@@ -512,6 +512,45 @@ def run_reference_arm(args):
 
 # ------------------------------------------------------------------ sweep
 
+SWEEP_VARIANTS = [
+    ("direct", "direct", lambda ra: []),
+    ("ring", "ring", lambda ra: []),
+    ("persistent", "persistent", lambda ra: []),
+    ("persistent_per_peer", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
+    ("pipelined", "pipelined", lambda ra: []),
+]
+
+
+def run_barriers(args):
+    """Barrier cost, counting vs per-peer, as the rank count grows: the
+    persistent variant on a tiny buffer (R x 256 fp32 elements, one channel),
+    so each call is one cooperative launch plus 2R-3 barrier rounds; the
+    pipelined variant on the same buffer for comparison.  One JSON line per R."""
+    import torch
+    from ring_allreduce_gb300 import build, inputs
+    build.build()
+    from ring_allreduce_gb300 import binding as ra
+    for R in (2, 3, 4, 6, 8, 12, 16, 24, 32):
+        n = 256 * R
+        host = inputs.generate(R, n, "f32", "normal", inputs.SWEEP_SEED)
+        _, ins = _device_ranks(torch, R, n, inputs.storage_dtype("f32"), host)
+        _, outs = _device_ranks(torch, R, n, inputs.storage_dtype("f32"))
+        line = {"barriers": "persistent, one channel", "R": R, "n_per_rank": n, "barrier_rounds": 2 * R - 3}
+        for name, v, opts in (("counting", "persistent", []),
+                              ("per_peer", "persistent", [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
+                              ("pipelined", "pipelined", [])):
+            h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
+            h.set_option(ra.Option.CTAS, 1)
+            for key, value in opts:
+                h.set_option(key, value)
+            _, lm = _time_variant(torch, ra, h, ins, outs, 500, 20)
+            assert h.device_status()[0] == ra.Status.OK
+            h.close()
+            t = statistics.median(lm)
+            line[name] = {"us_per_call": round(t * 1e3, 2)}
+        print(json.dumps(line), flush=True)
+
+
 def run_sweep(args):
     """Latency/bandwidth sweep (R=8 fp32 sum over n, and R over 2..32 at
     n=2^24), every variant; one JSON line per point on stdout."""
@@ -526,14 +565,16 @@ def run_sweep(args):
         _, ins = _device_ranks(torch, R, n, inputs.storage_dtype("f32"), host)
         _, outs = _device_ranks(torch, R, n, inputs.storage_dtype("f32"))
         line = {"sweep": "r8_f32_n" if R == 8 else "f32_R", "R": R, "n_per_rank": n}
-        for v in ("direct", "ring", "persistent"):
+        for name, v, opts in SWEEP_VARIANTS:
             h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
+            for key, value in opts(ra):
+                h.set_option(key, value)
             steps = 200 if n <= 2**20 else 30
             _, lm = _time_variant(torch, ra, h, ins, outs, steps, 10)
             assert h.device_status()[0] == ra.Status.OK
             h.close()
             t = statistics.median(lm) / 1e3
-            line[v] = {"us": round(t * 1e6, 2), "algbw": round(n * 4 / t / 1e9, 2),
+            line[name] = {"us": round(t * 1e6, 2), "algbw": round(n * 4 / t / 1e9, 2),
                        "busbw": round(n * 4 / t / 1e9 * 2 * (R - 1) / R, 2),
                        "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
         print(json.dumps(line), flush=True)
@@ -549,8 +590,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="r8_f32", choices=["r8_f32", "r8_bf16", "r16_i32", "r4_small"])
     ap.add_argument("--n", type=int, default=None, help="override n per rank (profiling of a smaller case)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined"])
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--barriers", action="store_true", help="barrier cost vs R, counting vs per-peer")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
@@ -566,6 +608,8 @@ def main():
         run_reference_arm(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.barriers:
+        run_barriers(args)
     else:
         run_gpu_arm(args)
 

@@ -37,8 +37,10 @@
  *     themselves are host arrays of R entries, read during the call only.
  *   - out[r] == in[r] (in place) is allowed.  Any other overlap between the
  *     2R ranges, or between two outputs, is RA_ERR_INVALID.
- *   - The handle owns only what it allocates at ra_create: the barrier
- *     signal slots and a device error record.
+ *   - The handle owns only what it allocates: at ra_create the counting
+ *     barrier's signal slots, a device error record and a private stream (for
+ *     capturing the ring variant's graph); on the first call that needs them,
+ *     the per-peer barrier's slots and the pipelined variant's flags.
  *
  * Asynchrony and errors
  *   - Every compute call is enqueued on `stream` (a cudaStream_t; NULL is the
@@ -88,10 +90,28 @@ typedef enum ra_variant {
   RA_VARIANT_RING = 2,        /* one launch per ring round: R-1 reduce rounds
                                  (recvReduceSend ... recvReduceCopySend), then
                                  R-1 AllGather rounds done with TMA bulk copies */
-  RA_VARIANT_PERSISTENT = 3   /* one cooperative launch running every round;
-                                 simulated ranks meet at a counting barrier
-                                 between rounds */
+  RA_VARIANT_PERSISTENT = 3,  /* one cooperative launch running every round;
+                                 simulated ranks meet at a barrier between
+                                 rounds (RA_OPT_BARRIER: counting, the
+                                 default, or per-peer) */
+  RA_VARIANT_PIPELINED = 4    /* one cooperative launch running every round
+                                 with no barrier: a rank starts a round on a
+                                 sub-slice as soon as its predecessor has
+                                 finished the previous round on it
+                                 (per-predecessor progress flags; rounds of
+                                 different sub-slices overlap) */
 } ra_variant;
+
+/* Barrier of the persistent variant (RA_OPT_BARRIER). */
+typedef enum ra_barrier {
+  RA_BARRIER_COUNTING = 0,    /* one 64-bit signal per (channel, round, waiter);
+                                 each of the R-1 peers adds 1 ("comm: lift the
+                                 GIN scale-out ceiling by making the rail
+                                 barrier a counting barrier", section "Fix") */
+  RA_BARRIER_PER_PEER = 1     /* one signal per (channel, round, waiter, peer),
+                                 the design that page replaced; a wait that runs
+                                 out can name the missing peer */
+} ra_barrier;
 
 typedef enum ra_option {
   RA_OPT_VARIANT = 1,        /* ra_variant, default RA_VARIANT_AUTO */
@@ -103,14 +123,16 @@ typedef enum ra_option {
                                 device memory of the handle's device; a call
                                 with the same pointers as the last call that
                                 passed is not checked again */
-  RA_OPT_SKIP_ARRIVAL = 5,   /* failure injection for tests, persistent
-                                variant: (rank << 16) | barrier_round names a
-                                rank whose arrival at that barrier is withheld
-                                in every channel; -1 (default) = off.  The
-                                peers' waits then run out after
+  RA_OPT_SKIP_ARRIVAL = 5,   /* failure injection for tests: (rank << 16) |
+                                round names a rank that withholds, in every
+                                channel, its arrival at that barrier round
+                                (persistent variant) or every progress flag
+                                from that ring round on (pipelined variant);
+                                -1 (default) = off.  The waits of the ranks
+                                that depend on it then run out after
                                 RA_OPT_TIMEOUT_NS and the call reports
                                 RA_ERR_TIMEOUT through ra_get_device_status. */
-  RA_OPT_GRAPHS = 6          /* 1 (default): the ring variant captures its
+  RA_OPT_GRAPHS = 6,         /* 1 (default): the ring variant captures its
                                 2(R-1) launches in a CUDA graph the first time
                                 it meets a set of buffers and replays the graph
                                 on later calls with the same buffers (one host
@@ -118,16 +140,23 @@ typedef enum ra_option {
                                 stream is itself being captured it launches
                                 directly.  0: always launch directly.  Any
                                 ra_set_option drops the cached graph. */
+  RA_OPT_BARRIER = 7,        /* ra_barrier of the persistent variant */
+  RA_OPT_SLICES = 8          /* sub-slices per channel slice of the pipelined
+                                variant, 1..64; 0 (default) = about 128 KiB each */
 } ra_option;
 
 /* Device error record, filled by the first wait that gives up. */
 typedef struct ra_device_error {
-  uint32_t code;      /* 0 = none, 1 = barrier wait ran out, 2 = copy wait ran out */
-  int32_t round;      /* barrier round (0-based) or tile index */
+  uint32_t code;      /* 0 = none; 1 = counting-barrier wait ran out; 2 = bulk-copy wait
+                         ran out; 3 = per-peer barrier wait ran out; 4 = pipelined
+                         flag wait ran out */
+  int32_t round;      /* barrier round (0-based), ring round (code 4) or AllGather round (code 2) */
   int32_t rank;       /* waiting rank */
   int32_t channel;    /* channel: the CTA index within its rank */
-  uint64_t observed;  /* signal value seen last */
-  uint64_t expected;  /* value waited for; expected - observed arrivals were missing */
+  int32_t peer;       /* rank that did not arrive when it can be named (codes 3, 4), else -1 */
+  int32_t reserved;
+  uint64_t observed;  /* arrivals (codes 1, 3) or progress (code 4) seen last */
+  uint64_t expected;  /* what was waited for: expected - observed were missing */
 } ra_device_error;
 
 typedef struct ra_ctx* ra_handle;
@@ -170,12 +199,17 @@ ra_status ra_get_option(ra_handle h, int key, long long* value);
  * handle can be used again. */
 ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
 
-/* Synchronise the device and copy the persistent variant's signal slots of
- * the last launch's kind into dst (host array of cap entries), laid out
- * [channel][barrier round][waiter rank].  With dst == NULL only the sizes
- * are returned.  *count, *channels, *rounds get
- * the sizes used; *calls gets how many calls of that kind ran since the
- * slots were last reset, so every slot must equal calls * (R - 1). */
+/* Synchronise the device and copy the signal array of the last persistent
+ * or pipelined launch (its kind and scheme) into dst (host array of cap
+ * entries).  With dst == NULL only the sizes are returned.  *count gets the
+ * entries, *channels the channel count G, *calls how many calls of that kind
+ * and scheme ran since the array was last zeroed, *rounds:
+ *   counting barrier  [G][rounds][R] (rounds = barrier rounds); every entry
+ *                     equals calls * (R - 1)
+ *   per-peer barrier  [G][rounds][R waiters][R peers]; every entry equals
+ *                     calls, except waiter == peer, which stays 0
+ *   pipelined flags   [G][R][J] (rounds = ring rounds, J = count / (G R));
+ *                     every entry equals calls * rounds */
 ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
                           int* channels, int* rounds, long long* calls);
 

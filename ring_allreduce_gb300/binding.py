@@ -14,7 +14,7 @@ import os
 from . import build as _build
 
 __all__ = [
-    "Status", "DType", "Op", "Variant", "Option", "DeviceError", "RAError",
+    "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error",
@@ -47,6 +47,12 @@ class Variant(enum.IntEnum):
     DIRECT = 1
     RING = 2
     PERSISTENT = 3
+    PIPELINED = 4
+
+
+class Barrier(enum.IntEnum):
+    COUNTING = 0
+    PER_PEER = 1
 
 
 class Option(enum.IntEnum):
@@ -56,11 +62,14 @@ class Option(enum.IntEnum):
     CHECK_POINTERS = 4
     SKIP_ARRIVAL = 5
     GRAPHS = 6
+    BARRIER = 7
+    SLICES = 8
 
 
 class DeviceError(ctypes.Structure):
     _fields_ = [("code", ctypes.c_uint32), ("round", ctypes.c_int32), ("rank", ctypes.c_int32),
-                ("channel", ctypes.c_int32), ("observed", ctypes.c_uint64), ("expected", ctypes.c_uint64)]
+                ("channel", ctypes.c_int32), ("peer", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("observed", ctypes.c_uint64), ("expected", ctypes.c_uint64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -224,19 +233,16 @@ def ra_get_device_status(h, stream=None):
 
 
 def ra_read_signals(h):
-    """Signal slots of the last persistent call's kind, as a list laid out
-    [channel][round][rank], plus (channels, rounds, calls)."""
+    """Signal array of the last persistent or pipelined call (its kind and
+    scheme), flat, plus (channels, rounds, calls); the layouts are those of
+    ra_read_signals in ra.h."""
     count, ch, rd, calls = _SZ(), ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
     _check(_lib.ra_read_signals(h, None, 0, ctypes.byref(count), ctypes.byref(ch), ctypes.byref(rd),
                                 ctypes.byref(calls)))
     buf = (ctypes.c_uint64 * max(count.value, 1))()
     _check(_lib.ra_read_signals(h, buf, count.value, ctypes.byref(count), ctypes.byref(ch),
                                 ctypes.byref(rd), ctypes.byref(calls)))
-    flat = list(buf)[:count.value]
-    R = count.value // (ch.value * rd.value) if ch.value and rd.value else 0
-    nested = [[flat[(g * rd.value + t) * R:(g * rd.value + t + 1) * R] for t in range(rd.value)]
-              for g in range(ch.value)]
-    return nested, ch.value, rd.value, calls.value
+    return list(buf)[:count.value], ch.value, rd.value, calls.value
 
 
 _DTYPES = {"f32": DType.F32, "bf16": DType.BF16, "i32": DType.I32}

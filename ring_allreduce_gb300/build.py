@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libra_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_static.cu"]
+SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_pipelined.cu", "ra_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE arithmetic throughout: no fast-math, no flush to zero, no contraction.
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-ftz=false",
@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "direct": ["ra_direct.cu", "ra_device.cuh", "ra_internal.h"],
     "round": ["ra_round.cu", "ra_device.cuh", "ra_internal.h"],
     "persistent": ["ra_persistent.cu", "ra_device.cuh", "ra_internal.h"],
+    "pipelined": ["ra_pipelined.cu", "ra_device.cuh", "ra_internal.h"],
 }
 
 

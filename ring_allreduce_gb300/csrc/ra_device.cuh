@@ -189,6 +189,10 @@ __device__ __forceinline__ uint64_t signal_load_relaxed(const uint64_t* p) {
   return v;
 }
 
+__device__ __forceinline__ void signal_store_relaxed(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t load_relaxed_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -198,6 +202,20 @@ __device__ __forceinline__ uint32_t load_relaxed_u32(const uint32_t* p) {
 // Rolling comparison: observed has reached target even across wrap-around.
 __device__ __forceinline__ bool rolling_reached(uint64_t observed, uint64_t target) {
   return (int64_t)(observed - target) >= 0;
+}
+
+// The first wait that gives up fills the error record; later ones leave it.
+__device__ __forceinline__ void record_wait_error(ra_device_error* err, uint32_t code, int round, int rank,
+                                                  int channel, int peer, uint64_t observed, uint64_t expected) {
+  if (atomicCAS(&err->code, 0u, code) == 0u) {
+    err->round = round;
+    err->rank = rank;
+    err->channel = channel;
+    err->peer = peer;
+    err->observed = observed;
+    err->expected = expected;
+    __threadfence();
+  }
 }
 
 // ------------------------------------------------- TMA bulk copy, mbarrier

@@ -53,16 +53,21 @@ struct DeviceGuard {
   }
 };
 
-// Signal slots of one kind of call (AllReduce, ReduceScatter, AllGather).
+// Signal slots of one synchronisation scheme (counting barrier, per-peer
+// barrier, pipelined flags) and one kind of call (AllReduce, ReduceScatter,
+// AllGather).
 struct SlotRegion {
   uint64_t* d = nullptr;
   size_t cap = 0;       // entries
+  bool owned = false;   // allocated on its own (the counting slots share one allocation)
   int G = 0;            // channel count the slots were last used with
+  int J = 0;            // sub-slices (pipelined flags)
   int rounds = 0;       // ring rounds of this kind
   long long calls = 0;  // completed-or-enqueued calls since the last reset
 };
 
 enum Kind { kKindAllReduce = 0, kKindReduceScatter = 1, kKindAllGather = 2 };
+constexpr int kMaxSlices = 64;
 
 }  // namespace
 
@@ -74,6 +79,9 @@ struct ra_ctx {
   int device = 0;
   int num_sms = 0;
   int persist_blocks_per_sm = 0;
+  int pipe_blocks_per_sm = 0;
+  int barrier = RA_BARRIER_COUNTING;
+  int slices = 0;
   int variant = RA_VARIANT_AUTO;
   long long timeout_ns = 1000000000LL;
   int ctas = 0;
@@ -81,7 +89,8 @@ struct ra_ctx {
   long long skip = -1;
   uint64_t* d_slots = nullptr;
   ra_device_error* d_err = nullptr;
-  SlotRegion region[3];
+  SlotRegion region[3][3];   // [ra::Sync][Kind]
+  int last_sync = -1;
   int last_kind = -1;
   // the last pointer set that passed the device-memory check: a call on the
   // same buffers does not query their attributes again
@@ -337,50 +346,154 @@ ra_status run_ring(ra_ctx* h, int kind, const void* const* in, void* const* out,
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "ring graph launch");
 }
 
+int gmax_channels(const ra_ctx* h, int blocks_per_sm) {
+  return (blocks_per_sm > 0 ? blocks_per_sm : 1) * h->num_sms / h->R + 1;
+}
+
+size_t region_entries(const ra_ctx* h, int sync, int rounds, int G, int J) {
+  const size_t R = (size_t)h->R;
+  const size_t br = (size_t)(rounds > 1 ? rounds - 1 : 0);
+  if (sync == ra::kSyncCounting) return (size_t)G * br * R;
+  if (sync == ra::kSyncPerPeer) return (size_t)G * br * R * R;
+  return (size_t)G * R * (size_t)J;
+}
+
+// The slot array of (sync, kind), allocated on first use for the per-peer
+// barrier and the pipelined flags (the counting slots come with ra_create).
+ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
+  SlotRegion& reg = h->region[sync][kind];
+  if (!reg.d) {
+    const int bps = sync == ra::kSyncFlags ? h->pipe_blocks_per_sm : h->persist_blocks_per_sm;
+    const size_t cap = region_entries(h, sync, reg.rounds, gmax_channels(h, bps), kMaxSlices);
+    if (cap > 0) {
+      cudaError_t e = cudaMalloc(&reg.d, cap * sizeof(uint64_t));
+      if (e == cudaSuccess) e = cudaMemset(reg.d, 0, cap * sizeof(uint64_t));
+      if (e != cudaSuccess) {
+        if (reg.d) cudaFree(reg.d);
+        reg.d = nullptr;
+        return cuda_fail(e, "signal slot allocation");
+      }
+    }
+    reg.cap = cap;
+    reg.owned = true;
+    reg.G = 0;
+    reg.calls = 0;
+  }
+  *out = &reg;
+  return RA_OK;
+}
+
+// Zero a region when the launch shape it was counted with changes.
+ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
+  if (reg.G != G || reg.J != J) {
+    if (reg.cap) {
+      cudaError_t e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
+      if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
+    }
+    reg.G = G;
+    reg.J = J;
+    reg.calls = 0;
+  }
+  return RA_OK;
+}
+
 ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                          cudaStream_t st) {
-  SlotRegion& reg = h->region[kind];
+  const int sync = h->barrier == RA_BARRIER_PER_PEER ? ra::kSyncPerPeer : ra::kSyncCounting;
+  SlotRegion* reg = nullptr;
+  ra_status s = ensure_region(h, sync, kind, &reg);
+  if (s != RA_OK) return s;
   ra::PersistArgs a;
   a.p = make_ptrs(h, in, out);
   a.plan = make_plan(h->R, h->n);
   a.R = h->R;
   a.mode = mode;
-  a.rounds = reg.rounds;
+  a.sync = sync;
+  a.J = 1;
+  a.rounds = reg->rounds;
   a.G = persistent_channels(h, a.plan);
   const int cap = h->persist_blocks_per_sm * h->num_sms;
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "persistent grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
-  const size_t need = (size_t)a.G * (size_t)(reg.rounds > 1 ? reg.rounds - 1 : 0) * (size_t)h->R;
-  if (need > reg.cap) return fail(RA_ERR_UNSUPPORTED, "too many channels for the signal slots");
-  if (reg.G != a.G) {
-    cudaError_t e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
-    if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
-    reg.G = a.G;
-    reg.calls = 0;
-  }
-  a.slots = reg.d;
-  a.epoch = (uint64_t)(reg.calls + 1);
+  if (region_entries(h, sync, a.rounds, a.G, 1) > reg->cap)
+    return fail(RA_ERR_UNSUPPORTED, "too many channels for the signal slots");
+  s = prepare_region(*reg, a.G, 1, st);
+  if (s != RA_OK) return s;
+  a.slots = reg->d;
+  a.epoch = (uint64_t)(reg->calls + 1);
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
   a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
   cudaError_t e = ra::launch_persistent(h->dtype, h->op, a, ra::kPersistThreads, st);
   if (e != cudaSuccess) return cuda_fail(e, "persistent kernel launch");
-  reg.calls += 1;
+  reg->calls += 1;
+  h->last_sync = sync;
+  h->last_kind = kind;
+  return RA_OK;
+}
+
+// Sub-slices of a channel's slice: about 128 KiB each, at most kMaxSlices.
+int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
+  if (h->slices > 0) return h->slices;
+  const int64_t slice_bytes = pl.C * (int64_t)elem_bytes(h->dtype) / G;
+  int64_t J = slice_bytes / (128 * 1024);
+  if (J > kMaxSlices) J = kMaxSlices;
+  return (int)(J < 1 ? 1 : J);
+}
+
+ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
+                        cudaStream_t st) {
+  SlotRegion* reg = nullptr;
+  ra_status s = ensure_region(h, ra::kSyncFlags, kind, &reg);
+  if (s != RA_OK) return s;
+  ra::PersistArgs a;
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.sync = ra::kSyncFlags;
+  a.rounds = reg->rounds;
+  const int cap = h->pipe_blocks_per_sm * h->num_sms;
+  if (h->ctas > 0) {
+    a.G = h->ctas;
+  } else {
+    const int64_t vecs = ceil_div(a.plan.C, vec_elems(h->dtype)) + 1;
+    const int64_t need = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
+    const int64_t most = cap / h->R;
+    a.G = (int)(need < most ? need : most);
+    if (a.G < 1) a.G = 1;
+  }
+  if ((long long)a.G * h->R > cap)
+    return fail(RA_ERR_UNSUPPORTED, "pipelined grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
+  a.J = pipeline_slices(h, a.plan, a.G);
+  if (region_entries(h, ra::kSyncFlags, a.rounds, a.G, a.J) > reg->cap)
+    return fail(RA_ERR_UNSUPPORTED, "too many channels or sub-slices for the progress flags");
+  s = prepare_region(*reg, a.G, a.J, st);
+  if (s != RA_OK) return s;
+  a.slots = reg->d;
+  a.epoch = (uint64_t)(reg->calls + 1);
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
+  a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
+  cudaError_t e = ra::launch_pipelined(h->dtype, h->op, a, ra::kPersistThreads, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pipelined kernel launch");
+  reg->calls += 1;
+  h->last_sync = ra::kSyncFlags;
   h->last_kind = kind;
   return RA_OK;
 }
 
 ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(h->d_err, 0, sizeof(ra_device_error), st);
-  if (e == cudaSuccess && h->d_slots) {
-    size_t total = 0;
-    for (auto& r : h->region) total += r.cap;
-    e = cudaMemsetAsync(h->d_slots, 0, total * sizeof(uint64_t), st);
-  }
+  for (auto& row : h->region)
+    for (auto& reg : row)
+      if (e == cudaSuccess && reg.d && reg.cap) e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "device state reset");
-  for (auto& r : h->region) r.calls = 0;
+  for (auto& row : h->region)
+    for (auto& reg : row) reg.calls = 0;
   return RA_OK;
 }
 
@@ -433,8 +546,9 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   int coop = 0;
   e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  int bps = 0;
+  int bps = 0, pbps = 0;
   e = ra::persistent_blocks_per_sm(dtype, op, ra::kPersistThreads, &bps);
+  if (e == cudaSuccess) e = ra::pipelined_blocks_per_sm(dtype, op, ra::kPersistThreads, &pbps);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   e = ra::prepare_ag_round();
   if (e != cudaSuccess) return cuda_fail(e, "AllGather kernel set-up");
@@ -448,16 +562,18 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   h->device = dev;
   h->num_sms = sms;
   h->persist_blocks_per_sm = coop ? bps : 0;
+  h->pipe_blocks_per_sm = coop ? pbps : 0;
 
-  // signal slots: per kind, the most channels that can be co-resident x
-  // barrier rounds x waiters
-  const size_t gmax = (size_t)(bps > 0 ? bps : 1) * (size_t)sms / (size_t)R + 1;
+  // counting-barrier slots: per kind, the most channels that can be
+  // co-resident x barrier rounds x waiters (the other schemes allocate theirs
+  // on first use)
+  const int gmax = gmax_channels(h, bps);
   const int rounds[3] = {2 * (R - 1), R - 1, R - 1};
   size_t total = 0;
   for (int k = 0; k < 3; ++k) {
-    h->region[k].rounds = rounds[k];
-    h->region[k].cap = gmax * (size_t)(rounds[k] > 1 ? rounds[k] - 1 : 0) * (size_t)R;
-    total += h->region[k].cap;
+    for (int sy = 0; sy < 3; ++sy) h->region[sy][k].rounds = rounds[k];
+    h->region[ra::kSyncCounting][k].cap = region_entries(h, ra::kSyncCounting, rounds[k], gmax, 1);
+    total += h->region[ra::kSyncCounting][k].cap;
   }
   if (total > 0) {
     e = cudaMalloc(&h->d_slots, total * sizeof(uint64_t));
@@ -472,7 +588,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
       return cuda_fail(e, "signal slot init");
     }
     size_t o = 0;
-    for (auto& r : h->region) {
+    for (auto& r : h->region[ra::kSyncCounting]) {
       r.d = h->d_slots + o;
       o += r.cap;
     }
@@ -498,6 +614,9 @@ ra_status ra_destroy(ra_handle h) {
   if (e != cudaSuccess) s = cuda_fail(e, "synchronise before destroy");
   drop_ring_graph(h);
   if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
+  for (auto& row : h->region)
+    for (auto& reg : row)
+      if (reg.owned && reg.d) cudaFree(reg.d);
   if (h->d_slots) cudaFree(h->d_slots);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
@@ -522,6 +641,8 @@ ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, voi
       return run_ring(h, kKindAllReduce, in, out, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
+    case RA_VARIANT_PIPELINED:
+      return run_pipelined(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
     default:
       return run_direct(h, ra::kModeAllReduce, in, out, st);
   }
@@ -545,6 +666,8 @@ ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out
       return run_ring(h, kKindReduceScatter, in, out, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
+    case RA_VARIANT_PIPELINED:
+      return run_pipelined(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
     default:
       return run_direct(h, ra::kModeReduceScatter, in, out, st);
   }
@@ -564,6 +687,8 @@ ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
       return run_ring(h, kKindAllGather, nullptr, buf, st);
     case RA_VARIANT_PERSISTENT:
       return run_persistent(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
+    case RA_VARIANT_PIPELINED:
+      return run_pipelined(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
     default:
       return run_direct(h, ra::kModeAllGather, buf, buf, st);
   }
@@ -593,11 +718,21 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       h->use_graphs = value != 0;
       return RA_OK;
     case RA_OPT_VARIANT:
-      if (value < RA_VARIANT_AUTO || value > RA_VARIANT_PERSISTENT)
+      if (value < RA_VARIANT_AUTO || value > RA_VARIANT_PIPELINED)
         return fail(RA_ERR_INVALID, "unknown variant %lld", value);
-      if (value == RA_VARIANT_PERSISTENT && h->persist_blocks_per_sm == 0)
+      if ((value == RA_VARIANT_PERSISTENT && h->persist_blocks_per_sm == 0) ||
+          (value == RA_VARIANT_PIPELINED && h->pipe_blocks_per_sm == 0))
         return fail(RA_ERR_UNSUPPORTED, "device has no cooperative launch");
       h->variant = (int)value;
+      return RA_OK;
+    case RA_OPT_BARRIER:
+      if (value != RA_BARRIER_COUNTING && value != RA_BARRIER_PER_PEER)
+        return fail(RA_ERR_INVALID, "unknown barrier %lld", value);
+      h->barrier = (int)value;
+      return RA_OK;
+    case RA_OPT_SLICES:
+      if (value < 0 || value > kMaxSlices) return fail(RA_ERR_INVALID, "slices %lld outside [0, %d]", value, kMaxSlices);
+      h->slices = (int)value;
       return RA_OK;
     case RA_OPT_TIMEOUT_NS:
       if (value < 1000) return fail(RA_ERR_INVALID, "timeout %lld ns below 1 us", value);
@@ -628,6 +763,8 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_CHECK_POINTERS: *value = h->check_pointers; return RA_OK;
     case RA_OPT_SKIP_ARRIVAL: *value = h->skip; return RA_OK;
     case RA_OPT_GRAPHS: *value = h->use_graphs; return RA_OK;
+    case RA_OPT_BARRIER: *value = h->barrier; return RA_OK;
+    case RA_OPT_SLICES: *value = h->slices; return RA_OK;
     default: return fail(RA_ERR_INVALID, "unknown option %d", key);
   }
 }
@@ -645,11 +782,15 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) 
   if (rec.code == 0) return RA_OK;
   ra_status s = reset_device_state(h, st);
   if (s != RA_OK) return s;
+  const char* what = rec.code == 1 ? "counting barrier"
+                     : rec.code == 2 ? "bulk copy"
+                     : rec.code == 3 ? "per-peer barrier"
+                     : "predecessor flag";
   return fail(RA_ERR_TIMEOUT,
-              "device wait gave up: %s, round %d, rank %d, channel %d, observed %llu of %llu (%llu missing)",
-              rec.code == 1 ? "barrier" : "bulk copy", rec.round, rec.rank, rec.channel,
-              (unsigned long long)rec.observed, (unsigned long long)rec.expected,
-              (unsigned long long)(rec.expected - rec.observed));
+              "device wait gave up: %s, round %d, rank %d, channel %d, peer %d, observed %llu of %llu "
+              "(%llu missing)",
+              what, rec.round, rec.rank, rec.channel, rec.peer, (unsigned long long)rec.observed,
+              (unsigned long long)rec.expected, (unsigned long long)(rec.expected - rec.observed));
 }
 
 ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count, int* channels, int* rounds,
@@ -663,17 +804,16 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
     if (calls) *calls = 0;
     return RA_OK;
   }
-  const SlotRegion& reg = h->region[h->last_kind];
-  const int br = reg.rounds > 1 ? reg.rounds - 1 : 0;
-  const size_t need = (size_t)reg.G * (size_t)br * (size_t)h->R;
+  const SlotRegion& reg = h->region[h->last_sync][h->last_kind];
+  const size_t need = region_entries(h, h->last_sync, reg.rounds, reg.G, reg.J);
   *count = need;
   if (channels) *channels = reg.G;
-  if (rounds) *rounds = br;
+  if (rounds) *rounds = h->last_sync == ra::kSyncFlags ? reg.rounds : (reg.rounds > 1 ? reg.rounds - 1 : 0);
   if (calls) *calls = reg.calls;
   if (!dst || need == 0) return RA_OK;  // sizes only
   if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess && need) e = cudaMemcpy(dst, reg.d, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(dst, reg.d, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "signal read");
   return RA_OK;
 }

@@ -54,16 +54,27 @@ struct CopyArgs {
   ra_device_error* err;
 };
 
-// Persistent variant: one cooperative launch of R*G CTAs (G channels).
+// How the ranks of a channel synchronise between rounds.
+enum Sync : int {
+  kSyncCounting = 0,   // one slot per (channel, round, waiter); each peer adds 1
+  kSyncPerPeer = 1,    // one slot per (channel, round, waiter, peer); each peer stores the epoch
+  kSyncFlags = 2       // pipelined variant: one progress flag per (channel, rank, sub-slice)
+};
+
+// Persistent and pipelined variants: one cooperative launch of R*G CTAs
+// (G channels).
 struct PersistArgs {
   Ptrs p;
   Plan plan;
   int R;
   int G;
+  int J;                // sub-slices per channel slice (pipelined variant)
   int mode;
+  int sync;             // Sync
   int rounds;           // ring rounds this call runs
-  uint64_t* slots;      // [G][rounds-1][R] signal slots of this call's kind
-  uint64_t epoch;       // calls of this kind since the slots were zeroed, this one included
+  uint64_t* slots;      // counting: [G][rounds-1][R]; per-peer: [G][rounds-1][R][R];
+                        // flags: [G][R][J]
+  uint64_t epoch;       // calls on this slot array since it was zeroed, this one included
   int64_t timeout_ns;
   ra_device_error* err;
   int skip_rank;        // failure injection: rank withholding one arrival, -1 = none
@@ -81,6 +92,8 @@ cudaError_t prepare_ag_round();
 cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
 // Co-resident CTAs per SM of the persistent kernel for `threads` threads.
 cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks);
+cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
+cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks);
 
 constexpr int kDirectThreads = 256;
 constexpr int kRoundThreads = 256;

@@ -62,20 +62,73 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
       }
       if (load_relaxed_u32(&a.err->code) != 0u) { abort = 1; break; }
       if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
-        if (atomicCAS(&a.err->code, 0u, 1u) == 0u) {
-          a.err->round = t;
-          a.err->rank = r;
-          a.err->channel = g;
-          a.err->observed = seen;
-          a.err->expected = target;
-          __threadfence();
-        }
+        // one counting slot cannot say which peer is late: peer = -1
+        record_wait_error(a.err, 1u, t, r, g, -1, seen, target);
         abort = 1;
         break;
       }
       if (it > 32) __nanosleep(100);
     }
     *s_abort = abort;
+  }
+  __syncthreads();
+  return *s_abort == 0;
+}
+
+// Per-peer barrier round, the design the counting barrier replaced ("comm:
+// lift the GIN scale-out ceiling ...", section "Problem" and the comparison in
+// section "Performance"): every waiter has one slot per peer; a peer stores
+// the call's epoch into its own slot of each waiter, and the waiter checks all
+// R-1 slots, one lane of warp 0 per peer.  A wait that runs out can name the
+// peer that did not arrive.
+__device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
+  __syncthreads();
+  const int R = a.R;
+  uint64_t* round_slots = a.slots + ((int64_t)g * (a.rounds - 1) + t) * R * R;   // [waiter][peer]
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();   // release: this round's stores of the whole CTA
+    if (!(r == a.skip_rank && t == a.skip_round)) {
+      for (int q = 0; q < R; ++q)
+        if (q != r) signal_store_relaxed(round_slots + (int64_t)q * R + r, a.epoch);
+    }
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const uint64_t* mine = round_slots + (int64_t)r * R;
+    const bool active = lane < R && lane != r;
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+    int abort = 0;
+    for (uint64_t it = 0;; ++it) {
+      bool ok = true;
+      uint64_t v = 0;
+      if (active) {
+        v = signal_load_relaxed(mine + lane);
+        ok = rolling_reached(v, a.epoch);
+      }
+      const unsigned missing = __ballot_sync(0xffffffffu, !ok);
+      if (missing == 0u) {
+        fence_acq_rel_gpu();   // acquire, by every lane that observed a slot
+        break;
+      }
+      int stop = 0;
+      if (lane == 0) {
+        if (load_relaxed_u32(&a.err->code) != 0u)
+          stop = 1;
+        else if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters)
+          stop = 2;
+      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (stop) {
+        if (stop == 2 && lane == 0)
+          record_wait_error(a.err, 3u, t, r, g, __ffs(missing) - 1, (uint64_t)(R - 1 - __popc(missing)),
+                            (uint64_t)(R - 1));
+        abort = 1;
+        break;
+      }
+      if (it > 32) __nanosleep(100);
+    }
+    if (lane == 0) *s_abort = abort;
   }
   __syncthreads();
   return *s_abort == 0;
@@ -155,7 +208,11 @@ persistent_kernel(const PersistArgs a) {
         copy_slice<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), off, end, g, G);
       }
     }
-    if (t + 1 < a.rounds && !counting_barrier(a, g, t, r, &s_abort)) return;
+    if (t + 1 < a.rounds) {
+      const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
+                                              : counting_barrier(a, g, t, r, &s_abort);
+      if (!go) return;
+    }
   }
 }
 

@@ -1,0 +1,193 @@
+// ra_pipelined.cu -- the pipelined variant: every ring round in one
+// cooperative launch, and no barrier -- each rank waits only for its
+// predecessor, one sub-slice at a time.
+//
+// "Why AllReduce = ReduceScatter + AllGather -- NCCL Ring AllReduce",
+// section 4: a rank receives only from its predecessor.  So instead of
+// stopping every rank at a barrier after each round, rank r starts round T on
+// a piece of its chunk as soon as rank r-1 has finished round T-1 on the
+// same piece.  The pieces: CTA g of each rank (channel g) owns the g-th slice
+// of the round's chunk, cut into J sub-slices; each (channel, rank, sub-slice)
+// has a progress flag holding how many rounds that rank has finished on it.
+// Different sub-slices of one rank can be in different rounds, so rounds
+// overlap along the ring, as NCCL pipelines a ring by slices.
+//
+// Why waiting on the predecessor alone is safe.  A rank's output buffer is
+// the "message" its successor reads, and one place of it is written twice:
+// chunk (r - t) holds the partial of ReduceScatter round t and, R rounds
+// later (AllGather round t + 1), the complete value.  Rank r can start round
+// T only once rank r-1 has finished round T-1, which needed rank r-2 to have
+// finished T-2, and so on round the ring to rank r+1 having finished
+// T-(R-1).  For T = R + t that is round t + 1, in which r+1 read the partial:
+// the overwrite can never overtake the read it would spoil.  Reads of inputs
+// in round 1 need no wait at all.
+//
+// Flags are never cleared between calls: the k-th call on a flag array
+// starts from (k-1) * rounds, compared in 64-bit rolling order.  Waits are
+// bounded; one that runs out records (round, rank, channel, predecessor,
+// observed, expected) and the CTA returns, and every other waiter returns
+// at its next poll.  Data another CTA wrote is read through L2.
+#include "ra_device.cuh"
+
+namespace ra {
+
+// Thread 0 waits until *flag reaches target; false when the CTA must stop.
+__device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* flag, uint64_t target, int t,
+                                          int r, int g, int pred, int* s_abort) {
+  if (threadIdx.x == 0) {
+    int abort = 0;
+    uint64_t seen = signal_load_relaxed(flag);
+    if (!rolling_reached(seen, target)) {
+      const uint64_t t0 = globaltimer_ns();
+      const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+      for (uint64_t it = 0;; ++it) {
+        if (it > 16) __nanosleep(64);
+        seen = signal_load_relaxed(flag);
+        if (rolling_reached(seen, target)) break;
+        if (load_relaxed_u32(&a.err->code) != 0u) {
+          abort = 1;
+          break;
+        }
+        if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
+          record_wait_error(a.err, 4u, t, r, g, pred, seen, target);
+          abort = 1;
+          break;
+        }
+      }
+    }
+    if (!abort) fence_acq_rel_gpu();   // acquire: the predecessor's sub-slice is visible
+    *s_abort = abort;
+  }
+  __syncthreads();
+  return *s_abort == 0;
+}
+
+// All threads' stores of the sub-slice are done; thread 0 publishes.
+__device__ __forceinline__ void publish_flag(uint64_t* flag, uint64_t value, bool withhold) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();   // release
+    if (!withhold) signal_store_relaxed(flag, value);
+  }
+}
+
+template <class D, int OP>
+__device__ __forceinline__ void reduce_range(const typename D::T* inc, const typename D::T* loc, typename D::T* dst,
+                                             int64_t qb, int64_t qe, const Span<D::kVec>& sp, bool scalars) {
+  for (int64_t v = qb + threadIdx.x; v < qe; v += blockDim.x) {
+    const uint4 x = ld_l2(reinterpret_cast<const uint4*>(inc) + v);
+    const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
+    st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+  }
+  if (scalars) {
+    const int64_t ns = sp.scalar_count();
+    for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
+      const int64_t i = sp.scalar_at(t);
+      dst[i] = Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i));
+    }
+  }
+}
+
+template <class D>
+__device__ __forceinline__ void copy_range(const typename D::T* src, typename D::T* dst, int64_t qb, int64_t qe,
+                                           const Span<D::kVec>& sp, bool scalars) {
+  for (int64_t v = qb + threadIdx.x; v < qe; v += blockDim.x)
+    st_l2(reinterpret_cast<uint4*>(dst) + v, ld_l2(reinterpret_cast<const uint4*>(src) + v));
+  if (scalars) {
+    const int64_t ns = sp.scalar_count();
+    for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
+      const int64_t i = sp.scalar_at(t);
+      dst[i] = ld_l2_scalar(src + i);
+    }
+  }
+}
+
+template <class D, int OP>
+__global__ void __launch_bounds__(kPersistThreads)
+pipelined_kernel(const PersistArgs a) {
+  using T = typename D::T;
+  constexpr int V = D::kVec;
+  __shared__ int s_abort;
+  const int R = a.R, G = a.G, J = a.J;
+  const int r = blockIdx.x % R;
+  const int g = blockIdx.x / R;
+  const int p = (r == 0) ? R - 1 : r - 1;
+  uint64_t* mine = a.slots + ((int64_t)g * R + r) * J;
+  const uint64_t* pred = a.slots + ((int64_t)g * R + p) * J;
+  const uint64_t base = (a.epoch - 1) * (uint64_t)a.rounds;
+  for (int t = 0; t < a.rounds; ++t) {
+    bool reduce;
+    int s;
+    if (a.mode == kModeAllGather) {
+      reduce = false;
+      s = t + 1;
+    } else if (t < R - 1) {
+      reduce = true;
+      s = t + 1;
+    } else {
+      reduce = false;
+      s = t - (R - 1) + 1;
+    }
+    int c = reduce ? (r - s) : (r + 1 - s);
+    c %= R;
+    if (c < 0) c += R;
+    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
+    const int64_t end = min(off + a.plan.C, a.plan.n);
+    const Span<V> sp(off, end);
+    int64_t pb, pe;
+    split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
+    // failure injection: a flag counts finished rounds, so a rank that is
+    // to fall silent withholds every publication from that round on
+    const bool withhold = (r == a.skip_rank && t >= a.skip_round);
+    for (int j = 0; j < J; ++j) {
+      int64_t qb, qe;
+      split_vectors(pb, pe, j, J, &qb, &qe);
+      // round 0 reads inputs only; every later round reads what the
+      // predecessor wrote in its previous round on this sub-slice
+      if (t > 0 && !wait_flag(a, pred + j, base + t, t, r, g, p, &s_abort)) return;
+      const bool scalars = (g == 0 && j == 0);
+      if (off < end) {
+        if (reduce) {
+          const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
+          reduce_range<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), qb, qe, sp,
+                              scalars);
+        } else {
+          copy_range<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), qb, qe, sp, scalars);
+        }
+      }
+      publish_flag(mine + j, base + t + 1, withhold);
+    }
+  }
+}
+
+template <class D, int OP>
+static const void* pipelined_fn() {
+  return reinterpret_cast<const void*>(&pipelined_kernel<D, OP>);
+}
+
+static const void* pipelined_select(int dtype, int op) {
+  switch (dtype * 2 + op) {
+    case RA_F32 * 2 + RA_SUM: return pipelined_fn<DF32, kOpSum>();
+    case RA_F32 * 2 + RA_MAX: return pipelined_fn<DF32, kOpMax>();
+    case RA_BF16 * 2 + RA_SUM: return pipelined_fn<DBF16, kOpSum>();
+    case RA_BF16 * 2 + RA_MAX: return pipelined_fn<DBF16, kOpMax>();
+    case RA_I32 * 2 + RA_SUM: return pipelined_fn<DI32, kOpSum>();
+    case RA_I32 * 2 + RA_MAX: return pipelined_fn<DI32, kOpMax>();
+    default: return nullptr;
+  }
+}
+
+cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
+  const void* fn = pipelined_select(dtype, op);
+  if (!fn) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
+}
+
+cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
+  const void* fn = pipelined_select(dtype, op);
+  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<PersistArgs*>(&a)};
+  return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
+}
+
+}  // namespace ra

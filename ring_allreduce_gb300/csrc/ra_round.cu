@@ -135,14 +135,7 @@ ag_round_kernel(const CopyArgs a) {
   for (int i = 0; i < count; ++i) {
     const int st = i % kStages;
     if (!wait_tile(&bars[st], (uint32_t)((i / kStages) & 1), a.timeout_ns)) {
-      if (atomicCAS(&a.err->code, 0u, 2u) == 0u) {
-        a.err->round = s;
-        a.err->rank = r;
-        a.err->channel = blockIdx.x;
-        a.err->observed = (uint64_t)i;
-        a.err->expected = (uint64_t)count;
-        __threadfence();
-      }
+      record_wait_error(a.err, 2u, s, r, blockIdx.x, -1, (uint64_t)i, (uint64_t)count);
       ok = false;
       break;
     }

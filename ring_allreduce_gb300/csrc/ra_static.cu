@@ -131,6 +131,8 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   a.R = R;
   a.G = (int)G;
   a.mode = kModeAllReduce;
+  a.sync = kSyncCounting;
+  a.J = 1;
   a.rounds = 2 * (R - 1);
   a.slots = scratch + kStaticErrWords;
   a.epoch = 1;

@@ -14,7 +14,7 @@ from rahelpers import DeviceRanks, assert_bitwise_equal
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-VARIANTS = ["direct", "ring", "persistent"]
+VARIANTS = ["direct", "ring", "persistent", "pipelined"]
 DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
              ("i32", "sum"), ("i32", "max")]
 # (R, n): degenerate, n < R, ragged, several tiles per chunk with a ragged tail
@@ -35,7 +35,7 @@ def _dist(dtype):
     return {"f32": "normal", "bf16": "grad", "i32": "int20"}[dtype]
 
 
-def run_gpu(ra, x, dtype, op, variant, kind="allreduce", inplace=False, ctas=0, repeat=1):
+def run_gpu(ra, x, dtype, op, variant, kind="allreduce", inplace=False, ctas=0, repeat=1, options=()):
     R, n = len(x), len(x[0])
     st = inputs.storage_dtype(dtype)
     inp = DeviceRanks(R, n, st, host=x)
@@ -43,6 +43,8 @@ def run_gpu(ra, x, dtype, op, variant, kind="allreduce", inplace=False, ctas=0, 
     with ra.RingAllReduce(R, n, dtype, op, variant=variant) as h:
         if ctas:
             h.set_option(ra.Option.CTAS, ctas)
+        for key, value in options:
+            h.set_option(key, value)
         for _ in range(repeat):
             if kind == "allreduce":
                 h.allreduce(inp.views, out.views)
@@ -134,7 +136,7 @@ def test_launch_shapes(ra, variant, ctas):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for R, n in ((8, 2**20 + 7), (3, 100003)):
         x = inputs.generate(R, n, "bf16", "grad", seed=ctas)
-        if variant == "persistent" and R * ctas > sms:
+        if variant in ("persistent", "pipelined") and R * ctas > sms:
             # more channels than can be co-resident: refused on the host
             with pytest.raises(ra.RAError) as e:
                 run_gpu(ra, x, "bf16", "sum", variant, ctas=4 * sms)
@@ -192,8 +194,9 @@ def test_barrier_exactly_r_minus_1_arrivals(ra, R, G):
             h.allreduce(inp.views, out.views)
             slots, ch, rounds, calls = h.read_signals()
             assert (ch, rounds, calls) == (G, barrier.barrier_rounds(R), k)
+            assert len(slots) == G * rounds * R
             exp = barrier.expected_slot_value(R, k)
-            assert all(v == exp for g in slots for t in g for v in t), slots
+            assert all(v == exp for v in slots), slots
         status, _ = h.device_status()
         assert status == ra.Status.OK
     got = out.host()
@@ -336,3 +339,111 @@ def test_calls_inside_a_caller_graph(ra, variant):
         assert h.device_status()[0] == ra.Status.OK
     finally:
         h.close()
+
+
+
+@pytest.mark.parametrize("dtype,op", DTYPE_OPS)
+def test_per_peer_barrier_matches_oracle(ra, dtype, op):
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=600 + i)
+        want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, dtype, op, "persistent", options=[(ra.Option.BARRIER, ra.Barrier.PER_PEER)])
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"per-peer {dtype}/{op} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("slices", [1, 2, 7, 64])
+def test_pipelined_sub_slices(ra, slices):
+    o = elementops.get_op("bf16", "sum")
+    for R, n in ((8, 2**20 + 7), (3, 100003), (16, 2**16 + 3)):
+        x = inputs.generate(R, n, "bf16", "grad", seed=slices)
+        want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, "bf16", "sum", "pipelined", options=[(ra.Option.SLICES, slices)])
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"slices={slices} R={R}")
+
+
+@pytest.mark.parametrize("R,G", [(2, 1), (5, 3), (8, 4)])
+def test_per_peer_slots_and_pipelined_flags(ra, R, G):
+    """Per-peer barrier: after k calls every (waiter, peer) slot holds k and
+    a waiter's own slot 0.  Pipelined: every (channel, rank, sub-slice) flag
+    holds k * rounds."""
+    n = R * 7000 + 3
+    x = inputs.generate(R, n, "f32", "normal", 9)
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    for variant in ("persistent", "pipelined"):
+        out = DeviceRanks(R, n, np.float32)
+        with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
+            h.set_option(ra.Option.CTAS, G)
+            if variant == "persistent":
+                h.set_option(ra.Option.BARRIER, ra.Barrier.PER_PEER)
+            else:
+                h.set_option(ra.Option.SLICES, 3)
+            for k in range(1, 4):
+                h.allreduce(inp.views, out.views)
+                slots, ch, rounds, calls = h.read_signals()
+                assert (ch, calls) == (G, k)
+                if variant == "persistent":
+                    assert rounds == barrier.barrier_rounds(R) and len(slots) == G * rounds * R * R
+                    for idx, v in enumerate(slots):
+                        waiter, peer = (idx // R) % R, idx % R
+                        assert v == (0 if waiter == peer else k), (idx, v)
+                else:
+                    assert rounds == 2 * (R - 1) and len(slots) == G * R * 3
+                    assert all(v == k * rounds for v in slots), slots
+            assert h.device_status()[0] == ra.Status.OK
+        got = out.host()
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], variant)
+
+
+def test_per_peer_timeout_names_the_missing_peer(ra):
+    R, n = 4, 4 * 4096
+    x = inputs.generate(R, n, "f32", "normal", 8)
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    out = DeviceRanks(R, n, np.float32)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="persistent") as h:
+        h.set_option(ra.Option.BARRIER, ra.Barrier.PER_PEER)
+        h.set_option(ra.Option.TIMEOUT_NS, 20_000_000)
+        last = barrier.barrier_rounds(R) - 1
+        h.set_option(ra.Option.SKIP_ARRIVAL, (2 << 16) | last)
+        h.allreduce(inp.views, out.views)
+        status, err = h.device_status()
+        assert status == ra.Status.ERR_TIMEOUT
+        assert err.code == 3 and err.round == last and err.rank != 2
+        assert err.peer == 2, "a per-peer slot names the rank that did not arrive"
+        assert err.expected - err.observed == 1
+        h.set_option(ra.Option.SKIP_ARRIVAL, -1)
+        h.allreduce(inp.views, out.views)
+        assert h.device_status()[0] == ra.Status.OK
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
+
+
+def test_pipelined_timeout_names_the_predecessor(ra):
+    """A rank that stops publishing progress from the next-to-last round on
+    leaves exactly its successor waiting in the last round."""
+    R, n = 4, 4 * 4096
+    x = inputs.generate(R, n, "f32", "normal", 8)
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    out = DeviceRanks(R, n, np.float32)
+    rounds = 2 * (R - 1)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.TIMEOUT_NS, 20_000_000)
+        h.set_option(ra.Option.SKIP_ARRIVAL, (2 << 16) | (rounds - 2))
+        h.allreduce(inp.views, out.views)
+        status, err = h.device_status()
+        assert status == ra.Status.ERR_TIMEOUT
+        assert err.code == 4 and err.rank == 3 and err.peer == 2 and err.round == rounds - 1
+        assert err.expected - err.observed == 1
+        h.set_option(ra.Option.SKIP_ARRIVAL, -1)
+        h.allreduce(inp.views, out.views)
+        assert h.device_status()[0] == ra.Status.OK
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
