@@ -187,7 +187,8 @@ def _device_ranks(torch, R, n, np_dtype, host=None):
     rank's base is 16-byte aligned."""
     import numpy as np
     tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.uint16): torch.int16,
-           np.dtype(np.int32): torch.int32}[np.dtype(np_dtype)]
+           np.dtype(np.int32): torch.int32, np.dtype(np.float16): torch.float16,
+           np.dtype(np.float64): torch.float64, np.dtype(np.int64): torch.int64}[np.dtype(np_dtype)]
     stride = ((n + 63) // 64) * 64
     big = torch.empty((R, stride), dtype=tdt, device="cuda")
     if host is not None:

@@ -24,11 +24,12 @@
  *               AllGather send.
  *
  * Results are bitwise the ones of that ring for every dtype: the fold order
- * of each element is fixed, bf16 partials are rounded to bf16
- * (round-to-nearest-even) at every hop, as a ring carrying bf16 messages
- * would store them, fp32 additions are single IEEE binary32 additions with
- * no contraction and no flush to zero, int32 sums wrap.  MAX keeps the
- * incoming partial unless the local value is strictly greater.
+ * of each element is fixed; bf16 and fp16 partials are rounded
+ * (round-to-nearest-even) to their format at every hop, as a ring carrying
+ * such messages would store them, each hop being one binary32 addition of
+ * the exactly widened operands; fp32 and fp64 additions are single IEEE
+ * additions with no contraction and no flush to zero; integer sums wrap.
+ * MAX keeps the incoming partial unless the local value is strictly greater.
  *
  * Buffers and ownership
  *   - The caller owns every buffer.  in[r] and out[r] (r = 0..R-1) are
@@ -57,7 +58,7 @@
  * Edge cases: n == 0 is a no-op returning RA_OK (the buffer pointers are not
  * looked at, NULL included).  R == 1 copies in[0] to
  * out[0].  R outside [1, 32], a NULL or misaligned pointer, an unknown dtype
- * or op return RA_ERR_INVALID.
+ * or op return RA_ERR_INVALID.  Every dtype supports RA_SUM and RA_MAX.
  */
 #ifndef RING_ALLREDUCE_GB300_RA_H
 #define RING_ALLREDUCE_GB300_RA_H
@@ -78,7 +79,14 @@ typedef enum ra_status {
   RA_ERR_TIMEOUT = 5       /* a device-side wait gave up (see ra_get_device_status) */
 } ra_status;
 
-typedef enum ra_dtype { RA_F32 = 0, RA_BF16 = 1, RA_I32 = 2 } ra_dtype;
+typedef enum ra_dtype {
+  RA_F32 = 0,   /* IEEE binary32 */
+  RA_BF16 = 1,  /* bfloat16 (16-bit patterns) */
+  RA_I32 = 2,   /* int32, sums wrap */
+  RA_F16 = 3,   /* IEEE binary16 */
+  RA_F64 = 4,   /* IEEE binary64 */
+  RA_I64 = 5    /* int64, sums wrap */
+} ra_dtype;
 typedef enum ra_op { RA_SUM = 0, RA_MAX = 1 } ra_op;
 
 /* Which kernels carry out a call.  All give bitwise the same result. */

@@ -18,11 +18,16 @@ format; the readings below are the plain ones):
   exactly, added in binary32 and the sum is rounded to bf16 with
   round-to-nearest-even.  binary32 carries 24 significand bits, at least
   2*8+2, so this double rounding gives the correctly rounded bf16 sum.
-* int32 SUM: two's-complement wrap-around.
+* fp16 SUM: as bf16: both operands widened exactly to binary32, one
+  binary32 addition, rounded to the nearest fp16, ties to even (24 >= 2*11+2,
+  so this double rounding is the correctly rounded fp16 sum).
+* fp64 SUM: one IEEE binary64 addition.
+* int32 / int64 SUM: two's-complement wrap-around.
 * MAX (every dtype): ``local if local > incoming else incoming``; on a tie,
   or when the comparison is false (NaN), the incoming partial is kept.
 
-bf16 values are held as their 16-bit patterns in ``numpy.uint16`` arrays.
+bf16 values are held as their 16-bit patterns in ``numpy.uint16`` arrays;
+fp16 values in ``numpy.float16`` arrays.
 """
 
 import numpy as np
@@ -112,6 +117,55 @@ class I32Max(_Op):
         return np.where(local > incoming, local, incoming).astype(np.int32)
 
 
+class F16Sum(_Op):
+    name, storage, itemsize = "f16_sum", np.float16, 2
+
+    def combine(self, incoming, local):
+        wide = np.add(np.asarray(incoming, dtype=np.float16).astype(np.float32),
+                      np.asarray(local, dtype=np.float16).astype(np.float32), dtype=np.float32)
+        with np.errstate(over="ignore"):      # a sum beyond fp16's range rounds to infinity
+            return wide.astype(np.float16)
+
+
+class F16Max(_Op):
+    name, storage, itemsize = "f16_max", np.float16, 2
+
+    def combine(self, incoming, local):
+        take_local = np.asarray(local, np.float16).astype(np.float32) > np.asarray(incoming, np.float16).astype(np.float32)
+        return np.where(take_local, local, incoming).astype(np.float16)
+
+
+class F64Sum(_Op):
+    name, storage, itemsize = "f64_sum", np.float64, 8
+
+    def combine(self, incoming, local):
+        return np.add(incoming, local, dtype=np.float64)
+
+
+class F64Max(_Op):
+    name, storage, itemsize = "f64_max", np.float64, 8
+
+    def combine(self, incoming, local):
+        return np.where(local > incoming, local, incoming).astype(np.float64)
+
+
+class I64Sum(_Op):
+    name, storage, itemsize = "i64_sum", np.int64, 8
+
+    def combine(self, incoming, local):
+        # unsigned addition wraps modulo 2^64; reinterpreted as two's complement
+        u = np.add(np.asarray(incoming, np.int64).view(np.uint64), np.asarray(local, np.int64).view(np.uint64),
+                   dtype=np.uint64)
+        return u.view(np.int64)
+
+
+class I64Max(_Op):
+    name, storage, itemsize = "i64_max", np.int64, 8
+
+    def combine(self, incoming, local):
+        return np.where(local > incoming, local, incoming).astype(np.int64)
+
+
 class Sym(_Op):
     """Symbolic elements for the page's worked example.
 
@@ -137,12 +191,18 @@ OPS = {
     ("bf16", "max"): BF16Max(),
     ("i32", "sum"): I32Sum(),
     ("i32", "max"): I32Max(),
+    ("f16", "sum"): F16Sum(),
+    ("f16", "max"): F16Max(),
+    ("f64", "sum"): F64Sum(),
+    ("f64", "max"): F64Max(),
+    ("i64", "sum"): I64Sum(),
+    ("i64", "max"): I64Max(),
 }
 
 
 def get_op(dtype, op):
-    """Return the reduction for ``dtype`` in {"f32", "bf16", "i32"} and
-    ``op`` in {"sum", "max"}."""
+    """Return the reduction for ``dtype`` in {"f32", "bf16", "i32", "f16",
+    "f64", "i64"} and ``op`` in {"sum", "max"}."""
     try:
         return OPS[(dtype, op)]
     except KeyError:

@@ -35,6 +35,9 @@ class DType(enum.IntEnum):
     F32 = 0
     BF16 = 1
     I32 = 2
+    F16 = 3
+    F64 = 4
+    I64 = 5
 
 
 class Op(enum.IntEnum):
@@ -245,7 +248,8 @@ def ra_read_signals(h):
     return list(buf)[:count.value], ch.value, rd.value, calls.value
 
 
-_DTYPES = {"f32": DType.F32, "bf16": DType.BF16, "i32": DType.I32}
+_DTYPES = {"f32": DType.F32, "bf16": DType.BF16, "i32": DType.I32, "f16": DType.F16, "f64": DType.F64,
+           "i64": DType.I64}
 _OPS = {"sum": Op.SUM, "max": Op.MAX}
 
 

@@ -23,6 +23,11 @@ LIB_NAME = "libra_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_pipelined.cu", "ra_static.cu"]
+# (source, object stem, preprocessor definitions): ra_direct_inst.cu is
+# compiled once per dtype so its instantiations build in parallel
+DTYPES = ["RA_F32", "RA_BF16", "RA_I32", "RA_F16", "RA_F64", "RA_I64"]
+UNITS = ([(src, os.path.splitext(src)[0], {}) for src in SOURCES] +
+         [("ra_direct_inst.cu", "ra_direct_" + dt[3:].lower(), {"RA_INST_DTYPE": dt}) for dt in DTYPES])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE arithmetic throughout: no fast-math, no flush to zero, no contraction.
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-ftz=false",
@@ -45,7 +50,7 @@ def _inputs():
 
 # The files each kernel's device code is built from.
 KERNEL_SOURCES = {
-    "direct": ["ra_direct.cu", "ra_device.cuh", "ra_internal.h"],
+    "direct": ["ra_direct.cu", "ra_direct.cuh", "ra_direct_inst.cu", "ra_device.cuh", "ra_internal.h"],
     "round": ["ra_round.cu", "ra_device.cuh", "ra_internal.h"],
     "persistent": ["ra_persistent.cu", "ra_device.cuh", "ra_internal.h"],
     "pipelined": ["ra_pipelined.cu", "ra_device.cuh", "ra_internal.h"],
@@ -88,15 +93,16 @@ def build(force=False, verbose=None, jobs=None):
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
-               os.path.join(CSRC, src), "-o", obj]
+    def compile_one(unit):
+        src, stem, defs = unit
+        obj = os.path.join(BUILD_DIR, stem + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, *[f"-D{k}={v}" for k, v in defs.items()],
+               "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
-        return src, obj, res
+        return stem, obj, res
 
-    with ThreadPoolExecutor(max_workers=jobs or len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    with ThreadPoolExecutor(max_workers=jobs or min(len(UNITS), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(compile_one, UNITS))
     failed = [(s, r) for s, _, r in results if r.returncode != 0]
     for s, _, r in results:
         if verbose or r.returncode != 0:

@@ -21,6 +21,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "ra_internal.h"
@@ -33,6 +34,36 @@ enum : int { kOpSum = 0, kOpMax = 1 };
 struct DF32 { using T = float;    static constexpr int kVec = 4; };
 struct DBF16 { using T = uint16_t; static constexpr int kVec = 8; };
 struct DI32 { using T = int32_t;  static constexpr int kVec = 4; };
+struct DF16 { using T = uint16_t; static constexpr int kVec = 8; };
+struct DF64 { using T = double;   static constexpr int kVec = 2; };
+struct DI64 { using T = int64_t;  static constexpr int kVec = 2; };
+
+template <int V> struct IntC { static constexpr int value = V; };
+
+template <int DT> struct DTypeOf;
+template <> struct DTypeOf<RA_F32> { using type = DF32; };
+template <> struct DTypeOf<RA_BF16> { using type = DBF16; };
+template <> struct DTypeOf<RA_I32> { using type = DI32; };
+template <> struct DTypeOf<RA_F16> { using type = DF16; };
+template <> struct DTypeOf<RA_F64> { using type = DF64; };
+template <> struct DTypeOf<RA_I64> { using type = DI64; };
+
+// Call f(D{}, IntC<OP>{}) for the (dtype, op) pair; cudaErrorInvalidValue
+// for an unknown one.  One place lists every supported combination.
+template <class F>
+cudaError_t with_dtype_op(int dtype, int op, F&& f) {
+  const bool mx = op == RA_MAX;
+  if (op != RA_SUM && op != RA_MAX) return cudaErrorInvalidValue;
+  switch (dtype) {
+    case RA_F32: return mx ? f(DF32{}, IntC<kOpMax>{}) : f(DF32{}, IntC<kOpSum>{});
+    case RA_BF16: return mx ? f(DBF16{}, IntC<kOpMax>{}) : f(DBF16{}, IntC<kOpSum>{});
+    case RA_I32: return mx ? f(DI32{}, IntC<kOpMax>{}) : f(DI32{}, IntC<kOpSum>{});
+    case RA_F16: return mx ? f(DF16{}, IntC<kOpMax>{}) : f(DF16{}, IntC<kOpSum>{});
+    case RA_F64: return mx ? f(DF64{}, IntC<kOpMax>{}) : f(DF64{}, IntC<kOpSum>{});
+    case RA_I64: return mx ? f(DI64{}, IntC<kOpMax>{}) : f(DI64{}, IntC<kOpSum>{});
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 // ------------------------------------------------------------ reduction
 
@@ -99,14 +130,90 @@ template <> struct Op<DBF16, kOpMax> {
   }
 };
 
+// fp16: as bf16, widened exactly to binary32, one addition, rounded to
+// nearest-even fp16 (24 >= 2*11+2, so the double rounding is innocuous).
+template <> struct Op<DF16, kOpSum> {
+  static __device__ __forceinline__ float widen(uint32_t bits16) {
+    return __half2float(__ushort_as_half((unsigned short)bits16));
+  }
+  static __device__ __forceinline__ uint16_t apply(uint16_t inc, uint16_t loc) {
+    return __half_as_ushort(__float2half_rn(__fadd_rn(widen(inc), widen(loc))));
+  }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    return (uint32_t)apply((uint16_t)(inc & 0xFFFFu), (uint16_t)(loc & 0xFFFFu)) |
+           ((uint32_t)apply((uint16_t)(inc >> 16), (uint16_t)(loc >> 16)) << 16);
+  }
+};
+
+template <> struct Op<DF16, kOpMax> {
+  static __device__ __forceinline__ uint16_t apply(uint16_t inc, uint16_t loc) {
+    return Op<DF16, kOpSum>::widen(loc) > Op<DF16, kOpSum>::widen(inc) ? loc : inc;
+  }
+  static __device__ __forceinline__ uint32_t word(uint32_t inc, uint32_t loc) {
+    return (uint32_t)apply((uint16_t)(inc & 0xFFFFu), (uint16_t)(loc & 0xFFFFu)) |
+           ((uint32_t)apply((uint16_t)(inc >> 16), (uint16_t)(loc >> 16)) << 16);
+  }
+};
+
+// 64-bit types: a 16-byte vector holds two elements.
+template <> struct Op<DF64, kOpSum> {
+  static __device__ __forceinline__ double apply(double inc, double loc) { return __dadd_rn(inc, loc); }
+  static __device__ __forceinline__ uint64_t lane(uint64_t inc, uint64_t loc) {
+    return (uint64_t)__double_as_longlong(__dadd_rn(__longlong_as_double((long long)inc),
+                                                    __longlong_as_double((long long)loc)));
+  }
+};
+
+template <> struct Op<DF64, kOpMax> {
+  static __device__ __forceinline__ double apply(double inc, double loc) { return loc > inc ? loc : inc; }
+  static __device__ __forceinline__ uint64_t lane(uint64_t inc, uint64_t loc) {
+    return __longlong_as_double((long long)loc) > __longlong_as_double((long long)inc) ? loc : inc;
+  }
+};
+
+template <> struct Op<DI64, kOpSum> {
+  static __device__ __forceinline__ int64_t apply(int64_t inc, int64_t loc) {
+    return (int64_t)((uint64_t)inc + (uint64_t)loc);
+  }
+  static __device__ __forceinline__ uint64_t lane(uint64_t inc, uint64_t loc) { return inc + loc; }
+};
+
+template <> struct Op<DI64, kOpMax> {
+  static __device__ __forceinline__ int64_t apply(int64_t inc, int64_t loc) { return loc > inc ? loc : inc; }
+  static __device__ __forceinline__ uint64_t lane(uint64_t inc, uint64_t loc) {
+    return (int64_t)loc > (int64_t)inc ? loc : inc;
+  }
+};
+
+template <class D> struct Is64 { static constexpr bool value = false; };
+template <> struct Is64<DF64> { static constexpr bool value = true; };
+template <> struct Is64<DI64> { static constexpr bool value = true; };
+
+template <class D, int OP, bool W64 = Is64<D>::value>
+struct VecOp {
+  static __device__ __forceinline__ uint4 apply(uint4 inc, uint4 loc) {
+    uint4 r;
+    r.x = Op<D, OP>::word(inc.x, loc.x);
+    r.y = Op<D, OP>::word(inc.y, loc.y);
+    r.z = Op<D, OP>::word(inc.z, loc.z);
+    r.w = Op<D, OP>::word(inc.w, loc.w);
+    return r;
+  }
+};
+
+template <class D, int OP>
+struct VecOp<D, OP, true> {
+  static __device__ __forceinline__ uint4 apply(uint4 inc, uint4 loc) {
+    const uint64_t a0 = ((uint64_t)inc.y << 32) | inc.x, a1 = ((uint64_t)inc.w << 32) | inc.z;
+    const uint64_t b0 = ((uint64_t)loc.y << 32) | loc.x, b1 = ((uint64_t)loc.w << 32) | loc.z;
+    const uint64_t r0 = Op<D, OP>::lane(a0, b0), r1 = Op<D, OP>::lane(a1, b1);
+    return make_uint4((uint32_t)r0, (uint32_t)(r0 >> 32), (uint32_t)r1, (uint32_t)(r1 >> 32));
+  }
+};
+
 template <class D, int OP>
 __device__ __forceinline__ uint4 combine_vec(uint4 inc, uint4 loc) {
-  uint4 r;
-  r.x = Op<D, OP>::word(inc.x, loc.x);
-  r.y = Op<D, OP>::word(inc.y, loc.y);
-  r.z = Op<D, OP>::word(inc.z, loc.z);
-  r.w = Op<D, OP>::word(inc.w, loc.w);
-  return r;
+  return VecOp<D, OP>::apply(inc, loc);
 }
 
 // ------------------------------------------------------------ vector I/O
@@ -125,6 +232,10 @@ template <> __device__ __forceinline__ float ld_l2_scalar<float>(const float* p)
 template <> __device__ __forceinline__ int32_t ld_l2_scalar<int32_t>(const int32_t* p) { return __ldcg(p); }
 template <> __device__ __forceinline__ uint16_t ld_l2_scalar<uint16_t>(const uint16_t* p) {
   return __ldcg(reinterpret_cast<const unsigned short*>(p));
+}
+template <> __device__ __forceinline__ double ld_l2_scalar<double>(const double* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ int64_t ld_l2_scalar<int64_t>(const int64_t* p) {
+  return (int64_t)__ldcg(reinterpret_cast<const long long*>(p));
 }
 
 // Split [off, end) (element indices, buffers 16-byte aligned) into a scalar

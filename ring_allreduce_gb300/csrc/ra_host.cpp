@@ -37,7 +37,13 @@ ra_status cuda_fail(cudaError_t e, const char* what) {
   return fail(s, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-size_t elem_bytes(ra_dtype d) { return d == RA_BF16 ? 2 : 4; }
+size_t elem_bytes(ra_dtype d) {
+  switch (d) {
+    case RA_BF16: case RA_F16: return 2;
+    case RA_F64: case RA_I64: return 8;
+    default: return 4;
+  }
+}
 
 // Switch to the handle's device for the duration of a call.
 struct DeviceGuard {
@@ -110,7 +116,7 @@ struct ra_ctx {
 
 namespace {
 
-bool valid_dtype(int d) { return d == RA_F32 || d == RA_BF16 || d == RA_I32; }
+bool valid_dtype(int d) { return d >= RA_F32 && d <= RA_I64; }
 bool valid_op(int o) { return o == RA_SUM || o == RA_MAX; }
 
 ra::Plan make_plan(int R, size_t n) {
@@ -196,7 +202,7 @@ ra_status check_buffers(ra_ctx* h, const void* const* in, void* const* out) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int vec_elems(ra_dtype d) { return d == RA_BF16 ? 8 : 4; }
+int vec_elems(ra_dtype d) { return (int)(16 / elem_bytes(d)); }
 
 // Enough CTAs for every thread to take its vectors once (see ra_direct.cu).
 int direct_ctas_per_chunk(const ra_ctx* h, const ra::Plan& pl, int mode) {

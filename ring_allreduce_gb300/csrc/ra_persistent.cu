@@ -174,7 +174,7 @@ __device__ __forceinline__ void copy_slice(const typename D::T* src, typename D:
 }
 
 template <class D, int OP>
-__global__ void __launch_bounds__(kPersistThreads)
+__global__ void __launch_bounds__(kPersistThreads, 2)
 persistent_kernel(const PersistArgs a) {
   using T = typename D::T;
   __shared__ int s_abort;
@@ -216,21 +216,13 @@ persistent_kernel(const PersistArgs a) {
   }
 }
 
-template <class D, int OP>
-static const void* persistent_fn() {
-  return reinterpret_cast<const void*>(&persistent_kernel<D, OP>);
-}
-
 static const void* persistent_select(int dtype, int op) {
-  switch (dtype * 2 + op) {
-    case RA_F32 * 2 + RA_SUM: return persistent_fn<DF32, kOpSum>();
-    case RA_F32 * 2 + RA_MAX: return persistent_fn<DF32, kOpMax>();
-    case RA_BF16 * 2 + RA_SUM: return persistent_fn<DBF16, kOpSum>();
-    case RA_BF16 * 2 + RA_MAX: return persistent_fn<DBF16, kOpMax>();
-    case RA_I32 * 2 + RA_SUM: return persistent_fn<DI32, kOpSum>();
-    case RA_I32 * 2 + RA_MAX: return persistent_fn<DI32, kOpMax>();
-    default: return nullptr;
-  }
+  const void* fn = nullptr;
+  with_dtype_op(dtype, op, [&](auto d, auto o) {
+    fn = reinterpret_cast<const void*>(&persistent_kernel<decltype(d), decltype(o)::value>);
+    return cudaSuccess;
+  });
+  return fn;
 }
 
 cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks) {

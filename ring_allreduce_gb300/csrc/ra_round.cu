@@ -58,16 +58,10 @@ rs_round_kernel(const RoundArgs a) {
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st) {
   if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
   dim3 grid(ctas_per_rank, a.R);
-  switch (dtype * 2 + op) {
-    case RA_F32 * 2 + RA_SUM: rs_round_kernel<DF32, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
-    case RA_F32 * 2 + RA_MAX: rs_round_kernel<DF32, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
-    case RA_BF16 * 2 + RA_SUM: rs_round_kernel<DBF16, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
-    case RA_BF16 * 2 + RA_MAX: rs_round_kernel<DBF16, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
-    case RA_I32 * 2 + RA_SUM: rs_round_kernel<DI32, kOpSum><<<grid, kRoundThreads, 0, st>>>(a); break;
-    case RA_I32 * 2 + RA_MAX: rs_round_kernel<DI32, kOpMax><<<grid, kRoundThreads, 0, st>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  return with_dtype_op(dtype, op, [&](auto d, auto o) {
+    rs_round_kernel<decltype(d), decltype(o)::value><<<grid, kRoundThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  });
 }
 
 // ---------------------------------------------------- AllGather round, TMA

@@ -68,12 +68,12 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
                                           void* const* out, void* stream) {
   using namespace ra;
   if (R < 2 || R > kMaxRanks) return record_error(RA_ERR_INVALID, "R=%d outside [2, %d]", R, kMaxRanks);
-  if (dtype != RA_F32 && dtype != RA_BF16 && dtype != RA_I32)
-    return record_error(RA_ERR_INVALID, "unknown dtype %d", (int)dtype);
+  if (dtype < RA_F32 || dtype > RA_I64) return record_error(RA_ERR_INVALID, "unknown dtype %d", (int)dtype);
   if (op != RA_SUM && op != RA_MAX) return record_error(RA_ERR_INVALID, "unknown op %d", (int)op);
   if (!in || !out) return record_error(RA_ERR_INVALID, "NULL pointer array");
   if (n == 0) return RA_OK;
-  const size_t bytes = n * (dtype == RA_BF16 ? 2 : 4);
+  const size_t esize = (dtype == RA_BF16 || dtype == RA_F16) ? 2 : ((dtype == RA_F64 || dtype == RA_I64) ? 8 : 4);
+  const size_t bytes = n * esize;
   for (int r = 0; r < R; ++r) {
     if (!in[r] || !out[r]) return record_error(RA_ERR_INVALID, "NULL buffer for rank %d", r);
     if (((uintptr_t)in[r] | (uintptr_t)out[r]) & 15u)
@@ -103,7 +103,8 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
 
   // channels: as many as are co-resident and useful, within the array
   const int64_t C = (int64_t)((n + (size_t)R - 1) / (size_t)R);
-  const int64_t vecs = (C + (dtype == RA_BF16 ? 8 : 4) - 1) / (dtype == RA_BF16 ? 8 : 4) + 1;
+  const int64_t per_vec = (int64_t)(16 / esize);
+  const int64_t vecs = (C + per_vec - 1) / per_vec + 1;
   int64_t G = (vecs + (int64_t)kPersistThreads * 4 - 1) / ((int64_t)kPersistThreads * 4);
   const int64_t co_resident = (int64_t)bps * sms / R;
   if (G > co_resident) G = co_resident;

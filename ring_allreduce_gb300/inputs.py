@@ -27,8 +27,9 @@ import numpy as np
 __all__ = ["WORKLOADS", "DISTS", "generate", "workload_inputs", "storage_dtype", "itemsize"]
 
 # dtype name -> numpy storage dtype (bf16 is held as its 16-bit pattern)
-_STORAGE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}
-_ITEMSIZE = {"f32": 4, "bf16": 2, "i32": 4}
+_STORAGE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.float16, "f64": np.float64,
+            "i64": np.int64}
+_ITEMSIZE = {"f32": 4, "bf16": 2, "i32": 4, "f16": 2, "f64": 8, "i64": 8}
 
 WORKLOADS = {
     "r4_small": dict(R=4, n=4096, dtype="f32", ops=("sum",), dist="int8", seed=0),
@@ -56,6 +57,12 @@ def _to_bf16_bits(v32):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def _to_f16(v32):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32))
+    return t.to(torch.float16).numpy().copy()
+
+
 def _draw(rng, n, dist, dtype):
     if dist == "int8":
         v = rng.integers(-8, 8, endpoint=True, size=n).astype(np.float64)
@@ -68,9 +75,13 @@ def _draw(rng, n, dist, dtype):
         mask = rng.random(n) < 0.01
         v[mask] *= 100.0
     elif dist == "int20":
-        if dtype == "i32":
-            return rng.integers(-2**20, 2**20, endpoint=True, size=n, dtype=np.int32)
+        if dtype in ("i32", "i64"):
+            return rng.integers(-2**20, 2**20, endpoint=True, size=n, dtype=_STORAGE[dtype])
         v = rng.integers(-2**20, 2**20, endpoint=True, size=n).astype(np.float64)
+    elif dist == "int40":
+        if dtype == "i64":
+            return rng.integers(-2**40, 2**40, endpoint=True, size=n, dtype=np.int64)
+        v = rng.integers(-2**40, 2**40, endpoint=True, size=n).astype(np.float64)
     elif dist == "uniform":
         v = rng.uniform(-1.0, 1.0, size=n)
     else:
@@ -81,16 +92,23 @@ def _draw(rng, n, dist, dtype):
         return _to_bf16_bits(v.astype(np.float32))
     if dtype == "i32":
         return np.clip(np.rint(v), -2**31, 2**31 - 1).astype(np.int32)
+    if dtype == "f16":
+        return _to_f16(v.astype(np.float32))
+    if dtype == "f64":
+        return v.astype(np.float64)
+    if dtype == "i64":
+        return np.rint(v).astype(np.int64)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
-DISTS = ("int8", "normal", "grad", "int20", "uniform")
+DISTS = ("int8", "normal", "grad", "int20", "int40", "uniform")
 
 
 def generate(R, n, dtype, dist, seed):
     """R rank inputs of n elements each, drawn rank after rank from
     ``numpy.random.default_rng(seed)``.  Returns a list of numpy arrays in
-    the storage dtype (float32, uint16 bf16 patterns or int32)."""
+    the storage dtype (float32, uint16 bf16 patterns, int32, float16,
+    float64 or int64)."""
     rng = np.random.default_rng(seed)
     return [_draw(rng, n, dist, dtype) for _ in range(R)]
 

@@ -12,7 +12,8 @@ _TORCH_DT = None
 def torch_dtype(np_dtype):
     import torch
     return {np.dtype(np.float32): torch.float32, np.dtype(np.uint16): torch.int16,
-            np.dtype(np.int32): torch.int32}[np.dtype(np_dtype)]
+            np.dtype(np.int32): torch.int32, np.dtype(np.float16): torch.float16,
+            np.dtype(np.float64): torch.float64, np.dtype(np.int64): torch.int64}[np.dtype(np_dtype)]
 
 
 def _stride(n):

@@ -16,7 +16,8 @@ torch = pytest.importorskip("torch")
 
 VARIANTS = ["direct", "ring", "persistent", "pipelined"]
 DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
-             ("i32", "sum"), ("i32", "max")]
+             ("i32", "sum"), ("i32", "max"), ("f16", "sum"), ("f16", "max"),
+             ("f64", "sum"), ("f64", "max"), ("i64", "sum"), ("i64", "max")]
 # (R, n): degenerate, n < R, ragged, several tiles per chunk with a ragged tail
 SHAPES = [(2, 1), (3, 2), (4, 4096), (5, 1001), (8, 8 * 1024 + 13), (2, 2**20 + 7),
           (8, 2**20 + 7), (13, 77777), (16, 2**16 + 3), (32, 2**16 + 1)]
@@ -32,7 +33,7 @@ def ra():
 
 
 def _dist(dtype):
-    return {"f32": "normal", "bf16": "grad", "i32": "int20"}[dtype]
+    return {"f32": "normal", "bf16": "grad", "i32": "int20", "f16": "grad", "f64": "normal", "i64": "int40"}[dtype]
 
 
 def run_gpu(ra, x, dtype, op, variant, kind="allreduce", inplace=False, ctas=0, repeat=1, options=()):
@@ -73,7 +74,8 @@ def test_allreduce_matches_oracle(ra, variant, dtype, op):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "sum"), ("i32", "max")])
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "sum"), ("i32", "max"), ("f16", "sum"),
+                                      ("f64", "sum"), ("i64", "max")])
 def test_reduce_scatter_owned_chunk(ra, variant, dtype, op):
     o = elementops.get_op(dtype, op)
     for i, (R, n) in enumerate(SHAPES):
@@ -87,7 +89,7 @@ def test_reduce_scatter_owned_chunk(ra, variant, dtype, op):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16", "f64", "i64"])
 def test_all_gather_from_reduce_scatter_layout(ra, variant, dtype):
     """AllGather takes the layout ReduceScatter leaves: only chunk (r+1) of
     buf[r] matters; the other chunks hold junk that must be overwritten."""
@@ -159,7 +161,7 @@ def test_single_rank_and_empty(ra):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("dtype,big", [("f32", 2.0**24), ("bf16", 256.0)])
+@pytest.mark.parametrize("dtype,big", [("f32", 2.0**24), ("bf16", 256.0), ("f16", 2048.0), ("f64", 2.0**53)])
 def test_ring_start_rank_pin_on_gpu(ra, variant, dtype, big):
     """Chunk k holds big, 1, 1, -big on ranks k..k+3: the ring's fold from
     rank k gives 0, any other start gives 2."""
@@ -171,6 +173,10 @@ def test_ring_start_rank_pin_on_gpu(ra, variant, dtype, big):
             vals[(k + j) % R][k * per:(k + 1) * per] = pattern[j]
     if dtype == "bf16":
         x = [torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for v in vals]
+    elif dtype == "f16":
+        x = [torch.from_numpy(v).to(torch.float16).numpy() for v in vals]
+    elif dtype == "f64":
+        x = [v.astype(np.float64) for v in vals]
     else:
         x = vals
     got = run_gpu(ra, x, dtype, "sum", variant)

@@ -13,7 +13,9 @@ from oracle import elementops, ring
 from ring_allreduce_gb300 import inputs
 
 DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
-             ("i32", "sum"), ("i32", "max")]
+             ("i32", "sum"), ("i32", "max"), ("f16", "sum"), ("f16", "max"),
+             ("f64", "sum"), ("f64", "max"), ("i64", "sum"), ("i64", "max")]
+DIST = {"f32": "normal", "bf16": "normal", "i32": "int20", "f16": "normal", "f64": "normal", "i64": "int40"}
 
 
 # ---------------------------------------------------------------- chunk plan
@@ -142,15 +144,28 @@ def _brute_allreduce(x, dtype, op):
                 else:
                     acc = v if bool(v.float() > acc.float()) else acc
             res.append(np.uint16(int(acc.view(torch.int16)) & 0xFFFF))
+        elif dtype == "f16":
+            acc = torch.tensor(float(x[order[0]][i]), dtype=torch.float16)
+            for q in order[1:]:
+                v = torch.tensor(float(x[q][i]), dtype=torch.float16)
+                acc = (acc + v) if op == "sum" else (v if bool(v > acc) else acc)
+            res.append(np.float16(acc.item()))
+        elif dtype == "f64":
+            acc = float(x[order[0]][i])            # Python floats are IEEE binary64
+            for q in order[1:]:
+                v = float(x[q][i])
+                acc = (acc + v) if op == "sum" else (v if v > acc else acc)
+            res.append(np.float64(acc))
         else:
+            bits = 32 if dtype == "i32" else 64
             acc = int(x[order[0]][i])
             for q in order[1:]:
                 v = int(x[q][i])
                 if op == "sum":
-                    acc = (acc + v + 2**31) % 2**32 - 2**31
+                    acc = (acc + v + 2**(bits - 1)) % 2**bits - 2**(bits - 1)
                 else:
                     acc = v if v > acc else acc
-            res.append(np.int32(acc))
+            res.append(acc)
     return np.array(res, dtype=inputs.storage_dtype(dtype))
 
 
@@ -158,10 +173,9 @@ def _brute_allreduce(x, dtype, op):
 def test_brute_force_tiny(dtype, op):
     for R in range(2, 7):
         for n in range(0, 3 * R + 3):
-            x = inputs.generate(R, n, dtype, "normal" if dtype != "i32" else "int20",
-                                seed=1000 * R + n)
-            if dtype == "i32" and n:
-                x[0][0] = 2**31 - 1         # force a wrap in the sum
+            x = inputs.generate(R, n, dtype, DIST[dtype], seed=1000 * R + n)
+            if dtype in ("i32", "i64") and n:
+                x[0][0] = 2**(31 if dtype == "i32" else 63) - 1     # force a wrap in the sum
                 x[1][0] = 5
             got = ring.ring_allreduce(x, elementops.get_op(dtype, op))
             want = _brute_allreduce(x, dtype, op)
@@ -202,7 +216,7 @@ def test_closed_form_each_rank_once(R):
 
 # ------------------------------------------------------ order sensitivity
 
-@pytest.mark.parametrize("dtype,big", [("f32", 2.0**24), ("bf16", 256.0)])
+@pytest.mark.parametrize("dtype,big", [("f32", 2.0**24), ("bf16", 256.0), ("f16", 2048.0), ("f64", 2.0**53)])
 def test_ring_start_rank_and_order(dtype, big):
     """Chunk k holds big, 1, 1, -big on ranks k, k+1, k+2, k+3.  Folding
     from rank k gives ((big + 1) + 1) - big = 0 (each +1 is a tie that rounds
@@ -217,12 +231,17 @@ def test_ring_start_rank_and_order(dtype, big):
             vals[(k + j) % R][k * per:(k + 1) * per] = pattern[j]
     if dtype == "bf16":
         x = [_torch_bf16_bits(v) for v in vals]
+    elif dtype == "f16":
+        x = [torch.from_numpy(v).to(torch.float16).numpy() for v in vals]
+    elif dtype == "f64":
+        x = [v.astype(np.float64) for v in vals]
     else:
         x = vals
     out = ring.ring_allreduce(x, elementops.get_op(dtype, "sum"))
     res = elementops.bf16_bits_to_f32(out[0]) if dtype == "bf16" else out[0]
     assert (res == 0).all()
-    # the other starting ranks give 2 (checked with torch bf16 / numpy f32)
+    # the other starting ranks give 2 (checked with numpy f32 scalars, torch
+    # bf16 / f16, Python binary64 floats)
     for start in range(1, R):
         order = [pattern[(start + j) % R] for j in range(R)]
         if dtype == "f32":
@@ -230,10 +249,16 @@ def test_ring_start_rank_and_order(dtype, big):
             for v in order[1:]:
                 acc = acc + np.float32(v)
             assert acc == 2
-        else:
-            acc = torch.tensor(order[0], dtype=torch.bfloat16)
+        elif dtype == "f64":
+            acc = order[0]
             for v in order[1:]:
-                acc = acc + torch.tensor(v, dtype=torch.bfloat16)
+                acc = acc + v
+            assert acc == 2
+        else:
+            tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+            acc = torch.tensor(order[0], dtype=tdt)
+            for v in order[1:]:
+                acc = acc + torch.tensor(v, dtype=tdt)
             assert float(acc) == 2
 
 
@@ -261,7 +286,7 @@ def test_fp32_error_within_recursive_summation_bound(R):
 @pytest.mark.parametrize("dtype,op", DTYPE_OPS)
 def test_allreduce_equals_reducescatter_then_allgather(dtype, op):
     for R, n in ((2, 9), (3, 10), (4, 4096), (5, 1001), (8, 8 * 257 + 3)):
-        x = inputs.generate(R, n, dtype, "grad" if dtype == "bf16" else "normal", R * n)
+        x = inputs.generate(R, n, dtype, "grad" if dtype in ("bf16", "f16") else DIST[dtype], R * n)
         o = elementops.get_op(dtype, op)
         ar = ring.ring_allreduce(x, o)
         rs = ring.ring_reduce_scatter(x, o)
@@ -343,3 +368,40 @@ def test_max_tie_keeps_incoming(dtype):
     sign = np.uint32(0x80000000) if dtype == "f32" else np.uint16(0x8000)
     # chunk 0 starts at rank 0 (+0 first), chunk 1 at rank 1 (+0 first)
     assert ((bits & sign) == 0).all()
+
+
+
+def test_f16_rounding_matches_torch():
+    """float32 -> float16 round-to-nearest-even (numpy's conversion, which the
+    oracle's fp16 hop uses) equals torch's conversion on random patterns."""
+    rng = np.random.default_rng(321)
+    bits = rng.integers(0, 2**32, size=500_000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    with np.errstate(over="ignore"):      # values beyond fp16's range round to infinity
+        a = f.astype(np.float16)
+    b = torch.from_numpy(f).to(torch.float16).numpy()
+    np.testing.assert_array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_f16_sum_matches_torch_float16_add():
+    rng = np.random.default_rng(5)
+    x = torch.from_numpy((rng.standard_normal(200_000) * 2.0 ** rng.integers(-14, 14, 200_000))
+                         .astype(np.float32)).to(torch.float16)
+    y = torch.from_numpy(rng.standard_normal(200_000).astype(np.float32)).to(torch.float16)
+    want = (x + y).numpy()
+    got = elementops.get_op("f16", "sum").combine(x.numpy(), y.numpy())
+    np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+@pytest.mark.parametrize("R", [2, 9, 62])
+def test_closed_form_int64(R):
+    """x_r = 2^r for 64-bit ranks: the sum 2^R - 1 counts every rank once;
+    x_r[i] = r * 10^12 + i gives 10^12 R(R-1)/2 + R i."""
+    n = 2 * R + 3
+    x = [np.full(n, 1 << r, dtype=np.int64) for r in range(R)]
+    s = ring.ring_allreduce(x, elementops.get_op("i64", "sum"))
+    assert all((v == (1 << R) - 1).all() for v in s)
+    y = [np.arange(n, dtype=np.int64) + np.int64(10**12 * r) for r in range(R)]
+    t = ring.ring_allreduce(y, elementops.get_op("i64", "sum"))
+    assert all((v == 10**12 * R * (R - 1) // 2 + R * np.arange(n)).all() for v in t)
