@@ -188,6 +188,21 @@ ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out
  * leaves); afterwards every buf[r] holds all R chunks. */
 ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream);
 
+/* ReduceScatter into compact outputs (the layout of NCCL's ReduceScatter):
+ * in[r] holds n elements; out[r] holds only rank r's chunk, (r+1) mod R,
+ * len elements as ra_owned_chunk reports (a rank whose chunk is empty gets
+ * no write and its out[r] is not looked at).  Buffers must not overlap, except
+ * inputs with each other.  Runs the direct kernel whatever RA_OPT_VARIANT
+ * says; when the chunk starts are not 16-byte aligned (ragged plans),
+ * element-wide accesses are used. */
+ra_status ra_reduce_scatter_compact(ra_handle h, const void* const* in, void* const* out, void* stream);
+
+/* AllGather from compact inputs: in[r] holds rank r's chunk, (r+1) mod R
+ * (len elements as ra_owned_chunk reports); out[r] gets all n elements.
+ * Buffers must not overlap, except inputs with each other.  Direct kernel,
+ * as ra_reduce_scatter_compact. */
+ra_status ra_all_gather_compact(ra_handle h, const void* const* in, void* const* out, void* stream);
+
 /* Ring AllReduce (sections 4-9): out[r] = S for every r. */
 ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, void* stream);
 

@@ -39,7 +39,8 @@ import numpy as np
 
 __all__ = [
     "chunk_plan", "owned_chunk", "ring_reduce_scatter", "ring_all_gather",
-    "ring_allreduce", "primitive_name",
+    "ring_allreduce", "primitive_name", "ring_reduce_scatter_compact",
+    "ring_all_gather_compact",
 ]
 
 
@@ -259,3 +260,35 @@ def ring_allreduce(x, op, trace=None, log=None, stats=None):
     if stats is not None:
         stats["bytes_sent"] = list(wire.bytes_sent)
     return out
+
+
+def ring_reduce_scatter_compact(x, op):
+    """ReduceScatter where each rank keeps only the chunk it owns, (r+1) mod R
+    (the placement of section 2 and 5): returns R arrays, rank r's of length
+    L_{(r+1) mod R}, cut from ``ring_reduce_scatter``."""
+    R, n = _check_inputs(x, op)
+    full = ring_reduce_scatter(x, op)
+    plan = chunk_plan(R, n)
+    out = []
+    for r in range(R):
+        off, L = plan[owned_chunk(R, r)]
+        out.append(np.array(full[r][off:off + L], copy=True))
+    return out
+
+
+def ring_all_gather_compact(chunks, n, op):
+    """AllGather from compact inputs: rank r brings chunk (r+1) mod R
+    (``chunks[r]``); the chunks are placed where ReduceScatter leaves them and
+    ``ring_all_gather`` runs on that layout.  Returns R arrays of n."""
+    R = len(chunks)
+    plan = chunk_plan(R, n)
+    dtype = np.asarray(chunks[0]).dtype if R else np.float32
+    buf = []
+    for r in range(R):
+        b = np.zeros(n, dtype=dtype)
+        off, L = plan[owned_chunk(R, r)]
+        if len(chunks[r]) != L:
+            raise ValueError(f"rank {r} brings {len(chunks[r])} elements, its chunk has {L}")
+        b[off:off + L] = chunks[r]
+        buf.append(b)
+    return ring_all_gather(buf, op)

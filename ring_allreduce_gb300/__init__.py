@@ -10,6 +10,7 @@ raises ImportError: there is no CPU fallback.
 
 _BINDING_NAMES = {
     "ra_create", "ra_destroy", "ra_reduce_scatter", "ra_all_gather", "ra_allreduce",
+    "ra_reduce_scatter_compact", "ra_all_gather_compact",
     "ra_chunk_plan", "ra_owned_chunk", "ra_set_option", "ra_get_option",
     "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error", "ra_status_string",
     "RingAllReduce", "RAError", "Status", "DType", "Op", "Variant", "Barrier", "Option",

@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
-    "ra_all_gather", "ra_allreduce", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
+    "ra_all_gather", "ra_allreduce", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error",
     "ra_status_string", "RingAllReduce", "EXPORTED",
 ]
@@ -94,6 +94,8 @@ EXPORTED = {
     "ra_reduce_scatter": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_all_gather": (_ST, [_P, ctypes.POINTER(_P), _P]),
     "ra_allreduce": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "ra_reduce_scatter_compact": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "ra_all_gather_compact": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_chunk_plan": (_ST, [ctypes.c_int, _SZ, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "ra_owned_chunk": (_ST, [_P, ctypes.c_int, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "ra_set_option": (_ST, [_P, ctypes.c_int, ctypes.c_longlong]),
@@ -202,6 +204,14 @@ def ra_allreduce_noalloc(R, n, dtype, op, ins, outs, stream=None):
                                      _ptr_array(outs), _stream(stream)))
 
 
+def ra_reduce_scatter_compact(h, ins, outs, stream=None):
+    _check(_lib.ra_reduce_scatter_compact(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
+def ra_all_gather_compact(h, ins, outs, stream=None):
+    _check(_lib.ra_all_gather_compact(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
 def ra_chunk_plan(R, n):
     off = (_SZ * max(R, 1))()
     ln = (_SZ * max(R, 1))()
@@ -281,6 +291,16 @@ class RingAllReduce:
     def all_gather(self, bufs, stream=None):
         self._ranks(bufs)
         ra_all_gather(self.h, bufs, stream)
+
+    def reduce_scatter_compact(self, ins, outs, stream=None):
+        """outs[r]: rank r's chunk only (length from owned_chunk(r))."""
+        self._ranks(ins, outs)
+        ra_reduce_scatter_compact(self.h, ins, outs, stream)
+
+    def all_gather_compact(self, ins, outs, stream=None):
+        """ins[r]: rank r's chunk only; outs[r]: all n elements."""
+        self._ranks(ins, outs)
+        ra_all_gather_compact(self.h, ins, outs, stream)
 
     def owned_chunk(self, r):
         return ra_owned_chunk(self.h, r)

@@ -227,6 +227,15 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
 __device__ __forceinline__ uint4 ld_l2(const uint4* p) { return __ldcg(p); }
 __device__ __forceinline__ void st_l2(uint4* p, uint4 v) { __stcg(p, v); }
 
+// One element, read once (evict-first), through the coherent path.
+template <class T> __device__ __forceinline__ T ld_stream_scalar(const T* p) { return __ldcs(p); }
+template <> __device__ __forceinline__ uint16_t ld_stream_scalar<uint16_t>(const uint16_t* p) {
+  return __ldcs(reinterpret_cast<const unsigned short*>(p));
+}
+template <> __device__ __forceinline__ int64_t ld_stream_scalar<int64_t>(const int64_t* p) {
+  return (int64_t)__ldcs(reinterpret_cast<const long long*>(p));
+}
+
 template <class T> __device__ __forceinline__ T ld_l2_scalar(const T* p);
 template <> __device__ __forceinline__ float ld_l2_scalar<float>(const float* p) { return __ldcg(p); }
 template <> __device__ __forceinline__ int32_t ld_l2_scalar<int32_t>(const int32_t* p) { return __ldcg(p); }

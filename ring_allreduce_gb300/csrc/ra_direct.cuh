@@ -15,7 +15,8 @@
 //
 // Modes: AllReduce writes S_k to all R outputs; ReduceScatter writes it to
 // the owner's output only (rank k-1, section 5's placement); AllGather
-// reads chunk k from its owner's buffer and writes it to the other R-1.
+// reads chunk k from its owner's buffer and writes it to the other R-1 (to
+// all R when the owner's input is a separate, compact buffer).
 //
 // Grid: (CTAs per chunk, R chunks).  By default a thread takes U 16-byte
 // vectors of its chunk (U = 4, 2, 1 for R <= 2, <= 4, more) and the grid has
@@ -65,7 +66,7 @@ direct_kernel(const DirectArgs a) {
         if (v < sp.ve) {
 #pragma unroll
           for (int j = 0; j < MAXR; ++j)
-            if (j < R && j != owner) st_stream(static_cast<uint4*>(a.p.out[j]) + v, s[u]);
+            if (j < R && (j != owner || a.write_owner)) st_stream(static_cast<uint4*>(a.p.out[j]) + v, s[u]);
         }
       }
     } else {
@@ -106,7 +107,7 @@ direct_kernel(const DirectArgs a) {
       if (MODE == kModeAllGather) {
         const T s = static_cast<const T*>(a.p.in[owner])[i];
         for (int j = 0; j < R; ++j)
-          if (j != owner) static_cast<T*>(a.p.out[j])[i] = s;
+          if (j != owner || a.write_owner) static_cast<T*>(a.p.out[j])[i] = s;
       } else {
         T acc = static_cast<const T*>(a.p.in[src_rank(0)])[i];
         for (int j = 1; j < R; ++j) acc = Op<D, OP>::apply(acc, static_cast<const T*>(a.p.in[src_rank(j)])[i]);

@@ -261,8 +261,91 @@ ra_status run_direct(ra_ctx* h, int mode, const void* const* in, void* const* ou
   a.plan = make_plan(h->R, h->n);
   a.R = h->R;
   a.mode = mode;
+  a.write_owner = 0;
   cudaError_t e = ra::launch_direct(h->dtype, h->op, a, direct_ctas_per_chunk(h, a.plan, mode), st);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "direct kernel launch");
+}
+
+// Compact ReduceScatter (compact_out) or AllGather (compact_in): the
+// compact side holds rank r's chunk (r+1) mod R only.
+ra_status check_compact(ra_ctx* h, const void* const* full, const void* const* compact, bool full_is_input) {
+  const int R = h->R;
+  const size_t b = elem_bytes(h->dtype);
+  size_t off[ra::kMaxRanks], len[ra::kMaxRanks];
+  ra_chunk_plan(R, h->n, off, len);
+  const char* fname = full_is_input ? "in" : "out";
+  const char* cname = full_is_input ? "out" : "in";
+  struct Range { const void* p; size_t bytes; const char* name; int r; bool input; };
+  Range rs[2 * ra::kMaxRanks];
+  int nr = 0;
+  for (int r = 0; r < R; ++r) {
+    const size_t cb = len[(r + 1) % R] * b;
+    if (!full[r]) return fail(RA_ERR_INVALID, "%s[%d] is NULL", fname, r);
+    if ((uintptr_t)full[r] & 15u) return fail(RA_ERR_INVALID, "%s[%d]=%p is not 16-byte aligned", fname, r, full[r]);
+    rs[nr++] = {full[r], h->n * b, fname, r, full_is_input};
+    if (cb == 0) continue;   // an empty chunk: the compact buffer is not accessed
+    if (!compact[r]) return fail(RA_ERR_INVALID, "%s[%d] is NULL", cname, r);
+    if ((uintptr_t)compact[r] & 15u)
+      return fail(RA_ERR_INVALID, "%s[%d]=%p is not 16-byte aligned", cname, r, compact[r]);
+    rs[nr++] = {compact[r], cb, cname, r, !full_is_input};
+  }
+  for (int i = 0; i < nr; ++i)
+    for (int j = i + 1; j < nr; ++j) {
+      if (rs[i].input && rs[j].input) continue;   // inputs may overlap each other
+      const uintptr_t x = (uintptr_t)rs[i].p, y = (uintptr_t)rs[j].p;
+      if (x < y + rs[j].bytes && y < x + rs[i].bytes)
+        return fail(RA_ERR_INVALID, "%s[%d] overlaps %s[%d]", rs[i].name, rs[i].r, rs[j].name, rs[j].r);
+    }
+  if (h->check_pointers)
+    for (int i = 0; i < nr; ++i) {
+      ra_status s = check_device_pointer(h, rs[i].p, rs[i].name, rs[i].r);
+      if (s != RA_OK) return s;
+    }
+  return RA_OK;
+}
+
+ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* out, cudaStream_t st) {
+  const int R = h->R;
+  const size_t b = elem_bytes(h->dtype);
+  const ra::Plan pl = make_plan(R, h->n);
+  size_t off[ra::kMaxRanks], len[ra::kMaxRanks];
+  ra_chunk_plan(R, h->n, off, len);
+  if ((pl.C * (int64_t)b) % 16 == 0) {
+    // every chunk starts on a 16-byte boundary: the direct kernel, with each
+    // compact buffer addressed as if it began at its chunk's offset
+    ra::DirectArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int r = 0; r < R; ++r) {
+      const size_t shift = off[(r + 1) % R] * b;
+      if (mode == ra::kModeReduceScatter) {
+        a.p.in[r] = in[r];
+        a.p.out[r] = static_cast<char*>(out[r]) - shift;
+      } else {
+        a.p.in[r] = static_cast<const char*>(in[r]) - shift;
+        a.p.out[r] = out[r];
+      }
+    }
+    a.plan = pl;
+    a.R = R;
+    a.mode = mode;
+    a.write_owner = 1;
+    cudaError_t e = ra::launch_direct(h->dtype, h->op, a, direct_ctas_per_chunk(h, pl, mode), st);
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "direct kernel launch");
+  }
+  ra::CompactArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < R; ++r) {
+    a.p.in[r] = in[r];
+    a.p.out[r] = out[r];
+  }
+  a.plan = pl;
+  a.R = R;
+  a.mode = mode;
+  int64_t ctas = h->ctas > 0 ? h->ctas : ceil_div(pl.C, (int64_t)ra::kCompactThreads * ra::kCompactPerThread);
+  if (ctas > 65535) ctas = 65535;
+  if (ctas < 1) ctas = 1;
+  cudaError_t e = ra::launch_compact(h->dtype, h->op, a, (int)ctas, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "compact kernel launch");
 }
 
 ra_status run_ring_reduce(ra_ctx* h, const void* const* in, void* const* out, cudaStream_t st) {
@@ -698,6 +781,32 @@ ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
     default:
       return run_direct(h, ra::kModeAllGather, buf, buf, st);
   }
+}
+
+ra_status ra_reduce_scatter_compact(ra_handle h, const void* const* in, void* const* out, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!in || !out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  if (h->n == 0) return RA_OK;
+  ra_status s = check_compact(h, in, out, true);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->R == 1) return run_direct(h, ra::kModeAllReduce, in, out, st);
+  return run_compact(h, ra::kModeReduceScatter, in, out, st);
+}
+
+ra_status ra_all_gather_compact(ra_handle h, const void* const* in, void* const* out, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!in || !out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  if (h->n == 0) return RA_OK;
+  ra_status s = check_compact(h, out, in, false);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->R == 1) return run_direct(h, ra::kModeAllReduce, in, out, st);
+  return run_compact(h, ra::kModeAllGather, in, out, st);
 }
 
 ra_status ra_owned_chunk(ra_handle h, int r, size_t* off, size_t* len) {

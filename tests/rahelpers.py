@@ -67,3 +67,41 @@ def assert_bitwise_equal(got, want, what=""):
         bad = np.nonzero((gb != wb).reshape(-1, item).any(axis=1))[0]
         raise AssertionError(f"{what}: {len(bad)} elements differ, first at {bad[:8].tolist()}: "
                              f"got {got[bad[:4]].tolist()} want {want[bad[:4]].tolist()}")
+
+
+class DeviceBuffers:
+    """Separately allocated device buffers of per-rank lengths (compact
+    chunks), each with guard bands on both sides."""
+
+    def __init__(self, lengths, np_dtype, host=None):
+        import torch
+        self.np_dtype = np.dtype(np_dtype)
+        self.lengths = list(lengths)
+        tdt = torch_dtype(np_dtype)
+        self.bigs = []
+        self.views = []
+        for r, L in enumerate(self.lengths):
+            big = torch.empty(GUARD + L + GUARD, dtype=tdt, device="cuda")
+            big.view(torch.uint8).fill_(SENTINEL)
+            if host is not None and L:
+                arr = np.ascontiguousarray(host[r]).view(self.np_dtype)
+                if self.np_dtype == np.uint16:
+                    arr = arr.view(np.int16)
+                big[GUARD:GUARD + L] = torch.from_numpy(arr).to("cuda")
+            self.bigs.append(big)
+            self.views.append(big[GUARD:GUARD + L])
+
+    def ptrs(self):
+        return [self.bigs[r].data_ptr() + GUARD * self.np_dtype.itemsize for r in range(len(self.bigs))]
+
+    def host(self):
+        return [self.bigs[r][GUARD:GUARD + L].cpu().numpy().view(self.np_dtype) for r, L in enumerate(self.lengths)]
+
+    def guards_intact(self):
+        import torch
+        item = self.np_dtype.itemsize
+        for big, L in zip(self.bigs, self.lengths):
+            g = big.view(torch.uint8)
+            if not bool((g[:GUARD * item] == SENTINEL).all()) or not bool((g[(GUARD + L) * item:] == SENTINEL).all()):
+                return False
+        return True

@@ -9,7 +9,7 @@ import pytest
 
 from oracle import barrier, elementops, ring
 from ring_allreduce_gb300 import inputs
-from rahelpers import DeviceRanks, assert_bitwise_equal
+from rahelpers import DeviceBuffers, DeviceRanks, assert_bitwise_equal
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -453,3 +453,30 @@ def test_pipelined_timeout_names_the_predecessor(ra):
     got = out.host()
     for r in range(R):
         assert_bitwise_equal(got[r], want[r])
+
+
+
+@pytest.mark.parametrize("dtype,op", DTYPE_OPS)
+def test_compact_reduce_scatter_and_all_gather(ra, dtype, op):
+    """Compact outputs / inputs (rank r: chunk (r+1) mod R only), on plans
+    whose chunk starts are 16-byte aligned (direct kernel, shifted pointers)
+    and on ragged ones (element-wide kernel), every element compared."""
+    o = elementops.get_op(dtype, op)
+    st = inputs.storage_dtype(dtype)
+    for i, (R, n) in enumerate(SHAPES + [(4, 4096 + 8), (6, 6 * 64 * 1024)]):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=700 + i)
+        lengths = [ring.chunk_plan(R, n)[ring.owned_chunk(R, r)][1] for r in range(R)]
+        want_rs = ring.ring_reduce_scatter_compact(x, o)
+        want_ag = ring.ring_all_gather_compact(want_rs, n, o)
+        inp = DeviceRanks(R, n, st, host=x)
+        cmp = DeviceBuffers(lengths, st)
+        full = DeviceRanks(R, n, st)
+        with ra.RingAllReduce(R, n, dtype, op) as h:
+            h.reduce_scatter_compact(inp.ptrs(), cmp.ptrs())
+            h.all_gather_compact(cmp.ptrs(), full.ptrs())
+            assert h.device_status()[0] == ra.Status.OK
+        assert inp.guards_intact() and cmp.guards_intact() and full.guards_intact()
+        got_rs, got_ag = cmp.host(), full.host()
+        for r in range(R):
+            assert_bitwise_equal(got_rs[r], want_rs[r], f"RS {dtype}/{op} R={R} n={n} rank {r}")
+            assert_bitwise_equal(got_ag[r], want_ag[r], f"AG {dtype}/{op} R={R} n={n} rank {r}")

@@ -159,3 +159,17 @@ def test_reduce_scatter_then_allgather_is_allreduce_symbolic():
         ag = ring.ring_all_gather(ring.ring_reduce_scatter(x, op), op)
         for r in range(R):
             assert list(ar[r]) == list(ag[r])
+
+
+def test_compact_forms_follow_the_placement():
+    """Compact ReduceScatter keeps exactly rank r's S_{(r+1) mod R}; compact
+    AllGather of those chunks gives every rank [S0 .. S_{R-1}]."""
+    x = _sym_inputs(4, 2)
+    op = elementops.Sym()
+    rs = ring.ring_reduce_scatter_compact(x, op)
+    ar = ring.ring_allreduce(x, op)
+    for r, k in enumerate([1, 2, 3, 0]):
+        assert list(rs[r]) == list(ar[0][2 * k:2 * k + 2])
+    ag = ring.ring_all_gather_compact(rs, 8, op)
+    for r in range(4):
+        assert list(ag[r]) == list(ar[0])
