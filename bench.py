@@ -552,6 +552,76 @@ def run_barriers(args):
         print(json.dumps(line), flush=True)
 
 
+def run_extras(args):
+    """The collectives and dtypes beyond the headline workload, direct
+    kernel, one JSON line each: AllReduce for every dtype (R = 8, n = 2^24),
+    and ReduceScatter / AllGather with full and compact buffers, on an
+    aligned plan (2^24 fp32) and a ragged one (2^26+3 bf16).  frac is the
+    fraction of the measured copy bandwidth on the call's compulsory bytes."""
+    import torch
+    from ring_allreduce_gb300 import build, inputs
+    build.build()
+    from ring_allreduce_gb300 import binding as ra
+    peak, _ = measured_peaks()
+    R = 8
+
+    def timed(fn, steps=50):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps / 1e3
+
+    dists = {"f32": "normal", "bf16": "grad", "i32": "int20", "f16": "grad", "f64": "normal", "i64": "int40"}
+    for dt in ("f32", "bf16", "i32", "f16", "f64", "i64"):
+        n = 2**24
+        b = inputs.itemsize(dt)
+        host = inputs.generate(R, n, dt, dists[dt], 1)
+        _, ins = _device_ranks(torch, R, n, inputs.storage_dtype(dt), host)
+        _, outs = _device_ranks(torch, R, n, inputs.storage_dtype(dt))
+        for op in ("sum", "max"):
+            h = ra.RingAllReduce(R, n, dt, op)
+            t = timed(lambda: h.allreduce(ins, outs))
+            assert h.device_status()[0] == ra.Status.OK
+            h.close()
+            byts = 2 * R * n * b
+            print(json.dumps({"extra": "allreduce", "dtype": dt, "op": op, "R": R, "n_per_rank": n,
+                              "us": round(t * 1e6, 2), "algbw": round(n * b / t / 1e9, 2),
+                              "frac": round(byts / t / 1e9 / peak, 4)}), flush=True)
+        del ins, outs
+        torch.cuda.empty_cache()
+    for dt, n in (("f32", 2**24), ("bf16", 2**26 + 3)):
+        b = inputs.itemsize(dt)
+        st = inputs.storage_dtype(dt)
+        host = inputs.generate(R, n, dt, dists[dt], 1)
+        _, ins = _device_ranks(torch, R, n, st, host)
+        full_big, full = _device_ranks(torch, R, n, st)
+        h = ra.RingAllReduce(R, n, dt, "sum")
+        lens = [h.owned_chunk(r)[1] for r in range(R)]
+        cmp = [torch.empty(((L + 63) // 64) * 64, dtype=full_big.dtype, device="cuda")[:L] for L in lens]
+        cases = [
+            ("reduce_scatter", lambda: h.reduce_scatter(ins, full), (R + 1) * n * b),
+            ("all_gather", lambda: h.all_gather(full), R * n * b),
+            ("reduce_scatter_compact", lambda: h.reduce_scatter_compact(ins, cmp), (R + 1) * n * b),
+            ("all_gather_compact", lambda: h.all_gather_compact(cmp, full), (R + 1) * n * b),
+        ]
+        for name, fn, byts in cases:
+            t = timed(fn)
+            print(json.dumps({"extra": name, "dtype": dt, "R": R, "n_per_rank": n,
+                              "aligned_chunks": (-(-n // R) * b) % 16 == 0,
+                              "us": round(t * 1e6, 2), "frac": round(byts / t / 1e9 / peak, 4),
+                              "bytes": byts}), flush=True)
+        assert h.device_status()[0] == ra.Status.OK
+        h.close()
+        del ins, full, full_big, cmp
+        torch.cuda.empty_cache()
+
+
 def run_sweep(args):
     """Latency/bandwidth sweep (R=8 fp32 sum over n, and R over 2..32 at
     n=2^24), every variant; one JSON line per point on stdout."""
@@ -594,6 +664,7 @@ def main():
     ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--barriers", action="store_true", help="barrier cost vs R, counting vs per-peer")
+    ap.add_argument("--extras", action="store_true", help="other dtypes and collectives (direct kernel)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
@@ -611,6 +682,8 @@ def main():
         run_sweep(args)
     elif args.barriers:
         run_barriers(args)
+    elif args.extras:
+        run_extras(args)
     else:
         run_gpu_arm(args)
 
