@@ -228,7 +228,8 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
  * entries, *channels the channel count G, *calls how many calls of that kind
  * and scheme ran since the array was last zeroed, *rounds:
  *   counting barrier  [G][rounds][R] (rounds = barrier rounds); every entry
- *                     equals calls * (R - 1)
+ *                     equals calls * (R - 1), as does every shadow
+ *                     (ra_read_shadows)
  *   per-peer barrier  [G][rounds][R waiters][R peers]; every entry equals
  *                     calls, except waiter == peer, which stays 0
  *   pipelined flags   [G][R][J] (rounds = ring rounds, J = count / (G R));
@@ -269,6 +270,14 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
  * ra_get_device_status. */
 ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op op, const void* const* in,
                                void* const* out, void* stream);
+
+/* The counting barrier's shadows after the last persistent call (when it
+ * used the counting barrier), laid out as its signals: each waiter moves its
+ * own shadow forward by R-1 per call and waits for its signal to meet it
+ * ("comm: lift the GIN scale-out ceiling ...", section "Fix"), so after a
+ * successful call every shadow equals its signal.  With dst == NULL only
+ * *count is set. */
+ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count);
 
 /* Text of the calling thread's last error ("" if none). */
 const char* ra_last_error(void);

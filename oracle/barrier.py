@@ -14,9 +14,10 @@ the signal as a 64-bit value compared in a rolling way, so that x < x + 1
 survives wrap-around.
 
 The simulation: R x G threads (rank r of channel g), each running the
-barrier rounds of one call.  After a call with sequence number ``epoch``
-(1 for the first call on a fresh slot array) every slot must hold
-``epoch * (R - 1)``.  A rank told to skip one arrival makes exactly that
+barrier rounds of one call.  Every waiter keeps a shadow per slot and moves
+it forward by R-1 before it polls.  After a call with sequence number
+``epoch`` (1 for the first call on a fresh slot array) every slot and every
+shadow must hold ``epoch * (R - 1)``.  A rank told to skip one arrival makes exactly that
 waiter of that round give up after the time limit with one arrival missing.
 """
 
@@ -28,11 +29,13 @@ __all__ = ["rolling_reached", "CountingBarrierSim", "expected_slot_value", "barr
 _MASK64 = (1 << 64) - 1
 
 
-def rolling_reached(observed, target):
-    """True when ``observed`` has reached ``target`` in 64-bit rolling
-    order: the signed difference observed - target is not negative."""
-    d = (observed - target) & _MASK64
-    return d < (1 << 63)
+def rolling_reached(observed, target, bits=64):
+    """True when ``observed`` has reached ``target`` in rolling order on the
+    low ``bits`` bits: the difference observed - target, taken modulo
+    2^bits, lies in the lower half (signals compare 64 bits, counters 56)."""
+    mask = (1 << bits) - 1
+    d = (observed - target) & mask
+    return d < (1 << (bits - 1))
 
 
 def barrier_rounds(R, phases=2):
@@ -50,11 +53,13 @@ def expected_slot_value(R, epoch):
 
 
 class CountingBarrierSim:
-    """Signal slots indexed [channel][barrier round][waiter rank]."""
+    """Signal slots indexed [channel][barrier round][waiter rank], and one
+    shadow per slot, owned by its waiter."""
 
     def __init__(self, R, G, T):
         self.R, self.G, self.T = R, G, T
         self.slots = [[[0] * R for _ in range(T)] for _ in range(G)]
+        self.shadows = [[[0] * R for _ in range(T)] for _ in range(G)]
         self._lock = threading.Lock()
 
     def arrive(self, g, t, r):
@@ -66,9 +71,12 @@ class CountingBarrierSim:
                     self.slots[g][t][p] = (self.slots[g][t][p] + 1) & _MASK64
 
     def wait(self, g, t, r, epoch, timeout_s):
-        """Poll rank r's own slot until the shadow target epoch*(R-1) is
-        reached.  Returns (ok, observed, target)."""
-        target = expected_slot_value(self.R, epoch)
+        """Move rank r's shadow of this slot forward by R-1 (the arrivals it
+        expects), then poll its slot until it meets the shadow.  Returns
+        (ok, observed, target).  ``epoch`` is the call's sequence number; on
+        a fresh slot array the shadow then equals epoch*(R-1)."""
+        self.shadows[g][t][r] = (self.shadows[g][t][r] + self.R - 1) & _MASK64
+        target = self.shadows[g][t][r]
         deadline = time.monotonic() + timeout_s
         while True:
             with self._lock:

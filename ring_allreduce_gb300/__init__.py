@@ -12,7 +12,7 @@ _BINDING_NAMES = {
     "ra_create", "ra_destroy", "ra_reduce_scatter", "ra_all_gather", "ra_allreduce",
     "ra_reduce_scatter_compact", "ra_all_gather_compact",
     "ra_chunk_plan", "ra_owned_chunk", "ra_set_option", "ra_get_option",
-    "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error", "ra_status_string",
+    "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc", "ra_last_error", "ra_status_string",
     "RingAllReduce", "RAError", "Status", "DType", "Op", "Variant", "Barrier", "Option",
     "DeviceError", "load_library", "library_path",
 }

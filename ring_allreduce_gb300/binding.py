@@ -17,7 +17,8 @@ __all__ = [
     "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
-    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_allreduce_noalloc", "ra_last_error",
+    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc",
+    "ra_last_error",
     "ra_status_string", "RingAllReduce", "EXPORTED",
 ]
 
@@ -106,6 +107,7 @@ EXPORTED = {
                               ctypes.POINTER(ctypes.c_longlong)]),
     "ra_allreduce_noalloc": (_ST, [ctypes.c_int, _SZ, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
                                    ctypes.POINTER(_P), _P]),
+    "ra_read_shadows": (_ST, [_P, ctypes.POINTER(ctypes.c_uint64), _SZ, ctypes.POINTER(_SZ)]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -258,6 +260,15 @@ def ra_read_signals(h):
     return list(buf)[:count.value], ch.value, rd.value, calls.value
 
 
+def ra_read_shadows(h):
+    """The counting barrier's shadows of the last persistent call, flat."""
+    count = _SZ()
+    _check(_lib.ra_read_shadows(h, None, 0, ctypes.byref(count)))
+    buf = (ctypes.c_uint64 * max(count.value, 1))()
+    _check(_lib.ra_read_shadows(h, buf, count.value, ctypes.byref(count)))
+    return list(buf)[:count.value]
+
+
 _DTYPES = {"f32": DType.F32, "bf16": DType.BF16, "i32": DType.I32, "f16": DType.F16, "f64": DType.F64,
            "i64": DType.I64}
 _OPS = {"sum": Op.SUM, "max": Op.MAX}
@@ -316,6 +327,9 @@ class RingAllReduce:
 
     def read_signals(self):
         return ra_read_signals(self.h)
+
+    def read_shadows(self):
+        return ra_read_shadows(self.h)
 
     def close(self):
         if self.h:

@@ -64,7 +64,8 @@ struct DeviceGuard {
 // AllGather).
 struct SlotRegion {
   uint64_t* d = nullptr;
-  size_t cap = 0;       // entries
+  uint64_t* shadows = nullptr;   // counting barrier: the waiters' shadows, cap entries after d
+  size_t cap = 0;       // entries (signals; the shadows take as many again)
   bool owned = false;   // allocated on its own (the counting slots share one allocation)
   int G = 0;            // channel count the slots were last used with
   int J = 0;            // sub-slices (pipelined flags)
@@ -473,10 +474,12 @@ ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
 }
 
 // Zero a region when the launch shape it was counted with changes.
+size_t region_words(const SlotRegion& reg) { return reg.shadows ? 2 * reg.cap : reg.cap; }
+
 ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   if (reg.G != G || reg.J != J) {
     if (reg.cap) {
-      cudaError_t e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
+      cudaError_t e = cudaMemsetAsync(reg.d, 0, region_words(reg) * sizeof(uint64_t), st);
       if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
     }
     reg.G = G;
@@ -509,6 +512,7 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   s = prepare_region(*reg, a.G, 1, st);
   if (s != RA_OK) return s;
   a.slots = reg->d;
+  a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -561,6 +565,7 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   s = prepare_region(*reg, a.G, a.J, st);
   if (s != RA_OK) return s;
   a.slots = reg->d;
+  a.shadows = nullptr;
   a.epoch = (uint64_t)(reg->calls + 1);
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -578,7 +583,7 @@ ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(h->d_err, 0, sizeof(ra_device_error), st);
   for (auto& row : h->region)
     for (auto& reg : row)
-      if (e == cudaSuccess && reg.d && reg.cap) e = cudaMemsetAsync(reg.d, 0, reg.cap * sizeof(uint64_t), st);
+      if (e == cudaSuccess && reg.d && reg.cap) e = cudaMemsetAsync(reg.d, 0, region_words(reg) * sizeof(uint64_t), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "device state reset");
   for (auto& row : h->region)
@@ -662,7 +667,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   for (int k = 0; k < 3; ++k) {
     for (int sy = 0; sy < 3; ++sy) h->region[sy][k].rounds = rounds[k];
     h->region[ra::kSyncCounting][k].cap = region_entries(h, ra::kSyncCounting, rounds[k], gmax, 1);
-    total += h->region[ra::kSyncCounting][k].cap;
+    total += 2 * h->region[ra::kSyncCounting][k].cap;   // signals and shadows
   }
   if (total > 0) {
     e = cudaMalloc(&h->d_slots, total * sizeof(uint64_t));
@@ -679,7 +684,8 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
     size_t o = 0;
     for (auto& r : h->region[ra::kSyncCounting]) {
       r.d = h->d_slots + o;
-      o += r.cap;
+      r.shadows = r.d + r.cap;
+      o += 2 * r.cap;
     }
   }
   e = cudaMalloc(&h->d_err, sizeof(ra_device_error));
@@ -930,6 +936,22 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(dst, reg.d, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "signal read");
+  return RA_OK;
+}
+
+ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count) {
+  if (!h || !count) return fail(RA_ERR_INVALID, "NULL argument");
+  DeviceGuard g(h->device);
+  *count = 0;
+  if (h->last_kind < 0 || h->last_sync != ra::kSyncCounting) return RA_OK;
+  const SlotRegion& reg = h->region[ra::kSyncCounting][h->last_kind];
+  const size_t need = region_entries(h, ra::kSyncCounting, reg.rounds, reg.G, 1);
+  *count = need;
+  if (!dst || need == 0) return RA_OK;
+  if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(dst, reg.shadows, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "shadow read");
   return RA_OK;
 }
 

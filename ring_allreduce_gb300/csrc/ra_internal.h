@@ -86,6 +86,7 @@ struct PersistArgs {
   int rounds;           // ring rounds this call runs
   uint64_t* slots;      // counting: [G][rounds-1][R]; per-peer: [G][rounds-1][R][R];
                         // flags: [G][R][J]
+  uint64_t* shadows;    // counting: each waiter's shadow, laid out as slots
   uint64_t epoch;       // calls on this slot array since it was zeroed, this one included
   int64_t timeout_ns;
   ra_device_error* err;

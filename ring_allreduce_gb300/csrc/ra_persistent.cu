@@ -25,51 +25,41 @@
 // waiter) has its own 64-bit slot, so a count comes only from its round.
 // Release and acquire take the fence form: one fence.acq_rel.gpu before the
 // R-1 relaxed adds, one after the poll has seen its target.
-// Slots are never cleared between calls: the k-th call on a slot array
-// waits for k * (R - 1), compared in 64-bit rolling order (NCCL Device API
-// GIN article, signals and counters).
+// Signals and shadows are never cleared between calls: each waiter's shadow
+// moves by R-1 per call and the signal is compared with it in 64-bit rolling
+// order (NCCL Device API GIN article, signals and counters; the signal layer
+// is ra_signal.cuh).
 //
 // No wait is unbounded: a poll that passes the time limit records
 // (round, rank, channel, observed, expected) in the handle's error record and
 // the CTA returns; every other CTA sees the record at its next poll and
 // returns as well.  Data produced by another CTA of the launch is read
 // through L2 (ld.global.cg), never from a possibly stale L1 line.
-#include "ra_device.cuh"
+#include "ra_signal.cuh"
 
 namespace ra {
 
-// One counting-barrier round.  Returns false when this CTA must stop.
+// One counting-barrier round, on the signal layer (ra_signal.cuh): each
+// peer adds 1 to the waiter's signal of this (channel, round); the waiter
+// moves its shadow forward by R-1 and waits for the signal to meet it.
+// Returns false when this CTA must stop.
 __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    int abort = 0;
-    uint64_t* row = a.slots + ((int64_t)g * (a.rounds - 1) + t) * a.R;
+    const int64_t row = ((int64_t)g * (a.rounds - 1) + t) * a.R;
+    uint64_t* sigs = a.slots + row;
     fence_acq_rel_gpu();   // release: this round's stores of the whole CTA
     if (!(r == a.skip_rank && t == a.skip_round)) {
       for (int q = 0; q < a.R; ++q)
-        if (q != r) signal_add_relaxed(row + q, 1);
+        if (q != r) sig::add(sigs + q, 1);
     }
-    const uint64_t target = a.epoch * (uint64_t)(a.R - 1);
-    const uint64_t t0 = globaltimer_ns();
-    // an iteration bound on top of the clock: every poll costs far more than 1 ns
-    const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+    const uint64_t target = sig::increase_shadow(a.shadows + row + r, (uint64_t)(a.R - 1));
     uint64_t seen = 0;
-    for (uint64_t it = 0;; ++it) {
-      seen = signal_load_relaxed(row + r);
-      if (rolling_reached(seen, target)) {
-        fence_acq_rel_gpu();   // acquire: the peers' round is visible to this CTA
-        break;
-      }
-      if (load_relaxed_u32(&a.err->code) != 0u) { abort = 1; break; }
-      if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
-        // one counting slot cannot say which peer is late: peer = -1
-        record_wait_error(a.err, 1u, t, r, g, -1, seen, target);
-        abort = 1;
-        break;
-      }
-      if (it > 32) __nanosleep(100);
-    }
-    *s_abort = abort;
+    const sig::Wait w = sig::wait(sigs + r, target, 64, a.timeout_ns,
+                                  [&] { return load_relaxed_u32(&a.err->code) != 0u; }, &seen);
+    // one counting slot cannot say which peer is late: peer = -1
+    if (w == sig::kTimedOut) record_wait_error(a.err, 1u, t, r, g, -1, seen, target);
+    *s_abort = w != sig::kReached;
   }
   __syncthreads();
   return *s_abort == 0;

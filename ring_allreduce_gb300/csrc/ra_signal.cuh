@@ -1,0 +1,97 @@
+// ra_signal.cuh -- signals and shadows over device memory, after the GIN
+// signal API of NCCL's Device API (the GIN article, section "信号（Signals）与
+// 计数器（Counters）"), for simulated ranks that are CTAs of one GPU.
+//
+// What the article describes, and how it is kept here:
+//   * a signal is a 64-bit value that remote actions add to; SignalInc may not
+//     be mixed with other operations without a reset, so only Add is offered
+//     (`add`);
+//   * readSignal returns the low `bits` bits, with acquire ordering (`read`);
+//   * waitSignal waits until the low `bits` bits reach a value, compared in
+//     rolling order so that x < x + 1 holds across wrap-around (`wait`);
+//   * resetSignal sets the value to 0 and must not race other updates
+//     (`reset`);
+//   * each signal has a shadow its owner moves at will; increaseSignalShadow
+//     and waitSignalMeetShadow wait for the value to catch up with it
+//     (`increase_shadow`, `wait_meet_shadow`).
+// Release is the caller's: one fence.acq_rel.gpu before a batch of adds
+// publishes everything the CTA wrote before it (the counting barrier issues
+// R-1 adds after one fence).  Every wait is bounded: it gives up after
+// `timeout_ns` (global timer) or an iteration limit, or when `abort()` says
+// another waiter has already given up.
+#pragma once
+
+#include "ra_device.cuh"
+
+namespace ra {
+namespace sig {
+
+enum Wait : int { kReached = 0, kAborted = 1, kTimedOut = 2 };
+
+__device__ __forceinline__ uint64_t low_bits(uint64_t v, int bits) {
+  return bits >= 64 ? v : (v & ((1ull << bits) - 1ull));
+}
+
+// Rolling comparison on the low `bits` bits: has `value` reached `least`?
+__device__ __forceinline__ bool reached(uint64_t value, uint64_t least, int bits = 64) {
+  if (bits >= 64) return (int64_t)(value - least) >= 0;
+  const uint64_t d = low_bits(value - least, bits);
+  return d < (1ull << (bits - 1));
+}
+
+__device__ __forceinline__ void add(uint64_t* sig, uint64_t delta) { signal_add_relaxed(sig, delta); }
+
+__device__ __forceinline__ uint64_t read(const uint64_t* sig, int bits = 64) {
+  const uint64_t v = signal_load_relaxed(sig);
+  fence_acq_rel_gpu();   // acquire
+  return low_bits(v, bits);
+}
+
+__device__ __forceinline__ void reset(uint64_t* sig) { signal_store_relaxed(sig, 0); }
+
+// Shadows belong to one waiter (one thread of one CTA), so plain L2 accesses
+// do; they persist across launches.
+__device__ __forceinline__ uint64_t shadow(const uint64_t* sh) { return __ldcg(reinterpret_cast<const unsigned long long*>(sh)); }
+
+__device__ __forceinline__ uint64_t increase_shadow(uint64_t* sh, uint64_t delta) {
+  const uint64_t v = shadow(sh) + delta;
+  __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
+  return v;
+}
+
+// Wait until the signal reaches `least` (rolling, low `bits` bits).  On
+// kReached the acquire fence has run; *seen holds the last value read.
+template <class Abort>
+__device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bits, int64_t timeout_ns,
+                                     Abort&& abort, uint64_t* seen) {
+  uint64_t v = signal_load_relaxed(sig);
+  if (!reached(v, least, bits)) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t max_iters = (uint64_t)timeout_ns + 1000000ull;   // every poll costs far more than 1 ns
+    for (uint64_t it = 0;; ++it) {
+      if (it > 32) __nanosleep(100);
+      v = signal_load_relaxed(sig);
+      if (reached(v, least, bits)) break;
+      if (abort()) {
+        *seen = v;
+        return kAborted;
+      }
+      if ((int64_t)(globaltimer_ns() - t0) > timeout_ns || it > max_iters) {
+        *seen = v;
+        return kTimedOut;
+      }
+    }
+  }
+  fence_acq_rel_gpu();   // acquire
+  *seen = v;
+  return kReached;
+}
+
+template <class Abort>
+__device__ __forceinline__ Wait wait_meet_shadow(const uint64_t* sig, const uint64_t* sh, int64_t timeout_ns,
+                                                 Abort&& abort, uint64_t* seen) {
+  return wait(sig, shadow(sh), 64, timeout_ns, abort, seen);
+}
+
+}  // namespace sig
+}  // namespace ra

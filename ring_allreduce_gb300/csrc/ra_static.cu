@@ -23,7 +23,8 @@
 namespace ra {
 
 // 64-bit words of scratch: the error record in the first 256 bytes, then the
-// counting barrier's signal slots.  256 KiB + 256 bytes per device.
+// counting barrier's signals followed by the waiters' shadows.  256 KiB +
+// 256 bytes per device.
 constexpr size_t kStaticErrWords = 32;
 constexpr size_t kStaticSlotWords = 32768;
 
@@ -108,15 +109,16 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   int64_t G = (vecs + (int64_t)kPersistThreads * 4 - 1) / ((int64_t)kPersistThreads * 4);
   const int64_t co_resident = (int64_t)bps * sms / R;
   if (G > co_resident) G = co_resident;
-  const int64_t per_channel = (int64_t)(2 * R - 3) * R;   // barrier rounds x waiters
-  if (G > (int64_t)kStaticSlotWords / per_channel) G = (int64_t)kStaticSlotWords / per_channel;
+  // barrier rounds x waiters, for the signals and again for the waiters' shadows
+  const int64_t per_channel = (int64_t)(2 * R - 3) * R;
+  if (G > (int64_t)kStaticSlotWords / (2 * per_channel)) G = (int64_t)kStaticSlotWords / (2 * per_channel);
   if (G < 1)
     return record_error(RA_ERR_INVALID, "R=%d needs %lld signal slots, the static scratch holds %zu", R,
                         (long long)per_channel, kStaticSlotWords);
 
   // every call starts from zeroed slots and a clear error record (epoch 1)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t used = (kStaticErrWords + (size_t)(G * per_channel)) * sizeof(uint64_t);
+  const size_t used = (kStaticErrWords + 2 * (size_t)(G * per_channel)) * sizeof(uint64_t);
   e = cudaMemsetAsync(scratch, 0, used, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -136,6 +138,7 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   a.J = 1;
   a.rounds = 2 * (R - 1);
   a.slots = scratch + kStaticErrWords;
+  a.shadows = a.slots + G * per_channel;
   a.epoch = 1;
   a.timeout_ns = 1000000000LL;
   a.err = reinterpret_cast<ra_device_error*>(scratch);

@@ -203,6 +203,8 @@ def test_barrier_exactly_r_minus_1_arrivals(ra, R, G):
             assert len(slots) == G * rounds * R
             exp = barrier.expected_slot_value(R, k)
             assert all(v == exp for v in slots), slots
+            shadows = h.read_shadows()
+            assert len(shadows) == len(slots) and all(v == exp for v in shadows), shadows
         status, _ = h.device_status()
         assert status == ra.Status.OK
     got = out.host()

@@ -18,6 +18,11 @@ def test_rolling_compare():
     top = (1 << 64) - 1
     assert barrier.rolling_reached(2, top)          # wrapped past the target
     assert not barrier.rolling_reached(top, 2)
+    # counters keep 56 bits (GIN article): the compare looks at those only
+    top56 = (1 << 56) - 1
+    assert barrier.rolling_reached(1, top56, bits=56)
+    assert not barrier.rolling_reached(top56, 1, bits=56)
+    assert barrier.rolling_reached((1 << 60) + 7, 7, bits=56)   # bits above 56 ignored
 
 
 def test_barrier_round_counts():
@@ -38,6 +43,7 @@ def test_exactly_r_minus_1_arrivals_per_slot(R, G):
                 for w in range(R):
                     assert sim.slots[g][t][w] == epoch * (R - 1)
                     assert sim.slots[g][t][w] == barrier.expected_slot_value(R, epoch)
+                    assert sim.shadows[g][t][w] == sim.slots[g][t][w]
 
 
 def test_skipped_arrival_times_out_with_one_missing():
