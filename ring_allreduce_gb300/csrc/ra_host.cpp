@@ -342,7 +342,7 @@ ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* o
   a.plan = pl;
   a.R = R;
   a.mode = mode;
-  int64_t ctas = h->ctas > 0 ? h->ctas : ceil_div(pl.C, (int64_t)ra::kCompactThreads * ra::kCompactPerThread);
+  int64_t ctas = h->ctas > 0 ? h->ctas : ceil_div(ceil_div(pl.C, vec_elems(h->dtype)) + 1, (int64_t)ra::kCompactThreads);
   if (ctas > 65535) ctas = 65535;
   if (ctas < 1) ctas = 1;
   cudaError_t e = ra::launch_compact(h->dtype, h->op, a, (int)ctas, st);

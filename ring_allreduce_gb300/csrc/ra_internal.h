@@ -37,7 +37,7 @@ struct DirectArgs {
 };
 
 // Compact ReduceScatter / AllGather where chunk starts are not 16-byte
-// aligned: one element per thread and step, grid.y = chunk.  in / out hold
+// aligned: one 16-byte output vector per thread and step, grid.y = chunk.  in / out hold
 // full buffers on the full side and compact ones (rank r: its chunk
 // (r+1) mod R only) on the compact side.
 struct CompactArgs {
@@ -99,7 +99,6 @@ cudaError_t launch_direct(int dtype, int op, const DirectArgs& a, int ctas_per_c
 int direct_vectors_per_thread(int R, int mode);
 cudaError_t launch_compact(int dtype, int op, const CompactArgs& a, int ctas_per_chunk, cudaStream_t st);
 constexpr int kCompactThreads = 256;
-constexpr int kCompactPerThread = 4;   // elements a thread takes per step
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st);
 cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st);
 // Per-device set-up of the AllGather kernel (its shared-memory opt-in);
