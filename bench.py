@@ -200,8 +200,9 @@ def _device_ranks(torch, R, n, np_dtype, host=None):
 
 def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True):
     stream = torch.cuda.current_stream()
+    call = h.prepare("allreduce", ins, outs, stream)
     for _ in range(warmup):
-        h.allreduce(ins, outs, stream)
+        call()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
         if per_launch else []
@@ -211,7 +212,7 @@ def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True):
     for i in range(steps):
         if per_launch:
             ev[i][0].record(stream)
-        h.allreduce(ins, outs, stream)
+        call()
         if per_launch:
             ev[i][1].record(stream)
     t1.record(stream)
@@ -253,10 +254,11 @@ def run_gpu_arm(args):
     except Exception:
         pass
     clocks = ClockSampler(gpu_id).start() if (rank == 0 and not args.no_clocks) else None
-    for _ in range(args.warmup):
-        h.allreduce(ins, outs)
-    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    call = h.prepare("allreduce", ins, outs, stream)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -268,7 +270,7 @@ def run_gpu_arm(args):
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        h.allreduce(ins, outs, stream)
+        call()
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()

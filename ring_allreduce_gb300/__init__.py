@@ -13,7 +13,7 @@ _BINDING_NAMES = {
     "ra_reduce_scatter_compact", "ra_all_gather_compact",
     "ra_chunk_plan", "ra_owned_chunk", "ra_set_option", "ra_get_option",
     "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc", "ra_last_error", "ra_status_string",
-    "RingAllReduce", "RAError", "Status", "DType", "Op", "Variant", "Barrier", "Option",
+    "RingAllReduce", "PreparedCall", "RAError", "Status", "DType", "Op", "Variant", "Barrier", "Option",
     "DeviceError", "load_library", "library_path",
 }
 

@@ -19,7 +19,7 @@ __all__ = [
     "ra_all_gather", "ra_allreduce", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc",
     "ra_last_error",
-    "ra_status_string", "RingAllReduce", "EXPORTED",
+    "ra_status_string", "RingAllReduce", "PreparedCall", "EXPORTED",
 ]
 
 
@@ -313,6 +313,15 @@ class RingAllReduce:
         self._ranks(ins, outs)
         ra_all_gather_compact(self.h, ins, outs, stream)
 
+    def prepare(self, kind, ins, outs=None, stream=None):
+        """Marshal the buffers and stream once and return a callable that
+        runs the collective on them: for repeated calls on the same buffers
+        (a training loop's gradient buckets), where rebuilding the pointer
+        arrays each call would cost more than a small collective itself.
+        kind: "allreduce", "reduce_scatter", "all_gather" (ins only),
+        "reduce_scatter_compact" or "all_gather_compact"."""
+        return PreparedCall(self, kind, ins, outs, stream)
+
     def owned_chunk(self, r):
         return ra_owned_chunk(self.h, r)
 
@@ -347,3 +356,29 @@ class RingAllReduce:
             self.close()
         except Exception:
             pass
+
+
+class PreparedCall:
+    """A collective with its arguments marshalled once (see
+    RingAllReduce.prepare).  The buffers must stay alive and in place."""
+
+    def __init__(self, owner, kind, ins, outs, stream):
+        two = {"allreduce": _lib.ra_allreduce, "reduce_scatter": _lib.ra_reduce_scatter,
+               "reduce_scatter_compact": _lib.ra_reduce_scatter_compact,
+               "all_gather_compact": _lib.ra_all_gather_compact}
+        if kind == "all_gather":
+            owner._ranks(ins)
+            self._fn = _lib.ra_all_gather
+            self._args = (owner.h, _ptr_array(ins), _stream(stream))
+        elif kind in two:
+            owner._ranks(ins, outs)
+            self._fn = two[kind]
+            self._args = (owner.h, _ptr_array(ins), _ptr_array(outs), _stream(stream))
+        else:
+            raise ValueError(f"unknown collective {kind!r}")
+        self._owner = owner      # keeps the handle alive
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != Status.OK:
+            raise RAError(st, ra_last_error())

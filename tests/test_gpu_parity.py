@@ -482,3 +482,27 @@ def test_compact_reduce_scatter_and_all_gather(ra, dtype, op):
         for r in range(R):
             assert_bitwise_equal(got_rs[r], want_rs[r], f"RS {dtype}/{op} R={R} n={n} rank {r}")
             assert_bitwise_equal(got_ag[r], want_ag[r], f"AG {dtype}/{op} R={R} n={n} rank {r}")
+
+
+
+def test_prepared_calls_match_oracle(ra):
+    """RingAllReduce.prepare marshals once; repeated calls read the buffers'
+    current contents."""
+    R, n = 8, 2**16 + 5
+    o = elementops.get_op("f32", "sum")
+    inp = DeviceRanks(R, n, np.float32)
+    out = DeviceRanks(R, n, np.float32)
+    for variant in VARIANTS:
+        with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
+            call = h.prepare("allreduce", inp.views, out.views)
+            for seed in (1, 2):
+                x = inputs.generate(R, n, "f32", "normal", seed)
+                inp.big.copy_(DeviceRanks(R, n, np.float32, host=x).big)
+                call()
+                assert h.device_status()[0] == ra.Status.OK
+                want = ring.ring_allreduce(x, o)
+                got = out.host()
+                for r in range(R):
+                    assert_bitwise_equal(got[r], want[r], f"{variant} seed {seed}")
+            with pytest.raises(ValueError):
+                h.prepare("allreduce", inp.views[:3], out.views)
