@@ -338,6 +338,16 @@ __device__ __forceinline__ void record_wait_error(ra_device_error* err, uint32_t
   }
 }
 
+// ------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the kernel before it in the stream is still running; it must wait for that
+// kernel (and the visibility of its memory) before touching data it wrote.
+// Letting dependents launch early only lets their CTAs be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------- TMA bulk copy, mbarrier
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

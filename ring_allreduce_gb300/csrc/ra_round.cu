@@ -16,7 +16,10 @@
 //     tiles in flight per CTA; the unaligned head and tail bytes of a chunk
 //     are copied by the CTA's threads.
 // One launch covers all R ranks of a round (grid.y = rank); the stream
-// order between launches is the round order of the ring.
+// order between launches is the round order of the ring.  Rounds are
+// launched with programmatic dependent launch: a round's CTAs may be
+// scheduled while the previous round drains and wait (griddepcontrol.wait)
+// for its completion before they read.
 #include "ra_device.cuh"
 
 namespace ra {
@@ -28,6 +31,8 @@ __global__ void __launch_bounds__(kRoundThreads)
 rs_round_kernel(const RoundArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
+  griddep_launch_dependents();   // the next round may be scheduled ...
+  griddep_wait();                // ... but this one reads what the previous round wrote
   const int R = a.R, s = a.s, r = blockIdx.y;
   int c = r - s;
   if (c < 0) c += R;
@@ -55,12 +60,29 @@ rs_round_kernel(const RoundArgs a) {
   }
 }
 
+// Launch with programmatic stream serialisation: the kernel may be
+// scheduled while the previous one in the stream drains, and waits for it
+// in griddep_wait().
+template <class K, class A>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const A& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st) {
   if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
   dim3 grid(ctas_per_rank, a.R);
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
-    rs_round_kernel<decltype(d), decltype(o)::value><<<grid, kRoundThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(rs_round_kernel<decltype(d), decltype(o)::value>, grid, dim3(kRoundThreads), 0, st, a);
   });
 }
 
@@ -84,6 +106,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 ag_round_kernel(const CopyArgs a) {
   extern __shared__ __align__(128) uint8_t tiles[];
   __shared__ __align__(8) uint64_t bars[kStages];
+  griddep_launch_dependents();
+  griddep_wait();
   const int R = a.R, s = a.s, r = blockIdx.y;
   int c = (r + 1 - s) % R;
   if (c < 0) c += R;
@@ -161,8 +185,7 @@ cudaError_t prepare_ag_round() {
 cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st) {
   if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
   dim3 grid(ctas_per_rank, a.R);
-  ag_round_kernel<<<grid, kCopyThreads, kCopySmem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(ag_round_kernel, grid, dim3(kCopyThreads), kCopySmem, st, a);
 }
 
 }  // namespace ra
