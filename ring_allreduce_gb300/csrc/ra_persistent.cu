@@ -23,8 +23,8 @@
 // deliberately" explains that a single counter reused across rounds lets a
 // peer a round ahead stand in for a late one; here every (channel, round,
 // waiter) has its own 64-bit slot, so a count comes only from its round.
-// Release and acquire take the fence form: one fence.acq_rel.gpu before the
-// R-1 relaxed adds, one after the poll has seen its target.
+// Release takes the fence form (one fence.acq_rel.gpu before the R-1
+// relaxed adds); the poll uses acquire loads.
 // Signals and shadows are never cleared between calls: each waiter's shadow
 // moves by R-1 per call and the signal is compared with it in 64-bit rolling
 // order (NCCL Device API GIN article, signals and counters; the signal layer
@@ -93,14 +93,11 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
       bool ok = true;
       uint64_t v = 0;
       if (active) {
-        v = signal_load_relaxed(mine + lane);
+        v = signal_load_acquire(mine + lane);   // acquire, by the lane that observes the slot
         ok = rolling_reached(v, a.epoch);
       }
       const unsigned missing = __ballot_sync(0xffffffffu, !ok);
-      if (missing == 0u) {
-        fence_acq_rel_gpu();   // acquire, by every lane that observed a slot
-        break;
-      }
+      if (missing == 0u) break;
       int stop = 0;
       if (lane == 0) {
         if (load_relaxed_u32(&a.err->code) != 0u)

@@ -36,13 +36,13 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
                                           int r, int g, int pred, int* s_abort) {
   if (threadIdx.x == 0) {
     int abort = 0;
-    uint64_t seen = signal_load_relaxed(flag);
+    uint64_t seen = signal_load_acquire(flag);   // acquire: the predecessor's sub-slice is visible
     if (!rolling_reached(seen, target)) {
       const uint64_t t0 = globaltimer_ns();
       const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
       for (uint64_t it = 0;; ++it) {
         if (it > 16) __nanosleep(64);
-        seen = signal_load_relaxed(flag);
+        seen = signal_load_acquire(flag);
         if (rolling_reached(seen, target)) break;
         if (load_relaxed_u32(&a.err->code) != 0u) {
           abort = 1;
@@ -55,7 +55,6 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
         }
       }
     }
-    if (!abort) fence_acq_rel_gpu();   // acquire: the predecessor's sub-slice is visible
     *s_abort = abort;
   }
   __syncthreads();

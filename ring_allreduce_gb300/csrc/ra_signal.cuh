@@ -16,7 +16,7 @@
 //     (`increase_shadow`, `wait_meet_shadow`).
 // Release is the caller's: one fence.acq_rel.gpu before a batch of adds
 // publishes everything the CTA wrote before it (the counting barrier issues
-// R-1 adds after one fence).  Every wait is bounded: it gives up after
+// R-1 adds after one fence); the waits poll with acquire loads.  Every wait is bounded: it gives up after
 // `timeout_ns` (global timer) or an iteration limit, or when `abort()` says
 // another waiter has already given up.
 #pragma once
@@ -42,9 +42,7 @@ __device__ __forceinline__ bool reached(uint64_t value, uint64_t least, int bits
 __device__ __forceinline__ void add(uint64_t* sig, uint64_t delta) { signal_add_relaxed(sig, delta); }
 
 __device__ __forceinline__ uint64_t read(const uint64_t* sig, int bits = 64) {
-  const uint64_t v = signal_load_relaxed(sig);
-  fence_acq_rel_gpu();   // acquire
-  return low_bits(v, bits);
+  return low_bits(signal_load_acquire(sig), bits);
 }
 
 __device__ __forceinline__ void reset(uint64_t* sig) { signal_store_relaxed(sig, 0); }
@@ -59,18 +57,19 @@ __device__ __forceinline__ uint64_t increase_shadow(uint64_t* sh, uint64_t delta
   return v;
 }
 
-// Wait until the signal reaches `least` (rolling, low `bits` bits).  On
-// kReached the acquire fence has run; *seen holds the last value read.
+// Wait until the signal reaches `least` (rolling, low `bits` bits), polling
+// with acquire loads: on kReached the load that saw it ordered what follows;
+// *seen holds the last value read.
 template <class Abort>
 __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bits, int64_t timeout_ns,
                                      Abort&& abort, uint64_t* seen) {
-  uint64_t v = signal_load_relaxed(sig);
+  uint64_t v = signal_load_acquire(sig);
   if (!reached(v, least, bits)) {
     const uint64_t t0 = globaltimer_ns();
     const uint64_t max_iters = (uint64_t)timeout_ns + 1000000ull;   // every poll costs far more than 1 ns
     for (uint64_t it = 0;; ++it) {
       if (it > 32) __nanosleep(100);
-      v = signal_load_relaxed(sig);
+      v = signal_load_acquire(sig);
       if (reached(v, least, bits)) break;
       if (abort()) {
         *seen = v;
@@ -82,7 +81,6 @@ __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bi
       }
     }
   }
-  fence_acq_rel_gpu();   // acquire
   *seen = v;
   return kReached;
 }
