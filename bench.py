@@ -81,6 +81,26 @@ def aggregate(local_seconds, local_units, dist):
     return float(t.item()), float(u.item())
 
 
+def build_info(torch):
+    """What the numbers were taken on: kernel source hashes, toolkit,
+    driver, device (the box has no git history)."""
+    from ring_allreduce_gb300 import build
+    info = {"sources": {k: build.kernel_source_hash(k) for k in build.KERNEL_SOURCES},
+            "torch": torch.__version__}
+    try:
+        out = subprocess.run(["nvcc", "--version"], capture_output=True, text=True, timeout=20).stdout
+        info["nvcc"] = out.strip().splitlines()[-1]
+    except Exception:
+        info["nvcc"] = None
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,name", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().splitlines()[0]
+        info["driver"], info["gpu"] = [x.strip() for x in out.split(",", 1)]
+    except Exception:
+        info["driver"] = info["gpu"] = None
+    return info
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -339,6 +359,8 @@ def run_gpu_arm(args):
     }
     if clk is not None:
         result["clocks"] = clk
+    if rank == 0:
+        result["build"] = build_info(torch)
 
     # ---- other variants, same workload (fewer steps)
     if not args.no_variants and rank == 0:
