@@ -149,8 +149,14 @@ typedef enum ra_option {
                                 directly.  0: always launch directly.  Any
                                 ra_set_option drops the cached graph. */
   RA_OPT_BARRIER = 7,        /* ra_barrier of the persistent variant */
-  RA_OPT_SLICES = 8          /* sub-slices per channel slice of the pipelined
+  RA_OPT_SLICES = 8,         /* sub-slices per channel slice of the pipelined
                                 variant, 1..64; 0 (default) = about 128 KiB each */
+  RA_OPT_GATHER = 9          /* kernel of the direct AllGather (and of the compact
+                                AllGather when chunk starts are 16-byte
+                                aligned): 0 (default) = chosen by the library,
+                                1 = 16-byte vector loads and stores, 2 = TMA
+                                broadcast (each tile loaded once into shared
+                                memory, bulk-stored to every other rank) */
 } ra_option;
 
 /* Device error record, filled by the first wait that gives up. */

@@ -68,6 +68,7 @@ class Option(enum.IntEnum):
     GRAPHS = 6
     BARRIER = 7
     SLICES = 8
+    GATHER = 9
 
 
 class DeviceError(ctypes.Structure):

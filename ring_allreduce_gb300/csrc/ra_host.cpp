@@ -89,6 +89,7 @@ struct ra_ctx {
   int pipe_blocks_per_sm = 0;
   int barrier = RA_BARRIER_COUNTING;
   int slices = 0;
+  int gather = 0;   // RA_OPT_GATHER
   int variant = RA_VARIANT_AUTO;
   long long timeout_ns = 1000000000LL;
   int ctas = 0;
@@ -256,7 +257,37 @@ ra::Ptrs make_ptrs(const ra_ctx* h, const void* const* in, void* const* out) {
   return p;
 }
 
+// The AllGather kernel RA_OPT_GATHER picks (0 = the library's choice).
+bool use_bcast(const ra_ctx* h) { return h->gather == 2; }
+
+ra_status run_bcast(ra_ctx* h, const void* const* src, void* const* dst, bool compact_src, cudaStream_t st) {
+  ra::BcastArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < h->R; ++r) {
+    a.src[r] = src[r];
+    a.dst[r] = dst[r];
+  }
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.elem_bytes = (int)elem_bytes(h->dtype);
+  a.write_owner = compact_src ? 1 : 0;
+  a.src_compact = compact_src ? 1 : 0;
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  int64_t ctas = h->ctas;
+  if (ctas <= 0) {
+    const int64_t tiles = ceil_div(a.plan.C * (int64_t)a.elem_bytes, ra::bcast_tile_bytes()) + 1;
+    const int64_t target = ceil_div((int64_t)h->num_sms * 3, h->R);
+    ctas = tiles < target ? tiles : target;
+  }
+  if (ctas > 65535) ctas = 65535;
+  if (ctas < 1) ctas = 1;
+  cudaError_t e = ra::launch_bcast(a, (int)ctas, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "broadcast kernel launch");
+}
+
 ra_status run_direct(ra_ctx* h, int mode, const void* const* in, void* const* out, cudaStream_t st) {
+  if (mode == ra::kModeAllGather && use_bcast(h)) return run_bcast(h, out, out, false, st);
   ra::DirectArgs a;
   a.p = make_ptrs(h, in, out);
   a.plan = make_plan(h->R, h->n);
@@ -311,6 +342,8 @@ ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* o
   const ra::Plan pl = make_plan(R, h->n);
   size_t off[ra::kMaxRanks], len[ra::kMaxRanks];
   ra_chunk_plan(R, h->n, off, len);
+  if ((pl.C * (int64_t)b) % 16 == 0 && mode == ra::kModeAllGather && use_bcast(h))
+    return run_bcast(h, in, out, true, st);
   if ((pl.C * (int64_t)b) % 16 == 0) {
     // every chunk starts on a 16-byte boundary: the direct kernel, with each
     // compact buffer addressed as if it began at its chunk's offset
@@ -645,6 +678,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   if (e == cudaSuccess) e = ra::pipelined_blocks_per_sm(dtype, op, ra::kPersistThreads, &pbps);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   e = ra::prepare_ag_round();
+  if (e == cudaSuccess) e = ra::prepare_bcast();
   if (e != cudaSuccess) return cuda_fail(e, "AllGather kernel set-up");
 
   ra_ctx* h = new (std::nothrow) ra_ctx();
@@ -855,6 +889,10 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       if (value < 0 || value > kMaxSlices) return fail(RA_ERR_INVALID, "slices %lld outside [0, %d]", value, kMaxSlices);
       h->slices = (int)value;
       return RA_OK;
+    case RA_OPT_GATHER:
+      if (value < 0 || value > 2) return fail(RA_ERR_INVALID, "gather kernel %lld outside [0, 2]", value);
+      h->gather = (int)value;
+      return RA_OK;
     case RA_OPT_TIMEOUT_NS:
       if (value < 1000) return fail(RA_ERR_INVALID, "timeout %lld ns below 1 us", value);
       h->timeout_ns = value;
@@ -886,6 +924,7 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_GRAPHS: *value = h->use_graphs; return RA_OK;
     case RA_OPT_BARRIER: *value = h->barrier; return RA_OK;
     case RA_OPT_SLICES: *value = h->slices; return RA_OK;
+    case RA_OPT_GATHER: *value = h->gather; return RA_OK;
     default: return fail(RA_ERR_INVALID, "unknown option %d", key);
   }
 }

@@ -36,6 +36,21 @@ struct DirectArgs {
   int write_owner;      // AllGather: also write the owner's output (compact input)
 };
 
+// AllGather as a TMA broadcast: chunk k read once from its owner (rank k-1)
+// and stored to every other rank (and to the owner too with write_owner).
+// src_compact: the owner's src buffer holds only its chunk.
+struct BcastArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  Plan plan;
+  int R;
+  int elem_bytes;
+  int write_owner;
+  int src_compact;
+  int64_t timeout_ns;
+  ra_device_error* err;
+};
+
 // Compact ReduceScatter / AllGather where chunk starts are not 16-byte
 // aligned: one 16-byte output vector per thread and step, grid.y = chunk.  in / out hold
 // full buffers on the full side and compact ones (rank r: its chunk
@@ -98,6 +113,9 @@ cudaError_t launch_direct(int dtype, int op, const DirectArgs& a, int ctas_per_c
 // 16-byte vectors a thread of the direct kernel takes per step.
 int direct_vectors_per_thread(int R, int mode);
 cudaError_t launch_compact(int dtype, int op, const CompactArgs& a, int ctas_per_chunk, cudaStream_t st);
+cudaError_t launch_bcast(const BcastArgs& a, int ctas_per_chunk, cudaStream_t st);
+cudaError_t prepare_bcast();   // per-device shared-memory opt-in, as prepare_ag_round
+int bcast_tile_bytes();
 constexpr int kCompactThreads = 256;
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st);
 cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st);

@@ -506,3 +506,32 @@ def test_prepared_calls_match_oracle(ra):
                     assert_bitwise_equal(got[r], want[r], f"{variant} seed {seed}")
             with pytest.raises(ValueError):
                 h.prepare("allreduce", inp.views[:3], out.views)
+
+
+@pytest.mark.parametrize("gather", [1, 2])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f64"])
+def test_all_gather_kernels(ra, gather, dtype):
+    """Both AllGather kernels of the direct variant (16-byte vectors; TMA
+    broadcast through shared memory), in place and compact, bitwise."""
+    o = elementops.get_op(dtype, "sum")
+    st = inputs.storage_dtype(dtype)
+    for i, (R, n) in enumerate(SHAPES + [(8, 8 * 40000), (4, 4 * 16384 * 3 + 8)]):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=800 + i)
+        rs = ring.ring_reduce_scatter(x, o, fill=np.zeros(1, st)[0])
+        want = ring.ring_all_gather(rs, o)
+        got = run_gpu(ra, rs, dtype, "sum", "direct", kind="all_gather", inplace=True,
+                      options=[(ra.Option.GATHER, gather)])
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"gather={gather} {dtype} R={R} n={n} rank {r}")
+        chunks = ring.ring_reduce_scatter_compact(x, o)
+        lengths = [len(c) for c in chunks]
+        cmp = DeviceBuffers(lengths, st, host=chunks)
+        full = DeviceRanks(R, n, st)
+        with ra.RingAllReduce(R, n, dtype, "sum") as h:
+            h.set_option(ra.Option.GATHER, gather)
+            h.all_gather_compact(cmp.ptrs(), full.ptrs())
+            assert h.device_status()[0] == ra.Status.OK
+        assert cmp.guards_intact() and full.guards_intact()
+        got = full.host()
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"compact gather={gather} {dtype} R={R} n={n} rank {r}")
