@@ -619,7 +619,7 @@ def run_extras(args):
                               "frac": round(byts / t / 1e9 / peak, 4)}), flush=True)
         del ins, outs
         torch.cuda.empty_cache()
-    for dt, n in (("f32", 2**24), ("bf16", 2**26 + 3)):
+    for dt, n in (("f32", 2**24), ("bf16", 2**26 + 3), ("i32", 2**24)):
         b = inputs.itemsize(dt)
         st = inputs.storage_dtype(dt)
         host = inputs.generate(R, n, dt, dists[dt], 1)
@@ -628,9 +628,15 @@ def run_extras(args):
         h = ra.RingAllReduce(R, n, dt, "sum")
         lens = [h.owned_chunk(r)[1] for r in range(R)]
         cmp = [torch.empty(((L + 63) // 64) * 64, dtype=full_big.dtype, device="cuda")[:L] for L in lens]
+        def gather_tma():
+            hg.all_gather(full)
+
+        hg = ra.RingAllReduce(R, n, dt, "sum")
+        hg.set_option(ra.Option.GATHER, 2)
         cases = [
             ("reduce_scatter", lambda: h.reduce_scatter(ins, full), (R + 1) * n * b),
             ("all_gather", lambda: h.all_gather(full), R * n * b),
+            ("all_gather_tma_broadcast", gather_tma, R * n * b),
             ("reduce_scatter_compact", lambda: h.reduce_scatter_compact(ins, cmp), (R + 1) * n * b),
             ("all_gather_compact", lambda: h.all_gather_compact(cmp, full), (R + 1) * n * b),
         ]
@@ -641,7 +647,9 @@ def run_extras(args):
                               "us": round(t * 1e6, 2), "frac": round(byts / t / 1e9 / peak, 4),
                               "bytes": byts}), flush=True)
         assert h.device_status()[0] == ra.Status.OK
+        assert hg.device_status()[0] == ra.Status.OK
         h.close()
+        hg.close()
         del ins, full, full_big, cmp
         torch.cuda.empty_cache()
 
