@@ -83,7 +83,7 @@ def aggregate(local_seconds, local_units, dist):
 
 def build_info(torch):
     """What the numbers were taken on: kernel source hashes, toolkit,
-    driver, device (the box has no git history)."""
+    driver, device (a copy of the sources need not carry its git history)."""
     from ring_allreduce_gb300 import build
     info = {"sources": {k: build.kernel_source_hash(k) for k in build.KERNEL_SOURCES},
             "torch": torch.__version__}

@@ -4,7 +4,7 @@ n = 2^31 + 3 int32 elements per rank (8 GiB per buffer, ragged chunks that
 straddle the 2^31 boundary): too large for the CPU oracle, so the inputs are
 built on the device from a closed form, x_0[i] = i mod 1000 and x_1[i] = 7,
 whose sum S[i] = (i mod 1000) + 7 and maximum are known exactly; outputs are
-compared with them on the device (torch is only the checker here).  Every
+compared with them on the device (torch only verifies here).  Every
 variant, in place and not."""
 
 import numpy as np
