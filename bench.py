@@ -542,6 +542,7 @@ SWEEP_VARIANTS = [
     ("ring", "ring", lambda ra: []),
     ("persistent", "persistent", lambda ra: []),
     ("persistent_per_peer", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
+    ("persistent_cluster", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
     ("pipelined", "pipelined", lambda ra: []),
 ]
 
@@ -563,7 +564,11 @@ def run_barriers(args):
         line = {"barriers": "persistent, one channel", "R": R, "n_per_rank": n, "barrier_rounds": 2 * R - 3}
         for name, v, opts in (("counting", "persistent", []),
                               ("per_peer", "persistent", [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
+                              ("cluster", "persistent", [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
                               ("pipelined", "pipelined", [])):
+            if name == "cluster" and R > 16:
+                line[name] = None
+                continue
             h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
             h.set_option(ra.Option.CTAS, 1)
             for key, value in opts:
@@ -669,6 +674,9 @@ def run_sweep(args):
         _, outs = _device_ranks(torch, R, n, inputs.storage_dtype("f32"))
         line = {"sweep": "r8_f32_n" if R == 8 else "f32_R", "R": R, "n_per_rank": n}
         for name, v, opts in SWEEP_VARIANTS:
+            if name == "persistent_cluster" and R > 16:
+                line[name] = None
+                continue
             h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
             for key, value in opts(ra):
                 h.set_option(key, value)

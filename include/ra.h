@@ -116,9 +116,13 @@ typedef enum ra_barrier {
                                  each of the R-1 peers adds 1 ("comm: lift the
                                  GIN scale-out ceiling by making the rail
                                  barrier a counting barrier", section "Fix") */
-  RA_BARRIER_PER_PEER = 1     /* one signal per (channel, round, waiter, peer),
+  RA_BARRIER_PER_PEER = 1,    /* one signal per (channel, round, waiter, peer),
                                  the design that page replaced; a wait that runs
                                  out can name the missing peer */
+  RA_BARRIER_CLUSTER = 2      /* the R CTAs of a channel form one thread-block
+                                 cluster and meet at the hardware cluster
+                                 barrier (R <= 16, else RA_ERR_UNSUPPORTED);
+                                 no signal memory, no cooperative launch */
 } ra_barrier;
 
 typedef enum ra_option {

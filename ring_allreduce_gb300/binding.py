@@ -57,6 +57,7 @@ class Variant(enum.IntEnum):
 class Barrier(enum.IntEnum):
     COUNTING = 0
     PER_PEER = 1
+    CLUSTER = 2
 
 
 class Option(enum.IntEnum):

@@ -522,8 +522,45 @@ ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   return RA_OK;
 }
 
+// Persistent variant with the R CTAs of each channel in one thread-block
+// cluster: no signal memory, no co-residency across channels.
+ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
+                                 cudaStream_t st) {
+  if (h->R > 16) return fail(RA_ERR_UNSUPPORTED, "cluster barrier needs R <= 16 (R=%d)", h->R);
+  int clusters = 0;
+  cudaError_t e = ra::persistent_cluster_capacity(h->dtype, h->op, h->R, ra::kPersistThreads, &clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "cluster occupancy query");
+  if (clusters < 1) return fail(RA_ERR_UNSUPPORTED, "a cluster of %d CTAs does not fit", h->R);
+  ra::PersistArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.sync = ra::kSyncCluster;
+  a.J = 1;
+  a.rounds = h->region[ra::kSyncCounting][kind].rounds;
+  if (h->ctas > 0) {
+    a.G = h->ctas;
+  } else {
+    const int64_t vecs = ceil_div(a.plan.C, vec_elems(h->dtype)) + 1;
+    int64_t G = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
+    if (G > clusters) G = clusters;          // one wave of clusters
+    a.G = (int)(G < 1 ? 1 : G);
+  }
+  if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
+  a.epoch = 1;
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  a.skip_rank = -1;
+  a.skip_round = -1;
+  e = ra::launch_persistent_cluster(h->dtype, h->op, a, ra::kPersistThreads, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "cluster kernel launch");
+}
+
 ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                          cudaStream_t st) {
+  if (h->barrier == RA_BARRIER_CLUSTER) return run_persistent_cluster(h, kind, mode, in, out, st);
   const int sync = h->barrier == RA_BARRIER_PER_PEER ? ra::kSyncPerPeer : ra::kSyncCounting;
   SlotRegion* reg = nullptr;
   ra_status s = ensure_region(h, sync, kind, &reg);
@@ -679,6 +716,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   e = ra::prepare_ag_round();
   if (e == cudaSuccess) e = ra::prepare_bcast();
+  if (e == cudaSuccess) e = ra::prepare_persistent_cluster();
   if (e != cudaSuccess) return cuda_fail(e, "AllGather kernel set-up");
 
   ra_ctx* h = new (std::nothrow) ra_ctx();
@@ -881,7 +919,7 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       h->variant = (int)value;
       return RA_OK;
     case RA_OPT_BARRIER:
-      if (value != RA_BARRIER_COUNTING && value != RA_BARRIER_PER_PEER)
+      if (value != RA_BARRIER_COUNTING && value != RA_BARRIER_PER_PEER && value != RA_BARRIER_CLUSTER)
         return fail(RA_ERR_INVALID, "unknown barrier %lld", value);
       h->barrier = (int)value;
       return RA_OK;

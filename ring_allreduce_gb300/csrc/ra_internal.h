@@ -85,7 +85,8 @@ struct CopyArgs {
 enum Sync : int {
   kSyncCounting = 0,   // one slot per (channel, round, waiter); each peer adds 1
   kSyncPerPeer = 1,    // one slot per (channel, round, waiter, peer); each peer stores the epoch
-  kSyncFlags = 2       // pipelined variant: one progress flag per (channel, rank, sub-slice)
+  kSyncFlags = 2,      // pipelined variant: one progress flag per (channel, rank, sub-slice)
+  kSyncCluster = 3     // the R CTAs of a channel form one thread-block cluster: hardware barrier
 };
 
 // Persistent and pipelined variants: one cooperative launch of R*G CTAs
@@ -123,6 +124,12 @@ cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t s
 // call with the device current before its first launch there.
 cudaError_t prepare_ag_round();
 cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
+// Cluster launch (one cluster of R CTAs per channel, no cooperative launch);
+// prepare once per device: allows clusters of up to 16 CTAs.
+cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
+cudaError_t prepare_persistent_cluster();
+// Clusters of R CTAs of `threads` threads that can be resident at once (0: none fit).
+cudaError_t persistent_cluster_capacity(int dtype, int op, int R, int threads, int* clusters);
 // Co-resident CTAs per SM of the persistent kernel for `threads` threads.
 cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks);
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);

@@ -30,6 +30,10 @@
 // order (NCCL Device API GIN article, signals and counters; the signal layer
 // is ra_signal.cuh).
 //
+// With RA_BARRIER_CLUSTER the R CTAs of a channel are launched as one
+// thread-block cluster and meet at the hardware cluster barrier instead
+// (R <= 16; no cooperative launch needed, as no cluster waits on another).
+//
 // No wait is unbounded: a poll that passes the time limit records
 // (round, rank, channel, observed, expected) in the handle's error record and
 // the CTA returns; every other CTA sees the record at its next poll and
@@ -121,6 +125,15 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
   return *s_abort == 0;
 }
 
+// Round boundary when the R CTAs of a channel form one thread-block cluster:
+// the hardware cluster barrier, release on arrival and acquire on the wait, at
+// cluster scope -- the scope that holds every CTA this one exchanges data with.
+// All threads of all R CTAs take it, the same number of times, and clusters
+// are scheduled whole, so no CTA can wait on one that is not running.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 template <class D, int OP>
 __device__ __forceinline__ void reduce_slice(const typename D::T* inc, const typename D::T* loc,
                                              typename D::T* dst, int64_t off, int64_t end, int g, int G) {
@@ -196,6 +209,10 @@ persistent_kernel(const PersistArgs a) {
       }
     }
     if (t + 1 < a.rounds) {
+      if (a.sync == kSyncCluster) {
+        cluster_barrier();
+        continue;
+      }
       const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
                                               : counting_barrier(a, g, t, r, &s_abort);
       if (!go) return;
@@ -216,6 +233,50 @@ cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks
   const void* fn = persistent_select(dtype, op);
   if (!fn) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
+}
+
+cudaError_t prepare_persistent_cluster() {
+  cudaError_t err = cudaSuccess;
+  for (int dt = RA_F32; dt <= RA_I64 && err == cudaSuccess; ++dt)
+    for (int op = RA_SUM; op <= RA_MAX && err == cudaSuccess; ++op)
+      err = cudaFuncSetAttribute(persistent_select(dt, op), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return err;
+}
+
+static cudaLaunchConfig_t cluster_config(const PersistArgs& a, int threads, cudaStream_t st,
+                                         cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.R * a.G);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.R;   // CTA (r, g) = blockIdx.x = g*R + r: rank r of cluster g
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+cudaError_t persistent_cluster_capacity(int dtype, int op, int R, int threads, int* clusters) {
+  const void* fn = persistent_select(dtype, op);
+  if (!fn || R < 2 || R > 16) return cudaErrorInvalidValue;
+  PersistArgs a;
+  a.R = R;
+  a.G = 1;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(a, threads, 0, attr);
+  return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
+}
+
+cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
+  const void* fn = persistent_select(dtype, op);
+  if (!fn || a.R < 2 || a.R > 16 || a.G < 1 || a.rounds < 1 || a.sync != kSyncCluster) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(a, threads, st, attr);
+  void* args[] = {const_cast<PersistArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {

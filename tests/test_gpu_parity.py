@@ -535,3 +535,31 @@ def test_all_gather_kernels(ra, gather, dtype):
         got = full.host()
         for r in range(R):
             assert_bitwise_equal(got[r], want[r], f"compact gather={gather} {dtype} R={R} n={n} rank {r}")
+
+
+
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "sum"), ("i32", "max"), ("f64", "sum")])
+def test_cluster_barrier_matches_oracle(ra, dtype, op):
+    """Persistent variant with each channel's R CTAs in one thread-block
+    cluster (hardware cluster barrier between rounds); R <= 16."""
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=900 + i)
+        opts = [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]
+        if R > 16:
+            with pytest.raises(ra.RAError) as e:
+                run_gpu(ra, x, dtype, op, "persistent", options=opts)
+            assert e.value.status == ra.Status.ERR_UNSUPPORTED
+            continue
+        for kind in ("allreduce", "reduce_scatter"):
+            got = run_gpu(ra, x, dtype, op, "persistent", kind=kind, options=opts)
+            if kind == "allreduce":
+                want = ring.ring_allreduce(x, o)
+                for r in range(R):
+                    assert_bitwise_equal(got[r], want[r], f"cluster {dtype}/{op} R={R} n={n} rank {r}")
+            else:
+                want = ring.ring_reduce_scatter(x, o)
+                plan = ring.chunk_plan(R, n)
+                for r in range(R):
+                    off, L = plan[ring.owned_chunk(R, r)]
+                    assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"cluster RS R={R} n={n}")
