@@ -365,14 +365,14 @@ def run_gpu_arm(args):
     # ---- other variants, same workload (fewer steps)
     if not args.no_variants and rank == 0:
         var = {}
-        for v in ("direct", "ring", "persistent", "pipelined"):
+        for v in ("direct", "ring", "persistent", "pipelined", "local"):
             hv = ra.RingAllReduce(R, n, dtype, op, variant=v)
             steps_v = max(5, min(args.steps, 100))
             total_ms, lm = _time_variant(torch, ra, hv, ins, outs, steps_v, max(3, args.warmup // 4 or 3))
             assert hv.device_status()[0] == ra.Status.OK
             hv.close()
             t = statistics.mean(lm) / 1e3
-            by = compulsory if v == "direct" else ring_bytes
+            by = compulsory if v in ("direct", "local") else ring_bytes
             var[v] = {"algbw": round(n * b / t / 1e9, 3),
                       "us_per_call": round(t * 1e6, 2),
                       "frac_compulsory": round(compulsory / t / 1e9 / peak, 4),
@@ -544,6 +544,7 @@ SWEEP_VARIANTS = [
     ("persistent_per_peer", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
     ("persistent_cluster", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
     ("pipelined", "pipelined", lambda ra: []),
+    ("local", "local", lambda ra: []),
 ]
 
 
@@ -701,7 +702,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="r8_f32", choices=["r8_f32", "r8_bf16", "r16_i32", "r4_small"])
     ap.add_argument("--n", type=int, default=None, help="override n per rank (profiling of a smaller case)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined", "local"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--barriers", action="store_true", help="barrier cost vs R, counting vs per-peer")
     ap.add_argument("--extras", action="store_true", help="other dtypes and collectives (direct kernel)")

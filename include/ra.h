@@ -102,12 +102,18 @@ typedef enum ra_variant {
                                  simulated ranks meet at a barrier between
                                  rounds (RA_OPT_BARRIER: counting, the
                                  default, or per-peer) */
-  RA_VARIANT_PIPELINED = 4    /* one cooperative launch running every round
+  RA_VARIANT_PIPELINED = 4,   /* one cooperative launch running every round
                                  with no barrier: a rank starts a round on a
                                  sub-slice as soon as its predecessor has
                                  finished the previous round on it
                                  (per-predecessor progress flags; rounds of
                                  different sub-slices overlap) */
+  RA_VARIANT_LOCAL = 5        /* one launch, each CTA running every ring round
+                                 for one slice of every chunk: the ranks'
+                                 messages pass through shared memory, rounds
+                                 end at __syncthreads; reads each input once,
+                                 writes each output once, no waits between
+                                 CTAs */
 } ra_variant;
 
 /* Barrier of the persistent variant (RA_OPT_BARRIER). */
@@ -129,7 +135,8 @@ typedef enum ra_option {
   RA_OPT_VARIANT = 1,        /* ra_variant, default RA_VARIANT_AUTO */
   RA_OPT_TIMEOUT_NS = 2,     /* limit of every device-side wait in ns, default 1e9 */
   RA_OPT_CTAS = 3,           /* CTAs per rank (ring, persistent) or per chunk
-                                (direct); 0 = chosen from the SM count */
+                                (direct), or in all (local); 0 = chosen
+                                from the SM count */
   RA_OPT_CHECK_POINTERS = 4, /* 1 (default): a call checks with
                                 cudaPointerGetAttributes that every buffer is
                                 device memory of the handle's device; a call

@@ -52,6 +52,7 @@ class Variant(enum.IntEnum):
     RING = 2
     PERSISTENT = 3
     PIPELINED = 4
+    LOCAL = 5
 
 
 class Barrier(enum.IntEnum):

@@ -23,7 +23,7 @@ LIB_NAME = "libra_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_pipelined.cu", "ra_compact.cu",
-           "ra_bcast.cu", "ra_static.cu"]
+           "ra_bcast.cu", "ra_static.cu", "ra_local.cu"]
 # (source, object stem, preprocessor definitions): ra_direct_inst.cu is
 # compiled once per dtype so its instantiations build in parallel
 DTYPES = ["RA_F32", "RA_BF16", "RA_I32", "RA_F16", "RA_F64", "RA_I64"]
@@ -57,6 +57,7 @@ KERNEL_SOURCES = {
     "pipelined": ["ra_pipelined.cu", "ra_device.cuh", "ra_internal.h"],
     "compact": ["ra_compact.cu", "ra_device.cuh", "ra_internal.h"],
     "bcast": ["ra_bcast.cu", "ra_device.cuh", "ra_internal.h"],
+    "local": ["ra_local.cu", "ra_device.cuh", "ra_internal.h"],
 }
 
 

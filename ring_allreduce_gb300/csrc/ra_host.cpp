@@ -6,6 +6,7 @@
 // chunks of about N/k), read as C = ceil(n/R), chunk k = [kC, min((k+1)C, n)).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -87,6 +88,7 @@ struct ra_ctx {
   int num_sms = 0;
   int persist_blocks_per_sm = 0;
   int pipe_blocks_per_sm = 0;
+  int local_blocks_per_sm = 0;
   int barrier = RA_BARRIER_COUNTING;
   int slices = 0;
   int gather = 0;   // RA_OPT_GATHER
@@ -296,6 +298,36 @@ ra_status run_direct(ra_ctx* h, int mode, const void* const* in, void* const* ou
   a.write_owner = 0;
   cudaError_t e = ra::launch_direct(h->dtype, h->op, a, direct_ctas_per_chunk(h, a.plan, mode), st);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "direct kernel launch");
+}
+
+// Local variant: slices of SV whole 16-byte vectors per chunk, one CTA per
+// slice at a time (grid-stride over slices); RA_OPT_CTAS sets the grid.
+ra_status run_local(ra_ctx* h, int mode, const void* const* in, void* const* out, cudaStream_t st) {
+  ra::LocalArgs a;
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.SV = ra::local_slice_vectors(h->R);
+  const int64_t V = 16 / (int64_t)elem_bytes(h->dtype);
+  int64_t most = 0;
+  for (int k = 0; k < h->R; ++k) {
+    const int64_t off = std::min((int64_t)k * a.plan.C, a.plan.n);
+    const int64_t end = std::min(off + a.plan.C, a.plan.n);
+    const int64_t vb = (off + V - 1) / V, ve = end / V;
+    if (ve > vb) most = std::max(most, ve - vb);
+  }
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  // narrow the slices so that every CTA gets the same number of them (within one)
+  int64_t ctas = h->ctas > 0 ? h->ctas : (int64_t)h->num_sms * std::max(1, h->local_blocks_per_sm);
+  const int64_t per_cta = std::max<int64_t>(1, ceil_div(ceil_div(most, a.SV), ctas));
+  a.SV = (int)std::max<int64_t>(1, std::min<int64_t>(a.SV, ceil_div(most, per_cta * ctas)));
+  a.slices = std::max<int64_t>(1, ceil_div(most, a.SV));
+  ctas = std::min(ctas, a.slices);
+  if (ctas > 0x7fffffff) ctas = 0x7fffffff;
+  cudaError_t e = ra::launch_local(h->dtype, h->op, a, (int)ctas, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "local kernel launch");
 }
 
 // Compact ReduceScatter (compact_out) or AllGather (compact_in): the
@@ -717,7 +749,13 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   e = ra::prepare_ag_round();
   if (e == cudaSuccess) e = ra::prepare_bcast();
   if (e == cudaSuccess) e = ra::prepare_persistent_cluster();
-  if (e != cudaSuccess) return cuda_fail(e, "AllGather kernel set-up");
+  if (e == cudaSuccess) e = ra::prepare_local();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel set-up");
+  int lbps = 0;
+  if (R >= 2) {
+    e = ra::local_blocks_per_sm(dtype, op, R, &lbps);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  }
 
   ra_ctx* h = new (std::nothrow) ra_ctx();
   if (!h) return fail(RA_ERR_OOM, "host allocation failed");
@@ -729,6 +767,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   h->num_sms = sms;
   h->persist_blocks_per_sm = coop ? bps : 0;
   h->pipe_blocks_per_sm = coop ? pbps : 0;
+  h->local_blocks_per_sm = lbps;
 
   // counting-barrier slots: per kind, the most channels that can be
   // co-resident x barrier rounds x waiters (the other schemes allocate theirs
@@ -810,6 +849,8 @@ ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, voi
       return run_persistent(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
     case RA_VARIANT_PIPELINED:
       return run_pipelined(h, kKindAllReduce, ra::kModeAllReduce, in, out, st);
+    case RA_VARIANT_LOCAL:
+      return run_local(h, ra::kModeAllReduce, in, out, st);
     default:
       return run_direct(h, ra::kModeAllReduce, in, out, st);
   }
@@ -835,6 +876,8 @@ ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out
       return run_persistent(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
     case RA_VARIANT_PIPELINED:
       return run_pipelined(h, kKindReduceScatter, ra::kModeReduceScatter, in, out, st);
+    case RA_VARIANT_LOCAL:
+      return run_local(h, ra::kModeReduceScatter, in, out, st);
     default:
       return run_direct(h, ra::kModeReduceScatter, in, out, st);
   }
@@ -856,6 +899,8 @@ ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
       return run_persistent(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
     case RA_VARIANT_PIPELINED:
       return run_pipelined(h, kKindAllGather, ra::kModeAllGather, buf, buf, st);
+    case RA_VARIANT_LOCAL:
+      return run_local(h, ra::kModeAllGather, buf, buf, st);
     default:
       return run_direct(h, ra::kModeAllGather, buf, buf, st);
   }
@@ -911,7 +956,7 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       h->use_graphs = value != 0;
       return RA_OK;
     case RA_OPT_VARIANT:
-      if (value < RA_VARIANT_AUTO || value > RA_VARIANT_PIPELINED)
+      if (value < RA_VARIANT_AUTO || value > RA_VARIANT_LOCAL)
         return fail(RA_ERR_INVALID, "unknown variant %lld", value);
       if ((value == RA_VARIANT_PERSISTENT && h->persist_blocks_per_sm == 0) ||
           (value == RA_VARIANT_PIPELINED && h->pipe_blocks_per_sm == 0))

@@ -81,6 +81,19 @@ struct CopyArgs {
   ra_device_error* err;
 };
 
+// Local variant: one CTA runs every ring round for slice g of every chunk
+// (SV 16-byte vectors per chunk), g = blockIdx.x, blockIdx.x + gridDim.x, ...
+struct LocalArgs {
+  Ptrs p;
+  Plan plan;
+  int R;
+  int mode;
+  int SV;               // 16-byte vectors of each chunk per slice, 1..local_slice_vectors(R)
+  int64_t slices;       // slices per chunk: ceil(most whole vectors in a chunk / SV)
+  int64_t timeout_ns;   // bound of every mbarrier wait
+  ra_device_error* err;
+};
+
 // How the ranks of a channel synchronise between rounds.
 enum Sync : int {
   kSyncCounting = 0,   // one slot per (channel, round, waiter); each peer adds 1
@@ -135,9 +148,18 @@ cudaError_t persistent_blocks_per_sm(int dtype, int op, int threads, int* blocks
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st);
 cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks);
 
+cudaError_t launch_local(int dtype, int op, const LocalArgs& a, int ctas, cudaStream_t st);
+cudaError_t prepare_local();   // per-device shared-memory opt-in
+cudaError_t local_blocks_per_sm(int dtype, int op, int R, int* blocks);
+int local_slice_vectors(int R);
+size_t local_smem_bytes(int R);
+
 constexpr int kDirectThreads = 256;
 constexpr int kRoundThreads = 256;
 constexpr int kCopyThreads = 32;
 constexpr int kPersistThreads = 512;
+constexpr int kLocalThreads = 256;   // warp 0 issues the bulk copies, 7 warps fold
+constexpr int kLocalSliceItems = 896;    // R * SV <= 896: 16-byte vectors per stage (14 KiB), 4 per folding thread
+constexpr int kLocalStages = 6;          // load steps in flight or in use per CTA
 
 }  // namespace ra

@@ -93,7 +93,7 @@ static int run(int R, size_t n, int variant) {
 
 int main(void) {
   static const int variants[] = {RA_VARIANT_AUTO, RA_VARIANT_DIRECT, RA_VARIANT_RING, RA_VARIANT_PERSISTENT,
-                                 RA_VARIANT_PIPELINED};
+                                 RA_VARIANT_PIPELINED, RA_VARIANT_LOCAL};
   static const int ranks[] = {2, 4, 7, 16};
   static const size_t sizes[] = {1, 4096, 100003};
   size_t off[4], len[4];

@@ -17,7 +17,7 @@ from rahelpers import DeviceRanks, assert_bitwise_equal
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-VARIANTS = ["direct", "ring", "persistent", "pipelined"]
+VARIANTS = ["direct", "ring", "persistent", "pipelined", "local"]
 
 
 @pytest.fixture(scope="module")

@@ -14,7 +14,7 @@ from rahelpers import DeviceBuffers, DeviceRanks, assert_bitwise_equal
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-VARIANTS = ["direct", "ring", "persistent", "pipelined"]
+VARIANTS = ["direct", "ring", "persistent", "pipelined", "local"]
 DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
              ("i32", "sum"), ("i32", "max"), ("f16", "sum"), ("f16", "max"),
              ("f64", "sum"), ("f64", "max"), ("i64", "sum"), ("i64", "max")]
