@@ -158,8 +158,5 @@ constexpr int kDirectThreads = 256;
 constexpr int kRoundThreads = 256;
 constexpr int kCopyThreads = 32;
 constexpr int kPersistThreads = 512;
-constexpr int kLocalThreads = 256;   // warp 0 issues the bulk copies, 7 warps fold
-constexpr int kLocalSliceItems = 896;    // R * SV <= 896: 16-byte vectors per stage (14 KiB), 4 per folding thread
-constexpr int kLocalStages = 6;          // load steps in flight or in use per CTA
 
 }  // namespace ra

@@ -7,8 +7,8 @@
 //   ReduceScatter round s = 1..R-1: every rank r at once forms
 //     m_r = m_{r-1} (+) x_r[c],  c = (r - s) mod R,
 //   where m_{r-1} is what rank r-1 made in round s-1 (x_{r-1}[c] itself in
-//   round 1), and a CTA barrier ends the round.  In round R-1, m_r is
-//   S_{(r+1) mod R}: rank r stores it to its own output (the
+//   round 1), and a barrier of the folding warps ends the round.  In round
+//   R-1, m_r is S_{(r+1) mod R}: rank r stores it to its own output (the
 //   recvReduceCopySend of section 9) and keeps it.
 //   AllGather round s = 1..R-1: rank r copies chunk (r+1-s) mod R -- the
 //   S kept by rank r-s -- to its output.
@@ -16,28 +16,30 @@
 // compulsory 2 R n b bytes, with no synchronisation between CTAs.
 //
 // Loads never stall a round.  Warp 0 streams the operands into a ring of
-// kStages shared-memory stages with TMA bulk copies (cp.async.bulk,
-// mbarrier completion; lane r copies rank r's part), in load steps that run
-// ahead of the rounds and across slice boundaries: step 0 of a slice holds
-// x_r[r] for every r (round 1's incoming messages), step s holds
-// x_r[(r - s) mod R].  Round s writes m_r over x_r[c] in step s's stage, so
-// that stage is round s+1's incoming messages and no other buffer is
-// needed; a step's stage is refilled once the round after it is done (the
-// last step's, once its results are stored).  The CTA's threads only
-// combine shared memory with shared memory and store results.  Every
-// mbarrier wait is bounded; a wait that runs out records error code 2 and
-// the CTA leaves after its copies in flight have landed.  The unaligned head
-// and tail elements of the chunks are folded element by element, in the
-// same ring order, by CTA 0.
+// kStages shared-memory stages with TMA bulk copies (cp.async.bulk, one
+// mbarrier per stage counting the bytes; lane r copies rank r's part), in
+// load steps that run ahead of the rounds and across slice boundaries: step
+// 0 of a slice holds x_r[r] for every r (round 1's incoming messages), step
+// s holds x_r[(r - s) mod R].  Round s writes m_r over x_r[c] in step s's
+// stage, so that stage is round s+1's incoming messages and no other buffer
+// is needed.  The folding warps release a step's stage once the round after
+// it is done (the last step's, once its results are stored) by arriving on
+// the stage's second mbarrier; warp 0 waits on that before refilling it and
+// takes no part in the rounds' barriers, so its copies overlap the folds.
+// Every wait is bounded; a wait that runs out records error code 2, the
+// folding warps tell warp 0 to stop, and the CTA leaves once its copies in
+// flight have landed.  The unaligned head and tail elements of the chunks
+// are folded element by element, in the same ring order, by CTA 0.
 #include "ra_device.cuh"
 
 namespace ra {
 
 namespace {
 
-constexpr int kStages = kLocalStages;
-constexpr int kSliceItems = kLocalSliceItems;        // R * SV <= kSliceItems
-constexpr int kFolders = kLocalThreads - 32;         // warps 1.. fold and store; warp 0 issues copies
+constexpr int kLocalThreads = 512;   // one CTA per SM: warp 0 issues the bulk copies, 15 warps fold
+constexpr int kStages = 6;           // load steps in flight or in use per CTA
+constexpr int kSliceItems = 1920;    // R * SV <= 1920 16-byte vectors per stage (30 KiB)
+constexpr int kFolders = kLocalThreads - 32;
 constexpr int kItems = kSliceItems / kFolders;       // (rank, vector) positions per folding thread
 static_assert(kItems * kFolders == kSliceItems, "slice items must split evenly over the folding threads");
 
@@ -93,7 +95,7 @@ __device__ __forceinline__ int slice_part(const LocalShared& sh, int c, int64_t 
 }  // namespace
 
 template <class D, int OP>
-__global__ void __launch_bounds__(kLocalThreads, 2)
+__global__ void __launch_bounds__(kLocalThreads, 1)
 local_kernel(const LocalArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
