@@ -397,70 +397,51 @@ def run_gpu_arm(args):
 
 
 def run_e2e(torch, ra, h, big_in, big_out, R, n, steps, dist):
-    """Algbw end to end: every step copies its R inputs in from pinned host
-    memory, runs ra_allreduce, and copies all R outputs back.  Two device
-    buffer sets and three streams let step k+1's upload overlap step k's
-    reduction and download (the host link carries both directions at once);
-    every transfer of every step is inside the timed region."""
+    """Algbw end to end through the C entry point for host buffers,
+    ra_allreduce_host: every step hands it the R page-locked host inputs and
+    R page-locked host outputs; the library copies each window of the inputs
+    in, folds it, and copies it out while the next window comes in, and
+    consecutive steps overlap the same way.  Every transfer of every step is
+    inside the timed region."""
     import numpy as np
-    dev_in = [big_in, torch.empty_like(big_in)]
-    dev_out = [big_out, torch.empty_like(big_out)]
-    pin_in = [torch.empty(big_in.shape, dtype=big_in.dtype, pin_memory=True) for _ in range(2)]
-    pin_out = [torch.empty(big_out.shape, dtype=big_out.dtype, pin_memory=True) for _ in range(2)]
-    for p in pin_in:
-        p.copy_(big_in)
-    views_in = [[d[r, :n] for r in range(R)] for d in dev_in]
-    views_out = [[d[r, :n] for r in range(R)] for d in dev_out]
-    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "cmp", "out")}
-
-    def run_steps(count):
-        for k in range(count):
-            b = k % 2
-            if k >= 2:
-                s_in.wait_event(ev["cmp"][b])        # step k-2 has consumed dev_in[b]
-            with torch.cuda.stream(s_in):
-                dev_in[b].copy_(pin_in[b], non_blocking=True)
-            ev["in"][b].record(s_in)
-            s_cmp.wait_event(ev["in"][b])
-            if k >= 2:
-                s_cmp.wait_event(ev["out"][b])       # step k-2's download has read dev_out[b]
-            h.allreduce(views_in[b], views_out[b], s_cmp)
-            ev["cmp"][b].record(s_cmp)
-            s_out.wait_event(ev["cmp"][b])
-            with torch.cuda.stream(s_out):
-                pin_out[b].copy_(dev_out[b], non_blocking=True)
-            ev["out"][b].record(s_out)
-
-    # untimed warm-up steps, copies included: the first transfers into and out of
-    # each pinned buffer are slower than the rest
-    run_steps(4)
+    pin_in = torch.empty(big_in.shape, dtype=big_in.dtype, pin_memory=True)
+    pin_in.copy_(big_in)
+    pin_out = torch.zeros(big_out.shape, dtype=big_out.dtype, pin_memory=True)
+    ins = [pin_in[r, :n] for r in range(R)]
+    outs = [pin_out[r, :n] for r in range(R)]
+    # two streams, alternated: a call waits for everything before it on its
+    # stream, so step k+1's uploads overlap step k's downloads only when the
+    # two are on different streams
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    # untimed warm-up calls, copies included: the first transfers into and out
+    # of each pinned buffer are slower than the rest
+    for k in range(4):
+        h.allreduce_host(ins, outs, streams[k % 2])
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e0.record(s_in)
-    s_cmp.wait_event(e0)
-    s_out.wait_event(e0)
-    run_steps(steps)
-    s_out.wait_stream(s_in)
-    s_out.wait_stream(s_cmp)
-    e1.record(s_out)
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for k in range(steps):
+        h.allreduce_host(ins, outs, streams[k % 2])
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize()
-    te, units = aggregate(e0.elapsed_time(e1) / 1e3 / steps, float(n * big_in.element_size()), dist)
-    last = (steps - 1) % 2
-    if not np.array_equal(pin_out[last][0, :n].numpy().view(np.uint8),
-                          dev_out[last][0, :n].cpu().numpy().view(np.uint8)):
-        raise RuntimeError("e2e read-back differs from the device result")
+    b = big_in.element_size()
+    te, units = aggregate(e0.elapsed_time(e1) / 1e3 / steps, float(n * b), dist)
+    for r in (0, R - 1):
+        if not np.array_equal(pin_out[r, :n].numpy().view(np.uint8), big_out[r, :n].cpu().numpy().view(np.uint8)):
+            raise RuntimeError("e2e read-back differs from the device result")
     return {"value": round(units / te / 1e9, 3), "unit": "GB/s",
-            "h2d_bytes_per_step": big_in.numel() * big_in.element_size(),
-            "d2h_bytes_per_step": big_out.numel() * big_out.element_size(),
+            "h2d_bytes_per_step": R * n * b, "d2h_bytes_per_step": R * n * b,
             "steps": steps, "ms_per_step": round(te * 1e3, 4),
-            "note": "every step: all R inputs copied in from pinned host memory, ra_allreduce, all R "
-                    "outputs copied back; double-buffered so uploads and downloads of neighbouring "
-                    "steps overlap"}
+            "note": "every step: ra_allreduce_host on R page-locked host inputs and R page-locked host "
+                    "outputs (all R inputs copied in, all R outputs copied back by the library, window "
+                    "by window); steps alternate between two streams so that one step's uploads overlap "
+                    "the previous step's downloads"}
 
 
 # ------------------------------------------------------------- CPU oracle

@@ -162,12 +162,16 @@ typedef enum ra_option {
   RA_OPT_BARRIER = 7,        /* ra_barrier of the persistent variant */
   RA_OPT_SLICES = 8,         /* sub-slices per channel slice of the pipelined
                                 variant, 1..64; 0 (default) = about 128 KiB each */
-  RA_OPT_GATHER = 9          /* kernel of the direct AllGather (and of the compact
+  RA_OPT_GATHER = 9,         /* kernel of the direct AllGather (and of the compact
                                 AllGather when chunk starts are 16-byte
                                 aligned): 0 (default) = chosen by the library,
                                 1 = 16-byte vector loads and stores, 2 = TMA
                                 broadcast (each tile loaded once into shared
                                 memory, bulk-stored to every other rank) */
+  RA_OPT_HOST_WINDOWS = 10   /* windows of ra_allreduce_host: 0 (default) =
+                                chosen by the library, 1..8 = that many (fewer
+                                when a window would hold less than one 16-byte
+                                vector per rank) */
 } ra_option;
 
 /* Device error record, filled by the first wait that gives up. */
@@ -222,6 +226,32 @@ ra_status ra_all_gather_compact(ra_handle h, const void* const* in, void* const*
 
 /* Ring AllReduce (sections 4-9): out[r] = S for every r. */
 ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, void* stream);
+
+/* Ring AllReduce (sections 4-9) of R buffers in HOST memory: host_out[r] =
+ * S for every r, computed by the direct kernel on device copies.  host_in and
+ * host_out are R host pointers to n elements each (any alignment; in place,
+ * host_in[r] == host_out[r], allowed; other overlaps are RA_ERR_INVALID, and
+ * device or managed memory is RA_ERR_INVALID -- use ra_allreduce).  Page-
+ * locked memory (cudaHostAlloc, cudaHostRegister) lets the copies run
+ * asynchronously and overlap; pageable memory works, with the CUDA runtime's
+ * synchronous copies.  The handle owns two sets of device copies, used by
+ * alternate calls (4 R n b bytes, allocated on the first call, RA_ERR_OOM if
+ * that fails, freed by ra_destroy).  The elements are processed in up to 8
+ * windows (RA_OPT_HOST_WINDOWS; by default at least 32 MiB per rank each,
+ * boundaries on 2 MiB multiples of the buffers): window j's inputs are copied
+ * in on one internal stream, folded on `stream`, and copied out on another,
+ * so window j+1 comes in while window j is folded and window j-1 goes out (a
+ * window moves in R copies per direction).  A call's copies in start after everything before it on
+ * `stream`, the previous call on that stream included; calls issued on two
+ * streams overlap, the second one's copies in running alongside the first
+ * one's copies out (each set of device copies passes from a call to the call
+ * after next, window by window, in order).
+ * Asynchronous on `stream` like ra_allreduce: work
+ * already on `stream` comes first, later work on `stream` sees host_out
+ * complete; host_in must not change and host_out must not be read before
+ * that.  Not capturable into a CUDA graph (RA_ERR_UNSUPPORTED while `stream`
+ * captures).  RA_OPT_VARIANT does not apply. */
+ra_status ra_allreduce_host(ra_handle h, const void* const* host_in, void* const* host_out, void* stream);
 
 /* Host only, needs no device: the chunk plan of section 12 as read here.
  * off[k], len[k] for k < R (arrays of R entries owned by the caller). */

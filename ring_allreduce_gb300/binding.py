@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
-    "ra_all_gather", "ra_allreduce", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
+    "ra_all_gather", "ra_allreduce", "ra_allreduce_host", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc",
     "ra_last_error",
     "ra_status_string", "RingAllReduce", "PreparedCall", "EXPORTED",
@@ -71,6 +71,7 @@ class Option(enum.IntEnum):
     BARRIER = 7
     SLICES = 8
     GATHER = 9
+    HOST_WINDOWS = 10
 
 
 class DeviceError(ctypes.Structure):
@@ -98,6 +99,7 @@ EXPORTED = {
     "ra_reduce_scatter": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_all_gather": (_ST, [_P, ctypes.POINTER(_P), _P]),
     "ra_allreduce": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
+    "ra_allreduce_host": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_reduce_scatter_compact": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_all_gather_compact": (_ST, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _P]),
     "ra_chunk_plan": (_ST, [ctypes.c_int, _SZ, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
@@ -159,7 +161,9 @@ def _check(status):
 def _addr(x):
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data   # a numpy array (host buffers of ra_allreduce_host)
 
 
 def _ptr_array(bufs):
@@ -190,6 +194,12 @@ def ra_destroy(h):
 
 def ra_allreduce(h, ins, outs, stream=None):
     _check(_lib.ra_allreduce(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
+def ra_allreduce_host(h, ins, outs, stream=None):
+    """ins, outs: R host buffers (CPU torch tensors, numpy arrays or
+    addresses); page-locked ones let the copies overlap."""
+    _check(_lib.ra_allreduce_host(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
 
 
 def ra_reduce_scatter(h, ins, outs, stream=None):
@@ -284,6 +294,8 @@ class RingAllReduce:
         self.R, self.n = int(R), int(n)
         self.dtype = _DTYPES[dtype] if isinstance(dtype, str) else DType(dtype)
         self.op = _OPS[op] if isinstance(op, str) else Op(op)
+        self.itemsize = {DType.F32: 4, DType.BF16: 2, DType.I32: 4, DType.F16: 2, DType.F64: 8,
+                         DType.I64: 8}[self.dtype]
         self.h = ra_create(self.R, self.n, self.dtype, self.op)
         if variant is not None:
             self.set_option(Option.VARIANT, Variant[variant.upper()] if isinstance(variant, str) else variant)
@@ -297,6 +309,20 @@ class RingAllReduce:
     def allreduce(self, ins, outs, stream=None):
         self._ranks(ins, outs)
         ra_allreduce(self.h, ins, outs, stream)
+
+    def allreduce_host(self, ins, outs, stream=None):
+        """AllReduce of R host buffers through the library's device copies
+        (ra_allreduce_host): asynchronous on `stream`."""
+        self._ranks(ins, outs)
+        for b in list(ins) + list(outs):
+            if isinstance(b, int):
+                continue
+            size = b.numel() * b.element_size() if hasattr(b, "numel") else b.nbytes
+            if size < self.n * self.itemsize:
+                raise ValueError(f"host buffer of {size} bytes, need {self.n * self.itemsize}")
+            if hasattr(b, "is_cuda") and b.is_cuda:
+                raise ValueError("allreduce_host takes host buffers; use allreduce for device tensors")
+        ra_allreduce_host(self.h, ins, outs, stream)
 
     def reduce_scatter(self, ins, outs, stream=None):
         self._ranks(ins, outs)

@@ -18,6 +18,9 @@
 // reads chunk k from its owner's buffer and writes it to the other R-1 (to
 // all R when the owner's input is a separate, compact buffer).
 //
+// A launch may cover only a window [lo, hi) of the elements: each chunk's
+// part of it, with the chunk's own fold order.
+//
 // Grid: (CTAs per chunk, R chunks).  By default a thread takes U 16-byte
 // vectors of its chunk (U = 4, 2, 1 for R <= 2, <= 4, more) and the grid has
 // as many CTAs as that needs: many short CTAs that the hardware schedules as
@@ -39,8 +42,9 @@ direct_kernel(const DirectArgs a) {
   constexpr int V = D::kVec;
   const int R = a.R;
   const int k = blockIdx.y;
-  const int64_t off = min((int64_t)k * a.plan.C, a.plan.n);
-  const int64_t end = min(off + a.plan.C, a.plan.n);
+  const int64_t chunk_off = min((int64_t)k * a.plan.C, a.plan.n);
+  const int64_t off = max(chunk_off, a.lo);
+  const int64_t end = min(min(chunk_off + a.plan.C, a.plan.n), a.hi);
   if (off >= end) return;
   const Span<V> sp(off, end);
   const int owner = (k == 0) ? R - 1 : k - 1;   // rank holding S_k after ReduceScatter

@@ -79,6 +79,10 @@ constexpr int kMaxSlices = 64;
 
 }  // namespace
 
+constexpr int kHostWindows = 8;   // ra_allreduce_host pipeline depth
+constexpr size_t kHostWindowBytes = (size_t)32 << 20;   // least bytes per rank and window
+constexpr size_t kHostWindowAlign = (size_t)2 << 20;    // window boundaries, in bytes
+
 struct ra_ctx {
   int R = 0;
   size_t n = 0;
@@ -116,6 +120,17 @@ struct ra_ctx {
   int ring_kind = -1;
   const void* ring_in[ra::kMaxRanks] = {};
   void* ring_out[ra::kMaxRanks] = {};
+  // ra_allreduce_host: two sets of device copies of the R inputs and R
+  // outputs, used by alternate calls (set s: inputs then outputs, rank r at
+  // element r * host_n_pad of each), two copy streams and one event per set,
+  // stage and window; allocated on first use
+  char* host_dev = nullptr;
+  size_t host_n_pad = 0;
+  cudaStream_t host_s_in = nullptr, host_s_out = nullptr;
+  cudaEvent_t host_start = nullptr;
+  cudaEvent_t host_ev[2][3][kHostWindows] = {};   // [set][in, fold, out][window]
+  int host_set = 0;                               // the set the next call uses
+  int host_windows = 0;   // RA_OPT_HOST_WINDOWS
 };
 
 namespace {
@@ -293,6 +308,8 @@ ra_status run_direct(ra_ctx* h, int mode, const void* const* in, void* const* ou
   ra::DirectArgs a;
   a.p = make_ptrs(h, in, out);
   a.plan = make_plan(h->R, h->n);
+  a.lo = 0;
+  a.hi = a.plan.n;
   a.R = h->R;
   a.mode = mode;
   a.write_owner = 0;
@@ -392,6 +409,8 @@ ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* o
       }
     }
     a.plan = pl;
+    a.lo = 0;
+    a.hi = pl.n;
     a.R = R;
     a.mode = mode;
     a.write_owner = 1;
@@ -825,8 +844,156 @@ ra_status ra_destroy(ra_handle h) {
       if (reg.owned && reg.d) cudaFree(reg.d);
   if (h->d_slots) cudaFree(h->d_slots);
   if (h->d_err) cudaFree(h->d_err);
+  if (h->host_dev) cudaFree(h->host_dev);
+  if (h->host_s_in) cudaStreamDestroy(h->host_s_in);
+  if (h->host_s_out) cudaStreamDestroy(h->host_s_out);
+  if (h->host_start) cudaEventDestroy(h->host_start);
+  for (auto& set : h->host_ev)
+    for (auto& row : set)
+      for (auto& ev : row)
+        if (ev) cudaEventDestroy(ev);
   delete h;
   return s;
+}
+
+namespace {
+
+ra_status prepare_host_pipe(ra_ctx* h) {
+  if (h->host_dev) return RA_OK;
+  const size_t b = elem_bytes(h->dtype);
+  const size_t n_pad = (h->n + 63) / 64 * 64;   // every rank's copy starts 128-byte aligned
+  cudaError_t e = cudaMalloc(&h->host_dev, 4 * (size_t)h->R * n_pad * b);
+  if (e != cudaSuccess) {
+    h->host_dev = nullptr;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? fail(RA_ERR_OOM, "staging for host buffers: %zu bytes",
+                                                 4 * (size_t)h->R * n_pad * b)
+                                          : cuda_fail(e, "staging allocation");
+  }
+  h->host_n_pad = n_pad;
+  if (!h->host_s_in) e = cudaStreamCreateWithFlags(&h->host_s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !h->host_s_out) e = cudaStreamCreateWithFlags(&h->host_s_out, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !h->host_start) e = cudaEventCreateWithFlags(&h->host_start, cudaEventDisableTiming);
+  for (auto& set : h->host_ev)
+    for (auto& row : set)
+      for (auto& ev : row)
+        if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "staging streams and events");
+}
+
+// Host buffers only: device (or managed) memory belongs to ra_allreduce.
+ra_status check_host_buffers(ra_ctx* h, const void* const* in, void* const* out) {
+  const size_t bytes = h->n * elem_bytes(h->dtype);
+  for (int r = 0; r < h->R; ++r) {
+    if (!in[r]) return fail(RA_ERR_INVALID, "host_in[%d] is NULL", r);
+    if (!out[r]) return fail(RA_ERR_INVALID, "host_out[%d] is NULL", r);
+    for (int q = 0; q < h->R; ++q) {
+      if (q != r && overlap(out[r], out[q], bytes))
+        return fail(RA_ERR_INVALID, "host_out[%d] overlaps host_out[%d]", r, q);
+      if (in[q] != out[r] && overlap(in[q], out[r], bytes))
+        return fail(RA_ERR_INVALID, "host_in[%d] overlaps host_out[%d]", q, r);
+    }
+    if (h->check_pointers) {
+      for (int side = 0; side < 2; ++side) {
+        const void* p = side ? static_cast<const void*>(out[r]) : in[r];
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+          cudaGetLastError();
+          continue;   // not known to CUDA: pageable host memory
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+          return fail(RA_ERR_INVALID, "%s[%d]=%p is device memory: use ra_allreduce", side ? "host_out" : "host_in",
+                      r, p);
+      }
+    }
+  }
+  return RA_OK;
+}
+
+}  // namespace
+
+ra_status ra_allreduce_host(ra_handle h, const void* const* host_in, void* const* host_out, void* stream) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  if (!host_in || !host_out) return fail(RA_ERR_INVALID, "NULL pointer array");
+  DeviceGuard g(h->device);
+  if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
+  if (h->n == 0) return RA_OK;
+  ra_status s = check_host_buffers(h, host_in, host_out);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "stream query");
+  if (cap != cudaStreamCaptureStatusNone) return fail(RA_ERR_UNSUPPORTED, "ra_allreduce_host cannot be captured");
+  s = prepare_host_pipe(h);
+  if (s != RA_OK) return s;
+
+  const int R = h->R;
+  const size_t b = elem_bytes(h->dtype);
+  const int64_t n = (int64_t)h->n;
+  // windows of whole 16-byte vectors (the last one takes the rest)
+  const int64_t vec = 16 / (int64_t)b;
+  int W = h->host_windows > 0
+              ? h->host_windows
+              : (int)std::min<int64_t>(kHostWindows, std::max<int64_t>(1, (int64_t)(h->n * b / kHostWindowBytes)));
+  // window boundaries on 2 MiB multiples of each buffer (whole 16-byte vectors
+  // when a window is smaller than that)
+  const int64_t align = std::max<int64_t>(vec, (int64_t)(kHostWindowAlign / b));
+  const int64_t want = ceil_div(n, W);
+  const int64_t step = want >= align ? ceil_div(want, align) * align : ceil_div(want, vec) * vec;
+  W = (int)ceil_div(n, step);
+  const int set = h->host_set;
+  char* d_in = h->host_dev + (size_t)(2 * set) * R * h->host_n_pad * b;
+  char* d_out = d_in + (size_t)R * h->host_n_pad * b;
+  const void* dev_in[ra::kMaxRanks];
+  void* dev_out[ra::kMaxRanks];
+  for (int r = 0; r < R; ++r) {
+    dev_in[r] = d_in + (size_t)r * h->host_n_pad * b;
+    dev_out[r] = d_out + (size_t)r * h->host_n_pad * b;
+  }
+  ra::DirectArgs a;
+  a.p = make_ptrs(h, dev_in, dev_out);
+  a.plan = make_plan(R, h->n);
+  a.R = R;
+  a.mode = ra::kModeAllReduce;
+  a.write_owner = 0;
+  const int ctas = direct_ctas_per_chunk(h, a.plan, ra::kModeAllReduce);
+
+  // everything before the call on `stream` happens first
+  e = cudaEventRecord(h->host_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_in, h->host_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_out, h->host_start, 0);
+  for (int j = 0; j < W && e == cudaSuccess; ++j) {
+    const int64_t lo = j * step, hi = std::min(n, lo + step);
+    const size_t off = (size_t)lo * b, len = (size_t)(hi - lo) * b;
+    cudaEvent_t ev_in = h->host_ev[set][0][j], ev_fold = h->host_ev[set][1][j], ev_out = h->host_ev[set][2][j];
+    // window j of this set is free once the call before last has folded it
+    // (inputs) and copied it out (outputs); events never recorded yet are
+    // complete
+    e = cudaStreamWaitEvent(h->host_s_in, ev_fold, 0);
+    for (int r = 0; r < R && e == cudaSuccess; ++r)
+      e = cudaMemcpyAsync(static_cast<char*>(const_cast<void*>(dev_in[r])) + off,
+                          static_cast<const char*>(host_in[r]) + off, len, cudaMemcpyHostToDevice, h->host_s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, h->host_s_in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_out, 0);
+    if (e == cudaSuccess) {
+      a.lo = lo;
+      a.hi = hi;
+      e = ra::launch_direct(h->dtype, h->op, a, ctas, st);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ev_fold, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_out, ev_fold, 0);
+    for (int r = 0; r < R && e == cudaSuccess; ++r)
+      e = cudaMemcpyAsync(static_cast<char*>(host_out[r]) + off, static_cast<char*>(dev_out[r]) + off, len,
+                          cudaMemcpyDeviceToHost, h->host_s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out, h->host_s_out);
+  }
+  // the caller's stream continues once the last window is back on the host
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->host_ev[set][2][W - 1], 0);
+  if (e != cudaSuccess) return cuda_fail(e, "host pipeline");
+  h->host_set = 1 - set;
+  return RA_OK;
 }
 
 ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, void* stream) {
@@ -976,6 +1143,11 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       if (value < 0 || value > 2) return fail(RA_ERR_INVALID, "gather kernel %lld outside [0, 2]", value);
       h->gather = (int)value;
       return RA_OK;
+    case RA_OPT_HOST_WINDOWS:
+      if (value < 0 || value > kHostWindows)
+        return fail(RA_ERR_INVALID, "host windows %lld outside [0, %d]", value, kHostWindows);
+      h->host_windows = (int)value;
+      return RA_OK;
     case RA_OPT_TIMEOUT_NS:
       if (value < 1000) return fail(RA_ERR_INVALID, "timeout %lld ns below 1 us", value);
       h->timeout_ns = value;
@@ -1008,6 +1180,7 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_BARRIER: *value = h->barrier; return RA_OK;
     case RA_OPT_SLICES: *value = h->slices; return RA_OK;
     case RA_OPT_GATHER: *value = h->gather; return RA_OK;
+    case RA_OPT_HOST_WINDOWS: *value = h->host_windows; return RA_OK;
     default: return fail(RA_ERR_INVALID, "unknown option %d", key);
   }
 }

@@ -31,6 +31,7 @@ struct Plan {
 struct DirectArgs {
   Ptrs p;
   Plan plan;
+  int64_t lo, hi;       // only elements [lo, hi) are processed (0, n: all)
   int R;
   int mode;
   int write_owner;      // AllGather: also write the owner's output (compact input)

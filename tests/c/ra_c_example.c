@@ -2,9 +2,9 @@
  * only include/ra.h and the CUDA runtime.  R ranks of n fp32 elements hold
  * x_r[i] = 1000 r + (i mod 997); every output must hold the closed form
  * S[i] = 1000 R(R-1)/2 + R (i mod 997) exactly (small integers: exact in fp32
- * whatever the order).  Runs every variant and the compact forms, checks the
- * chunk plan and the placement of the 4-rank example, and exits non-zero on
- * the first mismatch. */
+ * whatever the order).  Runs every variant, the compact forms and the
+ * host-buffer entry point, checks the chunk plan and the placement of the
+ * 4-rank example, and exits non-zero on the first mismatch. */
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -80,6 +80,28 @@ static int run(int R, size_t n, int variant) {
           return 1;
         }
       CHECK_CUDA(cudaFree(chunk[r]));
+    }
+    /* the same AllReduce from host buffers (plain malloc: pageable) */
+    {
+      float* hin[32];
+      float* hout[32];
+      for (r = 0; r < R; ++r) {
+        hin[r] = (float*)malloc(n * sizeof(float));
+        hout[r] = (float*)malloc(n * sizeof(float));
+        if (!hin[r] || !hout[r]) return 1;
+        for (i = 0; i < n; ++i) hin[r][i] = (float)(1000 * r + (int)(i % 997));
+      }
+      CHECK_RA(ra_allreduce_host(h, (const void* const*)hin, (void* const*)hout, NULL));
+      CHECK_CUDA(cudaStreamSynchronize(NULL));
+      for (r = 0; r < R; ++r) {
+        for (i = 0; i < n; ++i)
+          if (hout[r][i] != (float)(1000 * R * (R - 1) / 2 + R * (int)(i % 997))) {
+            fprintf(stderr, "host buffers R=%d rank %d element %zu wrong\n", R, r, i);
+            return 1;
+          }
+        free(hin[r]);
+        free(hout[r]);
+      }
     }
   }
   CHECK_RA(ra_destroy(h));
