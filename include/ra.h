@@ -41,19 +41,24 @@
  *   - The handle owns only what it allocates: at ra_create the counting
  *     barrier's signal slots, a device error record and a private stream (for
  *     capturing the ring variant's graph); on the first call that needs them,
- *     the per-peer barrier's slots and the pipelined variant's flags.
+ *     the per-peer barrier's slots, the pipelined variant's flags, and for
+ *     ra_allreduce_host its device copies of the buffers, two copy streams
+ *     and their events.
  *
  * Asynchrony and errors
  *   - Every compute call is enqueued on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and returns once enqueued.  Host-side argument
  *     errors return a status and enqueue nothing.
- *   - No device wait is unbounded: the persistent kernel's barrier polls and
- *     the AllGather kernel's copy waits give up after RA_OPT_TIMEOUT_NS, note
- *     what they waited for in the handle's error record and return.  That
- *     record is read by ra_get_device_status.  No kernel traps.
+ *   - No device wait is unbounded: the persistent and pipelined kernels'
+ *     polls and the copy waits of the AllGather round and local kernels give
+ *     up after RA_OPT_TIMEOUT_NS, note what they waited for in the handle's
+ *     error record and return (the cluster barrier is the hardware's own).
+ *     That record is read by ra_get_device_status.  No kernel traps.
  *   - ra_last_error() gives a text for the calling thread's last failure.
- *   - Calls on one handle must be ordered (one stream, or synchronised by the
- *     caller): the persistent variant's signal slots are per handle.
+ *   - A handle is used by one host thread at a time.  Its device calls must
+ *     be ordered (one stream, or synchronised by the caller): the persistent
+ *     variant's signal slots are per handle.  ra_allreduce_host is the
+ *     exception: its calls may alternate between streams (see there).
  *
  * Edge cases: n == 0 is a no-op returning RA_OK (the buffer pointers are not
  * looked at, NULL included).  R == 1 copies in[0] to
@@ -110,10 +115,10 @@ typedef enum ra_variant {
                                  different sub-slices overlap) */
   RA_VARIANT_LOCAL = 5        /* one launch, each CTA running every ring round
                                  for one slice of every chunk: the ranks'
-                                 messages pass through shared memory, rounds
-                                 end at __syncthreads; reads each input once,
-                                 writes each output once, no waits between
-                                 CTAs */
+                                 messages pass through shared memory, the
+                                 operands arrive by TMA bulk copies ahead of
+                                 the rounds; reads each input once, writes
+                                 each output once, no waits between CTAs */
 } ra_variant;
 
 /* Barrier of the persistent variant (RA_OPT_BARRIER). */
