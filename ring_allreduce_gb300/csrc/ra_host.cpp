@@ -130,6 +130,8 @@ struct ra_ctx {
   cudaEvent_t host_start = nullptr;
   cudaEvent_t host_ev[2][3][kHostWindows] = {};   // [set][in, fold, out][window]
   int host_set = 0;                               // the set the next call uses
+  int64_t host_step = 0;                          // window size of the last call (elements)
+  bool host_ready = false;                        // every staging resource exists
   int host_windows = 0;   // RA_OPT_HOST_WINDOWS
 };
 
@@ -859,16 +861,19 @@ ra_status ra_destroy(ra_handle h) {
 namespace {
 
 ra_status prepare_host_pipe(ra_ctx* h) {
-  if (h->host_dev) return RA_OK;
+  if (h->host_ready) return RA_OK;
   const size_t b = elem_bytes(h->dtype);
   const size_t n_pad = (h->n + 63) / 64 * 64;   // every rank's copy starts 128-byte aligned
-  cudaError_t e = cudaMalloc(&h->host_dev, 4 * (size_t)h->R * n_pad * b);
-  if (e != cudaSuccess) {
-    h->host_dev = nullptr;
-    cudaGetLastError();
-    return e == cudaErrorMemoryAllocation ? fail(RA_ERR_OOM, "staging for host buffers: %zu bytes",
-                                                 4 * (size_t)h->R * n_pad * b)
-                                          : cuda_fail(e, "staging allocation");
+  cudaError_t e = cudaSuccess;
+  if (!h->host_dev) {
+    e = cudaMalloc(&h->host_dev, 4 * (size_t)h->R * n_pad * b);
+    if (e != cudaSuccess) {
+      h->host_dev = nullptr;
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? fail(RA_ERR_OOM, "staging for host buffers: %zu bytes",
+                                                   4 * (size_t)h->R * n_pad * b)
+                                            : cuda_fail(e, "staging allocation");
+    }
   }
   h->host_n_pad = n_pad;
   if (!h->host_s_in) e = cudaStreamCreateWithFlags(&h->host_s_in, cudaStreamNonBlocking);
@@ -878,7 +883,9 @@ ra_status prepare_host_pipe(ra_ctx* h) {
     for (auto& row : set)
       for (auto& ev : row)
         if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-  return e == cudaSuccess ? RA_OK : cuda_fail(e, "staging streams and events");
+  if (e != cudaSuccess) return cuda_fail(e, "staging streams and events");
+  h->host_ready = true;
+  return RA_OK;
 }
 
 // Host buffers only: device (or managed) memory belongs to ra_allreduce.
@@ -963,6 +970,16 @@ ra_status ra_allreduce_host(ra_handle h, const void* const* host_in, void* const
   e = cudaEventRecord(h->host_start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_in, h->host_start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_out, h->host_start, 0);
+  // windows of another size than the last call's: the per-window events no
+  // longer cover the same elements, so wait for every earlier use of both sets
+  if (h->host_step != 0 && h->host_step != step)
+    for (auto& set_ev : h->host_ev)
+      for (auto& row : set_ev)
+        for (cudaEvent_t ev : row) {
+          if (e == cudaSuccess) e = cudaStreamWaitEvent(h->host_s_in, ev, 0);
+          if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev, 0);
+        }
+  h->host_step = step;
   for (int j = 0; j < W && e == cudaSuccess; ++j) {
     const int64_t lo = j * step, hi = std::min(n, lo + step);
     const size_t off = (size_t)lo * b, len = (size_t)(hi - lo) * b;

@@ -185,3 +185,24 @@ def test_host_calls_on_two_streams(ra):
     for k in range(4):
         for r in range(R):
             assert_bitwise_equal(_host(outs[k][r], xs[k][r]), wants[k][r], f"call {k} rank {r}")
+
+
+def test_host_window_count_changes_between_calls(ra):
+    """Calls with 2, 8, 3 and 8 windows issued back to back on two streams,
+    no synchronisation between them: a call whose windows differ from the
+    last call's waits for every earlier use of the device copies."""
+    o = elementops.get_op("f32", "sum")
+    R, n = 4, 2**22 + 9
+    xs = [inputs.generate(R, n, "f32", "normal", seed=560 + k) for k in range(4)]
+    wants = [ring.ring_allreduce(x, o) for x in xs]
+    ins = [[_pinned(v) for v in x] for x in xs]
+    outs = [[_pinned(np.zeros_like(v)) for v in x] for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    with ra.RingAllReduce(R, n, "f32", "sum") as h:
+        for k, windows in enumerate((2, 8, 3, 8)):
+            h.set_option(ra.Option.HOST_WINDOWS, windows)
+            h.allreduce_host(ins[k], outs[k], streams[k % 2])
+        torch.cuda.synchronize()
+    for k in range(4):
+        for r in range(R):
+            assert_bitwise_equal(_host(outs[k][r], xs[k][r]), wants[k][r], f"call {k} rank {r}")
