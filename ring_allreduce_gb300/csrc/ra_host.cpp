@@ -252,18 +252,23 @@ int copy_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
   return (int)(c < 1 ? 1 : c);
 }
 
+// Channels of the persistent and pipelined variants when RA_OPT_CTAS is 0:
+// one per 128 vectors of a chunk up to 16 -- a round's latency falls as its
+// slice shrinks (measured at R = 8: 53.6 -> 36.9 us per call at 2^18 fp32 per
+// rank), while tiny chunks gain nothing from more CTAs -- then enough for 4
+// vectors per thread at 512 threads, up to `most` (one wave).
+int64_t default_channels(const ra_ctx* h, const ra::Plan& pl, int64_t most) {
+  const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
+  int64_t G = std::max<int64_t>(std::min<int64_t>(16, ceil_div(vecs, 128)),
+                                ceil_div(vecs, (int64_t)ra::kPersistThreads * 4));
+  if (G > most) G = most;
+  return G < 1 ? 1 : G;
+}
+
 int persistent_channels(const ra_ctx* h, const ra::Plan& pl) {
   const int cap = h->persist_blocks_per_sm * h->num_sms / h->R;
-  int G;
-  if (h->ctas > 0) {
-    G = h->ctas;
-  } else {
-    const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
-    const int64_t need = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
-    G = (int)(need < cap ? need : cap);
-  }
-  if (G < 1) G = 1;
-  return G;
+  const int G = h->ctas > 0 ? h->ctas : (int)default_channels(h, pl, cap);
+  return G < 1 ? 1 : G;
 }
 
 ra::Ptrs make_ptrs(const ra_ctx* h, const void* const* in, void* const* out) {
@@ -596,10 +601,7 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   if (h->ctas > 0) {
     a.G = h->ctas;
   } else {
-    const int64_t vecs = ceil_div(a.plan.C, vec_elems(h->dtype)) + 1;
-    int64_t G = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
-    if (G > clusters) G = clusters;          // one wave of clusters
-    a.G = (int)(G < 1 ? 1 : G);
+    a.G = (int)default_channels(h, a.plan, clusters);   // one wave of clusters
   }
   if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
   a.epoch = 1;
@@ -674,11 +676,7 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   if (h->ctas > 0) {
     a.G = h->ctas;
   } else {
-    const int64_t vecs = ceil_div(a.plan.C, vec_elems(h->dtype)) + 1;
-    const int64_t need = ceil_div(vecs, (int64_t)ra::kPersistThreads * 4);
-    const int64_t most = cap / h->R;
-    a.G = (int)(need < most ? need : most);
-    if (a.G < 1) a.G = 1;
+    a.G = (int)default_channels(h, a.plan, cap / h->R);
   }
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "pipelined grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
