@@ -173,10 +173,16 @@ typedef enum ra_option {
                                 1 = 16-byte vector loads and stores, 2 = TMA
                                 broadcast (each tile loaded once into shared
                                 memory, bulk-stored to every other rank) */
-  RA_OPT_HOST_WINDOWS = 10   /* windows of ra_allreduce_host: 0 (default) =
+  RA_OPT_HOST_WINDOWS = 10,  /* windows of ra_allreduce_host: 0 (default) =
                                 chosen by the library, 1..8 = that many (fewer
                                 when a window would hold less than one 16-byte
                                 vector per rank) */
+  RA_OPT_DEBUG_SHRINK = 11   /* bounds-checked builds only (see
+                                ra_debug_bounds_report): register each of the
+                                call's buffers this many bytes shorter than it
+                                is, so that the accesses to its last bytes are
+                                reported and skipped -- a test of the checks.
+                                RA_ERR_UNSUPPORTED in other builds. */
 } ra_option;
 
 /* Device error record, filled by the first wait that gives up. */
@@ -330,6 +336,18 @@ ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op op, const 
  * successful call every shadow equals its signal.  With dst == NULL only
  * *count is set. */
 ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count);
+
+/* Builds with bounds checks (libra_gb300_debug.so, compiled with
+ * -DRA_DEBUG_BOUNDS) only.  There every global access of every kernel is first
+ * checked against the byte ranges of the call's buffers and of the handle's
+ * device memory; an access outside all of them is counted and skipped (a load
+ * reads zero), so a wrong index shows up here instead of as a memory fault.
+ * This call synchronises the device and returns how many such accesses there
+ * were since the last reset (*count) and the address of the first one
+ * (*first_address, 0 if none); a non-zero `reset` clears both.  Such builds
+ * launch the ring variant directly (no CUDA graphs) and are not capturable.
+ * RA_ERR_UNSUPPORTED in other builds. */
+ra_status ra_debug_bounds_report(unsigned long long* count, unsigned long long* first_address, int reset);
 
 /* Text of the calling thread's last error ("" if none). */
 const char* ra_last_error(void);

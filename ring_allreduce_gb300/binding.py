@@ -18,6 +18,7 @@ __all__ = [
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_allreduce_host", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc",
+    "ra_debug_bounds_report",
     "ra_last_error",
     "ra_status_string", "RingAllReduce", "PreparedCall", "EXPORTED",
 ]
@@ -72,6 +73,7 @@ class Option(enum.IntEnum):
     SLICES = 8
     GATHER = 9
     HOST_WINDOWS = 10
+    DEBUG_SHRINK = 11
 
 
 class DeviceError(ctypes.Structure):
@@ -113,6 +115,8 @@ EXPORTED = {
     "ra_allreduce_noalloc": (_ST, [ctypes.c_int, _SZ, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
                                    ctypes.POINTER(_P), _P]),
     "ra_read_shadows": (_ST, [_P, ctypes.POINTER(ctypes.c_uint64), _SZ, ctypes.POINTER(_SZ)]),
+    "ra_debug_bounds_report": (_ST, [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_ulonglong),
+                                     ctypes.c_int]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -121,6 +125,11 @@ _LIB = None
 
 
 def library_path():
+    """The library to load: the bounds-checked debug build when the
+    environment sets RA_GB300_DEBUG_BOUNDS=1 (build it with
+    build.build(debug=True)), else the release build."""
+    if os.environ.get("RA_GB300_DEBUG_BOUNDS") == "1":
+        return _build.DEBUG_LIB_PATH
     return _build.LIB_PATH
 
 
@@ -194,6 +203,15 @@ def ra_destroy(h):
 
 def ra_allreduce(h, ins, outs, stream=None):
     _check(_lib.ra_allreduce(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)))
+
+
+def ra_debug_bounds_report(reset=True):
+    """Bounds-checked builds only: (accesses outside the registered ranges
+    since the last reset, address of the first); RAError UNSUPPORTED in
+    release builds."""
+    count, first = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    _check(_lib.ra_debug_bounds_report(ctypes.byref(count), ctypes.byref(first), 1 if reset else 0))
+    return count.value, first.value
 
 
 def ra_allreduce_host(h, ins, outs, stream=None):

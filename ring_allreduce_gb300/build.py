@@ -5,6 +5,10 @@ translation unit under ``csrc/`` with nvcc in parallel into ``_build/`` and
 links ``libra_gb300.so`` next to this file.  Nothing is rebuilt when the
 library is newer than every source and header and the flags are unchanged.
 Set RA_PTXAS_VERBOSE=1 to print ptxas register / spill / shared-memory use.
+``build(debug=True)`` builds ``libra_gb300_debug.so`` from the same sources
+with -DRA_DEBUG_BOUNDS (into ``_build_debug/``): every global access of every
+kernel is checked against the byte ranges registered for the call, and
+violations are counted and skipped (``ra_debug_bounds_report``).
 """
 
 import hashlib
@@ -21,6 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libra_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "libra_gb300_debug.so")
 
 SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_pipelined.cu", "ra_compact.cu",
            "ra_bcast.cu", "ra_static.cu", "ra_local.cu"]
@@ -84,22 +90,24 @@ def _stamp(extra):
     return h.hexdigest()
 
 
-def build(force=False, verbose=None, jobs=None):
-    """Compile and link the library; returns its path."""
+def build(force=False, verbose=None, jobs=None, debug=False):
+    """Compile and link the library (the bounds-checked one with debug=True);
+    returns its path."""
     verbose = os.environ.get("RA_PTXAS_VERBOSE") == "1" if verbose is None else verbose
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + (["-DRA_DEBUG_BOUNDS"] if debug else [])
+    build_dir, lib_path = (DEBUG_BUILD_DIR, DEBUG_LIB_PATH) if debug else (BUILD_DIR, LIB_PATH)
     stamp = _stamp(extra)
-    stamp_file = os.path.join(BUILD_DIR, "stamp")
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+    stamp_file = os.path.join(build_dir, "stamp")
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+                return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(unit):
         src, stem, defs = unit
-        obj = os.path.join(BUILD_DIR, stem + ".o")
+        obj = os.path.join(build_dir, stem + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, *[f"-D{k}={v}" for k, v in defs.items()],
                "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -114,17 +122,17 @@ def build(force=False, verbose=None, jobs=None):
     if failed:
         raise RuntimeError("nvcc failed for " + ", ".join(s for s, _ in failed))
     objs = [o for _, o, _ in results]
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         sys.stderr.write(res.stdout + res.stderr)
-        raise RuntimeError("link of libra_gb300.so failed")
-    os.replace(tmp, LIB_PATH)
+        raise RuntimeError(f"link of {os.path.basename(lib_path)} failed")
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

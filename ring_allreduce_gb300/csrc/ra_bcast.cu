@@ -53,8 +53,8 @@ bcast_kernel(const BcastArgs a) {
     for (int j = 0; j < R; ++j) {
       if (j == owner && !a.write_owner) continue;
       uint8_t* dst = static_cast<uint8_t*>(a.dst[j]);
-      for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) dst[i] = src[i];
-      for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) dst[i] = src[i];
+      for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) st_g(dst + i, ld_g(src + i));
+      for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) st_g(dst + i, ld_g(src + i));
     }
   }
   const int64_t body = a1 - a0;
@@ -115,6 +115,8 @@ int bcast_tile_bytes() { return kTile; }
 
 cudaError_t launch_bcast(const BcastArgs& a, int ctas_per_chunk, cudaStream_t st) {
   if (a.R < 1 || a.R > kMaxRanks || ctas_per_chunk < 1) return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   dim3 grid(ctas_per_chunk, a.R);
   bcast_kernel<<<grid, 32, kSmem, st>>>(a);
   return cudaGetLastError();

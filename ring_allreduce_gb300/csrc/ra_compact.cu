@@ -42,9 +42,9 @@ __device__ __forceinline__ uint4 load_at(const T* base, int64_t e) {
   constexpr int V = 16 / sizeof(T);
   const uint4* v = reinterpret_cast<const uint4*>(base) + e / V;
   const int s = (int)(e % V) * (int)sizeof(T);
-  const uint4 A = __ldg(v);
+  const uint4 A = ld_ro(v);
   if (s == 0) return A;
-  return shift_bytes(A, __ldg(v + 1), s);
+  return shift_bytes(A, ld_ro(v + 1), s);
 }
 
 // Whole 16-byte vectors a thread may read starting at element e of a buffer
@@ -82,10 +82,10 @@ compact_kernel(const CompactArgs a) {
     while (nu > 0 && !readable<V>(off + (nu - 1) * V, n)) --nu;
     T* dst = static_cast<T*>(a.p.out[owner]);
     auto fold = [&](int64_t g) {
-      uint4 acc = __ldg(reinterpret_cast<const uint4*>(a.p.in[k]) + g);
+      uint4 acc = ld_ro(reinterpret_cast<const uint4*>(a.p.in[k]) + g);
       for (int j = 1; j < R; ++j) {
         const int q = (k + j >= R) ? k + j - R : k + j;
-        acc = combine_vec<D, OP>(acc, __ldg(reinterpret_cast<const uint4*>(a.p.in[q]) + g));
+        acc = combine_vec<D, OP>(acc, ld_ro(reinterpret_cast<const uint4*>(a.p.in[q]) + g));
       }
       return acc;
     };
@@ -115,7 +115,7 @@ compact_kernel(const CompactArgs a) {
           const int q = (k + j >= R) ? k + j - R : k + j;
           acc = Op<D, OP>::apply(acc, ld_stream_scalar(static_cast<const T*>(a.p.in[q]) + off + c));
         }
-        dst[c] = acc;
+        st_g(dst + c, acc);
       }
     }
   } else {
@@ -139,7 +139,7 @@ compact_kernel(const CompactArgs a) {
       for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
         const int64_t c = t < head_n ? t : tail_b + (t - head_n);
         const T v = ld_stream_scalar(src + c);
-        for (int j = 0; j < R; ++j) static_cast<T*>(a.p.out[j])[off + c] = v;
+        for (int j = 0; j < R; ++j) st_g(static_cast<T*>(a.p.out[j]) + off + c, v);
       }
     }
   }
@@ -148,6 +148,8 @@ compact_kernel(const CompactArgs a) {
 cudaError_t launch_compact(int dtype, int op, const CompactArgs& a, int ctas_per_chunk, cudaStream_t st) {
   if (a.R < 1 || a.R > kMaxRanks || ctas_per_chunk < 1) return cudaErrorInvalidValue;
   if (a.mode != kModeReduceScatter && a.mode != kModeAllGather) return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   dim3 grid(ctas_per_chunk, a.R);
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
     compact_kernel<decltype(d), decltype(o)::value><<<grid, kCompactThreads, 0, st>>>(a);

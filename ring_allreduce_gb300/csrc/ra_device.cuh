@@ -216,35 +216,104 @@ __device__ __forceinline__ uint4 combine_vec(uint4 inc, uint4 loc) {
   return VecOp<D, OP>::apply(inc, loc);
 }
 
+// --------------------------------------------- bounds checks (debug builds)
+// Built with -DRA_DEBUG_BOUNDS, every global access below is first checked
+// against the byte ranges registered for the launch; one outside all of them
+// is counted, the first one noted, and skipped (a load reads zero), so the
+// kernel runs on without touching memory it does not own.  This stands in
+// for a memory checker.  Without the flag the checks are compiled out and
+// every helper is the plain access.
+
+#ifdef RA_DEBUG_BOUNDS
+static __constant__ DebugTable g_debug_ranges;   // one per translation unit
+
+static __device__ __noinline__ bool debug_access_ok(const void* p, unsigned bytes, unsigned kind) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  for (int i = 0; i < g_debug_ranges.count; ++i)
+    if (a >= g_debug_ranges.r[i].lo && a + bytes <= g_debug_ranges.r[i].hi) return true;
+  DebugReport* rep = g_debug_ranges.report;
+  if (rep && atomicAdd(&rep->count, 1ull) == 0ull) {
+    rep->first_addr = a;
+    rep->first_bytes = bytes;
+    rep->first_kind = kind;
+  }
+  return false;
+}
+#define RA_ACCESS_OK(p, bytes, kind) (::ra::debug_access_ok((p), (bytes), (kind)))
+
+// Launch functions call this first: the kernels of this translation unit
+// check against the table the host filled for the call.
+inline cudaError_t debug_upload(cudaStream_t st) {
+  return cudaMemcpyToSymbolAsync(g_debug_ranges, &debug_table(), sizeof(DebugTable), 0, cudaMemcpyHostToDevice,
+                                 st);
+}
+#else
+#define RA_ACCESS_OK(p, bytes, kind) true
+inline cudaError_t debug_upload(cudaStream_t) { return cudaSuccess; }
+#endif
+
+// One element of global memory, plain access.
+template <class T> __device__ __forceinline__ T ld_g(const T* p) {
+  if (!RA_ACCESS_OK(p, sizeof(T), 1u)) return T();
+  return *p;
+}
+template <class T> __device__ __forceinline__ void st_g(T* p, T v) {
+  if (RA_ACCESS_OK(p, sizeof(T), 2u)) *p = v;
+}
+
 // ------------------------------------------------------------ vector I/O
 // Streaming loads/stores for data touched once per launch (evict-first in
 // L2), and L2-only (.cg) accesses for data another CTA of the same launch
 // wrote or will read (the persistent kernel), which must not come from a
 // stale L1 line.
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
-__device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
-__device__ __forceinline__ uint4 ld_l2(const uint4* p) { return __ldcg(p); }
-__device__ __forceinline__ void st_l2(uint4* p, uint4 v) { __stcg(p, v); }
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  if (!RA_ACCESS_OK(p, 16u, 1u)) return make_uint4(0u, 0u, 0u, 0u);
+  return __ldcs(p);
+}
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+  if (RA_ACCESS_OK(p, 16u, 2u)) __stcs(p, v);
+}
+// Read-only data (the non-coherent path): buffers no CTA of the launch writes.
+__device__ __forceinline__ uint4 ld_ro(const uint4* p) {
+  if (!RA_ACCESS_OK(p, 16u, 1u)) return make_uint4(0u, 0u, 0u, 0u);
+  return __ldg(p);
+}
+__device__ __forceinline__ uint4 ld_l2(const uint4* p) {
+  if (!RA_ACCESS_OK(p, 16u, 1u)) return make_uint4(0u, 0u, 0u, 0u);
+  return __ldcg(p);
+}
+__device__ __forceinline__ void st_l2(uint4* p, uint4 v) {
+  if (RA_ACCESS_OK(p, 16u, 2u)) __stcg(p, v);
+}
 
 // One element, read once (evict-first), through the coherent path.
-template <class T> __device__ __forceinline__ T ld_stream_scalar(const T* p) { return __ldcs(p); }
+template <class T> __device__ __forceinline__ T ld_stream_scalar(const T* p) {
+  if (!RA_ACCESS_OK(p, sizeof(T), 1u)) return T();
+  return __ldcs(p);
+}
 template <> __device__ __forceinline__ uint16_t ld_stream_scalar<uint16_t>(const uint16_t* p) {
+  if (!RA_ACCESS_OK(p, 2u, 1u)) return 0;
   return __ldcs(reinterpret_cast<const unsigned short*>(p));
 }
 template <> __device__ __forceinline__ int64_t ld_stream_scalar<int64_t>(const int64_t* p) {
+  if (!RA_ACCESS_OK(p, 8u, 1u)) return 0;
   return (int64_t)__ldcs(reinterpret_cast<const long long*>(p));
 }
 
-template <class T> __device__ __forceinline__ T ld_l2_scalar(const T* p);
-template <> __device__ __forceinline__ float ld_l2_scalar<float>(const float* p) { return __ldcg(p); }
-template <> __device__ __forceinline__ int32_t ld_l2_scalar<int32_t>(const int32_t* p) { return __ldcg(p); }
-template <> __device__ __forceinline__ uint16_t ld_l2_scalar<uint16_t>(const uint16_t* p) {
+template <class T> __device__ __forceinline__ T ld_l2_scalar_raw(const T* p);
+template <> __device__ __forceinline__ float ld_l2_scalar_raw<float>(const float* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ int32_t ld_l2_scalar_raw<int32_t>(const int32_t* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ uint16_t ld_l2_scalar_raw<uint16_t>(const uint16_t* p) {
   return __ldcg(reinterpret_cast<const unsigned short*>(p));
 }
-template <> __device__ __forceinline__ double ld_l2_scalar<double>(const double* p) { return __ldcg(p); }
-template <> __device__ __forceinline__ int64_t ld_l2_scalar<int64_t>(const int64_t* p) {
+template <> __device__ __forceinline__ double ld_l2_scalar_raw<double>(const double* p) { return __ldcg(p); }
+template <> __device__ __forceinline__ int64_t ld_l2_scalar_raw<int64_t>(const int64_t* p) {
   return (int64_t)__ldcg(reinterpret_cast<const long long*>(p));
+}
+template <class T> __device__ __forceinline__ T ld_l2_scalar(const T* p) {
+  if (!RA_ACCESS_OK(p, sizeof(T), 1u)) return T();
+  return ld_l2_scalar_raw(p);
 }
 
 // Split [off, end) (element indices, buffers 16-byte aligned) into a scalar
@@ -300,6 +369,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void signal_add_relaxed(uint64_t* p, uint64_t v) {
+  if (!RA_ACCESS_OK(p, 8u, 2u)) return;
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
@@ -307,22 +377,26 @@ __device__ __forceinline__ void signal_add_relaxed(uint64_t* p, uint64_t v) {
 // the target behind the peers' release, with no separate fence (measured
 // on GB300: 14 % cheaper barrier rounds than relaxed polls plus a fence).
 __device__ __forceinline__ uint64_t signal_load_acquire(const uint64_t* p) {
+  if (!RA_ACCESS_OK(p, 8u, 1u)) return 0;
   uint64_t v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __forceinline__ uint64_t signal_load_relaxed(const uint64_t* p) {
+  if (!RA_ACCESS_OK(p, 8u, 1u)) return 0;
   uint64_t v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __forceinline__ void signal_store_relaxed(uint64_t* p, uint64_t v) {
+  if (!RA_ACCESS_OK(p, 8u, 2u)) return;
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t load_relaxed_u32(const uint32_t* p) {
+  if (!RA_ACCESS_OK(p, 4u, 1u)) return 0;
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
@@ -336,6 +410,7 @@ __device__ __forceinline__ bool rolling_reached(uint64_t observed, uint64_t targ
 // The first wait that gives up fills the error record; later ones leave it.
 __device__ __forceinline__ void record_wait_error(ra_device_error* err, uint32_t code, int round, int rank,
                                                   int channel, int peer, uint64_t observed, uint64_t expected) {
+  if (!RA_ACCESS_OK(err, sizeof(ra_device_error), 2u)) return;
   if (atomicCAS(&err->code, 0u, code) == 0u) {
     err->round = round;
     err->rank = rank;
@@ -394,7 +469,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // global -> shared (this CTA), completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
+// (A debug build that skips a copy leaves its bytes unannounced: the wait on
+// `bar` then runs out, bounded, and reports.)
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  if (!RA_ACCESS_OK(gmem_src, bytes, 3u)) return;
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_addr(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
@@ -403,6 +481,7 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
 
 // shared (this CTA) -> global, tracked by bulk async-groups.
 __device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  if (!RA_ACCESS_OK(gmem_dst, bytes, 4u)) return;
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                ::"l"(gmem_dst), "r"(smem_addr(smem_src)), "r"(bytes)
                : "memory");

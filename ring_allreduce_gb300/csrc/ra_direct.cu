@@ -7,6 +7,8 @@ namespace ra {
 // AllGather moves bits only: one instantiation per element width.
 template <class D>
 static cudaError_t launch_direct_ag(const DirectArgs& a, dim3 grid, cudaStream_t st) {
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   if (a.R <= 8)
     direct_kernel<D, kOpSum, 8, kModeAllGather, kGatherUnroll><<<grid, kDirectThreads, 0, st>>>(a);
   else

@@ -109,16 +109,16 @@ direct_kernel(const DirectArgs a) {
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
       if (MODE == kModeAllGather) {
-        const T s = static_cast<const T*>(a.p.in[owner])[i];
+        const T s = ld_g(static_cast<const T*>(a.p.in[owner]) + i);
         for (int j = 0; j < R; ++j)
-          if (j != owner || a.write_owner) static_cast<T*>(a.p.out[j])[i] = s;
+          if (j != owner || a.write_owner) st_g(static_cast<T*>(a.p.out[j]) + i, s);
       } else {
-        T acc = static_cast<const T*>(a.p.in[src_rank(0)])[i];
-        for (int j = 1; j < R; ++j) acc = Op<D, OP>::apply(acc, static_cast<const T*>(a.p.in[src_rank(j)])[i]);
+        T acc = ld_g(static_cast<const T*>(a.p.in[src_rank(0)]) + i);
+        for (int j = 1; j < R; ++j) acc = Op<D, OP>::apply(acc, ld_g(static_cast<const T*>(a.p.in[src_rank(j)]) + i));
         if (MODE == kModeAllReduce) {
-          for (int j = 0; j < R; ++j) static_cast<T*>(a.p.out[j])[i] = acc;
+          for (int j = 0; j < R; ++j) st_g(static_cast<T*>(a.p.out[j]) + i, acc);
         } else {
-          static_cast<T*>(a.p.out[owner])[i] = acc;
+          st_g(static_cast<T*>(a.p.out[owner]) + i, acc);
         }
       }
     }

@@ -12,6 +12,8 @@ namespace ra {
 template <>
 cudaError_t launch_direct_dt<RA_INST_DTYPE>(int op, const DirectArgs& a, dim3 grid, cudaStream_t st) {
   using D = typename DTypeOf<RA_INST_DTYPE>::type;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   if (op == RA_SUM) return launch_direct_d<D, kOpSum>(a, grid, st);
   if (op == RA_MAX) return launch_direct_d<D, kOpMax>(a, grid, st);
   return cudaErrorInvalidValue;

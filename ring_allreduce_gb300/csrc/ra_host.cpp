@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -133,9 +134,37 @@ struct ra_ctx {
   int64_t host_step = 0;                          // window size of the last call (elements)
   bool host_ready = false;                        // every staging resource exists
   int host_windows = 0;   // RA_OPT_HOST_WINDOWS
+  long long debug_shrink = 0;   // RA_OPT_DEBUG_SHRINK (debug builds)
 };
 
+#ifdef RA_DEBUG_BOUNDS
+namespace ra {
+
+DebugTable& debug_table() {
+  static thread_local DebugTable t;
+  return t;
+}
+
+DebugReport* debug_report() {
+  static DebugReport* rep = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!rep) {
+    if (cudaMalloc(&rep, sizeof(DebugReport)) != cudaSuccess || cudaMemset(rep, 0, sizeof(*rep)) != cudaSuccess) {
+      cudaGetLastError();
+      rep = nullptr;
+    }
+  }
+  return rep;
+}
+
+}  // namespace ra
+#endif
+
 namespace {
+
+void debug_add(const void* p, size_t bytes);   // bounds checks of debug builds, below
+
 
 bool valid_dtype(int d) { return d >= RA_F32 && d <= RA_I64; }
 bool valid_op(int o) { return o == RA_SUM || o == RA_MAX; }
@@ -539,6 +568,9 @@ size_t region_entries(const ra_ctx* h, int sync, int rounds, int G, int J) {
   return (size_t)G * R * (size_t)J;
 }
 
+// Words of a region: its signals, and as many shadows after them when it has any.
+size_t region_words(const SlotRegion& reg) { return reg.shadows ? 2 * reg.cap : reg.cap; }
+
 // The slot array of (sync, kind), allocated on first use for the per-peer
 // barrier and the pipelined flags (the counting slots come with ra_create).
 ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
@@ -559,13 +591,69 @@ ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
     reg.owned = true;
     reg.G = 0;
     reg.calls = 0;
+    debug_add(reg.d, region_words(reg) * sizeof(uint64_t));
   }
   *out = &reg;
   return RA_OK;
 }
 
 // Zero a region when the launch shape it was counted with changes.
-size_t region_words(const SlotRegion& reg) { return reg.shadows ? 2 * reg.cap : reg.cap; }
+
+// ---------------------------------------------------------------- bounds checks
+// Debug builds (-DRA_DEBUG_BOUNDS): the byte ranges one call may touch, put in
+// this host thread's table (ra::debug_table()) before its launches -- the
+// call's buffers and every piece of the handle's device memory; memory the
+// call allocates on the way is added when it is allocated.  Release builds:
+// nothing.
+#ifdef RA_DEBUG_BOUNDS
+using ra::debug_report;
+
+void debug_add(const void* p, size_t bytes) {
+  ra::DebugTable& t = ra::debug_table();
+  if (!p || bytes == 0 || t.count >= ra::kDebugRanges) return;
+  t.r[t.count].lo = reinterpret_cast<uint64_t>(p);
+  t.r[t.count].hi = reinterpret_cast<uint64_t>(p) + bytes;
+  ++t.count;
+}
+
+void debug_begin(const ra_ctx* h) {
+  ra::DebugTable& t = ra::debug_table();
+  t.count = 0;
+  t.report = debug_report();
+  if (!h) return;
+  for (auto& row : h->region)
+    for (auto& reg : row)
+      if (reg.d) debug_add(reg.d, region_words(reg) * sizeof(uint64_t));
+  debug_add(h->d_err, sizeof(ra_device_error));
+  if (h->host_dev) debug_add(h->host_dev, 4 * (size_t)h->R * h->host_n_pad * elem_bytes(h->dtype));
+}
+
+// one of the call's own buffers, RA_OPT_DEBUG_SHRINK bytes shorter than it
+// is (a test of the checks: the accesses to its last bytes are then reported
+// and skipped)
+void debug_user(const ra_ctx* h, const void* p, size_t bytes) {
+  const size_t cut = (size_t)std::max<long long>(0, h->debug_shrink);
+  debug_add(p, bytes > cut ? bytes - cut : 0);
+}
+#else
+void debug_add(const void*, size_t) {}
+void debug_begin(const ra_ctx*) {}
+void debug_user(const ra_ctx*, const void*, size_t) {}
+#endif
+
+void debug_buffers(const ra_ctx* h, const void* const* p, size_t bytes) {
+  for (int r = 0; r < h->R; ++r) debug_user(h, p[r], bytes);
+}
+
+// Compact calls: the full side n elements per rank, the compact side rank r's
+// chunk (r+1) mod R only.
+void debug_compact(const ra_ctx* h, const void* const* full, const void* const* compact) {
+  size_t off[ra::kMaxRanks], len[ra::kMaxRanks];
+  ra_chunk_plan(h->R, h->n, off, len);
+  const size_t b = elem_bytes(h->dtype);
+  debug_buffers(h, full, h->n * b);
+  for (int r = 0; r < h->R; ++r) debug_user(h, compact[r], len[(r + 1) % h->R] * b);
+}
 
 ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   if (reg.G != G || reg.J != J) {
@@ -785,6 +873,9 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   h->device = dev;
   h->num_sms = sms;
   h->persist_blocks_per_sm = coop ? bps : 0;
+#ifdef RA_DEBUG_BOUNDS
+  h->use_graphs = 0;   // the bounds table is uploaded before every launch
+#endif
   h->pipe_blocks_per_sm = coop ? pbps : 0;
   h->local_blocks_per_sm = lbps;
 
@@ -882,6 +973,7 @@ ra_status prepare_host_pipe(ra_ctx* h) {
       for (auto& ev : row)
         if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_fail(e, "staging streams and events");
+  debug_add(h->host_dev, 4 * (size_t)h->R * n_pad * b);
   h->host_ready = true;
   return RA_OK;
 }
@@ -930,6 +1022,7 @@ ra_status ra_allreduce_host(ra_handle h, const void* const* host_in, void* const
   cudaError_t e = cudaStreamIsCapturing(st, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "stream query");
   if (cap != cudaStreamCaptureStatusNone) return fail(RA_ERR_UNSUPPORTED, "ra_allreduce_host cannot be captured");
+  debug_begin(h);
   s = prepare_host_pipe(h);
   if (s != RA_OK) return s;
 
@@ -1018,6 +1111,9 @@ ra_status ra_allreduce(ra_handle h, const void* const* in, void* const* out, voi
   if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
   ra_status s = check_buffers(h, in, out);
   if (s != RA_OK) return s;
+  debug_begin(h);
+  debug_buffers(h, in, h->n * elem_bytes(h->dtype));
+  debug_buffers(h, out, h->n * elem_bytes(h->dtype));
   if (h->n == 0) return RA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->R == 1) {
@@ -1045,6 +1141,9 @@ ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out
   if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
   ra_status s = check_buffers(h, in, out);
   if (s != RA_OK) return s;
+  debug_begin(h);
+  debug_buffers(h, in, h->n * elem_bytes(h->dtype));
+  debug_buffers(h, out, h->n * elem_bytes(h->dtype));
   if (h->n == 0) return RA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->R == 1) {
@@ -1072,6 +1171,8 @@ ra_status ra_all_gather(ra_handle h, void* const* buf, void* stream) {
   if (!g.ok) return fail(RA_ERR_CUDA, "cannot switch to device %d", h->device);
   ra_status s = check_buffers(h, nullptr, buf);
   if (s != RA_OK) return s;
+  debug_begin(h);
+  debug_buffers(h, buf, h->n * elem_bytes(h->dtype));
   if (h->n == 0 || h->R == 1) return RA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (h->variant) {
@@ -1096,6 +1197,8 @@ ra_status ra_reduce_scatter_compact(ra_handle h, const void* const* in, void* co
   if (h->n == 0) return RA_OK;
   ra_status s = check_compact(h, in, out, true);
   if (s != RA_OK) return s;
+  debug_begin(h);
+  debug_compact(h, in, out);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->R == 1) return run_direct(h, ra::kModeAllReduce, in, out, st);
   return run_compact(h, ra::kModeReduceScatter, in, out, st);
@@ -1109,6 +1212,8 @@ ra_status ra_all_gather_compact(ra_handle h, const void* const* in, void* const*
   if (h->n == 0) return RA_OK;
   ra_status s = check_compact(h, out, in, false);
   if (s != RA_OK) return s;
+  debug_begin(h);
+  debug_compact(h, out, in);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->R == 1) return run_direct(h, ra::kModeAllReduce, in, out, st);
   return run_compact(h, ra::kModeAllGather, in, out, st);
@@ -1135,8 +1240,19 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
   }
   switch (key) {
     case RA_OPT_GRAPHS:
+#ifdef RA_DEBUG_BOUNDS
+      if (value != 0) return fail(RA_ERR_UNSUPPORTED, "bounds-checked builds launch the ring variant directly");
+#endif
       h->use_graphs = value != 0;
       return RA_OK;
+    case RA_OPT_DEBUG_SHRINK:
+#ifdef RA_DEBUG_BOUNDS
+      if (value < 0) return fail(RA_ERR_INVALID, "shrink %lld below 0", value);
+      h->debug_shrink = value;
+      return RA_OK;
+#else
+      return fail(RA_ERR_UNSUPPORTED, "built without bounds checks");
+#endif
     case RA_OPT_VARIANT:
       if (value < RA_VARIANT_AUTO || value > RA_VARIANT_LOCAL)
         return fail(RA_ERR_INVALID, "unknown variant %lld", value);
@@ -1196,8 +1312,30 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_SLICES: *value = h->slices; return RA_OK;
     case RA_OPT_GATHER: *value = h->gather; return RA_OK;
     case RA_OPT_HOST_WINDOWS: *value = h->host_windows; return RA_OK;
+    case RA_OPT_DEBUG_SHRINK: *value = h->debug_shrink; return RA_OK;
     default: return fail(RA_ERR_INVALID, "unknown option %d", key);
   }
+}
+
+ra_status ra_debug_bounds_report(unsigned long long* count, unsigned long long* first_address, int reset) {
+#ifdef RA_DEBUG_BOUNDS
+  if (!count || !first_address) return fail(RA_ERR_INVALID, "NULL output pointer");
+  ra::DebugReport* rep = debug_report();
+  if (!rep) return fail(RA_ERR_CUDA, "no bounds report on this device");
+  cudaError_t e = cudaDeviceSynchronize();
+  ra::DebugReport host;
+  if (e == cudaSuccess) e = cudaMemcpy(&host, rep, sizeof(host), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && reset) e = cudaMemset(rep, 0, sizeof(*rep));
+  if (e != cudaSuccess) return cuda_fail(e, "bounds report");
+  *count = host.count;
+  *first_address = host.count ? host.first_addr : 0;
+  return RA_OK;
+#else
+  (void)count;
+  (void)first_address;
+  (void)reset;
+  return fail(RA_ERR_UNSUPPORTED, "built without bounds checks (build with debug=True)");
+#endif
 }
 
 ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) {

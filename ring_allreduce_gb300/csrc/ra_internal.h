@@ -12,6 +12,31 @@ namespace ra {
 
 constexpr int kMaxRanks = 32;
 
+// Bounds checks of debug builds (-DRA_DEBUG_BOUNDS): the byte ranges a
+// launch may touch -- the call's buffers and the handle's device memory --
+// and where violations are counted.  The host fills the table before every
+// launch (debug_table(), per host thread); each kernel translation unit
+// uploads it to its own constant copy in its launch functions.
+struct DebugRange {
+  uint64_t lo, hi;     // [lo, hi)
+};
+struct DebugReport {
+  unsigned long long count;        // accesses outside every range (skipped)
+  unsigned long long first_addr;   // the first one
+  unsigned int first_bytes;
+  unsigned int first_kind;         // 1 load, 2 store, 3 bulk copy source, 4 bulk copy destination
+};
+constexpr int kDebugRanges = 96;
+struct DebugTable {
+  int count;
+  DebugReport* report;
+  DebugRange r[kDebugRanges];
+};
+#ifdef RA_DEBUG_BOUNDS
+DebugTable& debug_table();     // ra_host.cpp: this host thread's table
+DebugReport* debug_report();   // ra_host.cpp: the process's report (device memory)
+#endif
+
 // Which collective a launch carries out.
 enum Mode : int { kModeAllReduce = 0, kModeReduceScatter = 1, kModeAllGather = 2 };
 

@@ -321,19 +321,19 @@ local_kernel(const LocalArgs a) {
         const int64_t i = sp.scalar_at(e);
         T acc;
         if (!reduce) {
-          acc = static_cast<const T*>(a.p.in[owner])[i];
+          acc = ld_g(static_cast<const T*>(a.p.in[owner]) + i);
         } else {
-          acc = static_cast<const T*>(a.p.in[k])[i];
+          acc = ld_g(static_cast<const T*>(a.p.in[k]) + i);
           for (int jr = 1; jr < R; ++jr) {
             const int q = (k + jr >= R) ? k + jr - R : k + jr;
-            acc = Op<D, OP>::apply(acc, static_cast<const T*>(a.p.in[q])[i]);
+            acc = Op<D, OP>::apply(acc, ld_g(static_cast<const T*>(a.p.in[q]) + i));
           }
         }
         if (a.mode == kModeReduceScatter) {
-          static_cast<T*>(a.p.out[owner])[i] = acc;
+          st_g(static_cast<T*>(a.p.out[owner]) + i, acc);
         } else {
           for (int jr = 0; jr < R; ++jr)
-            if (a.mode == kModeAllReduce || jr != owner) static_cast<T*>(a.p.out[jr])[i] = acc;
+            if (a.mode == kModeAllReduce || jr != owner) st_g(static_cast<T*>(a.p.out[jr]) + i, acc);
         }
       }
     }
@@ -375,6 +375,8 @@ cudaError_t local_blocks_per_sm(int dtype, int op, int R, int* blocks) {
 cudaError_t launch_local(int dtype, int op, const LocalArgs& a, int ctas, cudaStream_t st) {
   if (a.R < 2 || a.R > kMaxRanks || a.SV < 1 || a.SV > local_slice_vectors(a.R) || ctas < 1 || a.slices < 1)
     return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
     const size_t smem = (size_t)kStages * a.R * a.SV * sizeof(uint4);
     local_kernel<decltype(d), decltype(o)::value><<<ctas, kLocalThreads, smem, st>>>(a);

@@ -150,7 +150,7 @@ __device__ __forceinline__ void reduce_slice(const typename D::T* inc, const typ
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
-      dst[i] = Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i));
+      st_g(dst + i, Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i)));
     }
   }
 }
@@ -168,7 +168,7 @@ __device__ __forceinline__ void copy_slice(const typename D::T* src, typename D:
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
-      dst[i] = ld_l2_scalar(src + i);
+      st_g(dst + i, ld_l2_scalar(src + i));
     }
   }
 }
@@ -273,6 +273,8 @@ cudaError_t persistent_cluster_capacity(int dtype, int op, int R, int threads, i
 cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = persistent_select(dtype, op);
   if (!fn || a.R < 2 || a.R > 16 || a.G < 1 || a.rounds < 1 || a.sync != kSyncCluster) return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(a, threads, st, attr);
   void* args[] = {const_cast<PersistArgs*>(&a)};
@@ -282,6 +284,8 @@ cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, i
 cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = persistent_select(dtype, op);
   if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PersistArgs*>(&a)};
   return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
 }

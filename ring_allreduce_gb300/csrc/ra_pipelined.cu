@@ -82,7 +82,7 @@ __device__ __forceinline__ void reduce_range(const typename D::T* inc, const typ
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
-      dst[i] = Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i));
+      st_g(dst + i, Op<D, OP>::apply(ld_l2_scalar(inc + i), ld_l2_scalar(loc + i)));
     }
   }
 }
@@ -96,7 +96,7 @@ __device__ __forceinline__ void copy_range(const typename D::T* src, typename D:
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
-      dst[i] = ld_l2_scalar(src + i);
+      st_g(dst + i, ld_l2_scalar(src + i));
     }
   }
 }
@@ -177,6 +177,8 @@ cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks)
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = pipelined_select(dtype, op);
   if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PersistArgs*>(&a)};
   return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
 }

@@ -55,7 +55,7 @@ rs_round_kernel(const RoundArgs a) {
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
-      dst[i] = Op<D, OP>::apply(inc[i], loc[i]);
+      st_g(dst + i, Op<D, OP>::apply(ld_g(inc + i), ld_g(loc + i)));
     }
   }
 }
@@ -65,6 +65,8 @@ rs_round_kernel(const RoundArgs a) {
 // in griddep_wait().
 template <class K, class A>
 static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const A& args) {
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -124,8 +126,8 @@ ag_round_kernel(const CopyArgs a) {
   int64_t a1 = b1 & ~int64_t(15);
   if (a0 >= a1) { a0 = b1; a1 = b1; }
   if (blockIdx.x == 0) {
-    for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) dst[i] = src[i];
-    for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) dst[i] = src[i];
+    for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) st_g(dst + i, ld_g(src + i));
+    for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) st_g(dst + i, ld_g(src + i));
   }
   const int64_t body = a1 - a0;
   const int64_t ntiles = (body + kTileBytes - 1) / kTileBytes;

@@ -49,11 +49,13 @@ __device__ __forceinline__ void reset(uint64_t* sig) { signal_store_relaxed(sig,
 
 // Shadows belong to one waiter (one thread of one CTA), so plain L2 accesses
 // do; they persist across launches.
-__device__ __forceinline__ uint64_t shadow(const uint64_t* sh) { return __ldcg(reinterpret_cast<const unsigned long long*>(sh)); }
+__device__ __forceinline__ uint64_t shadow(const uint64_t* sh) {
+  return (uint64_t)ld_l2_scalar(reinterpret_cast<const int64_t*>(sh));
+}
 
 __device__ __forceinline__ uint64_t increase_shadow(uint64_t* sh, uint64_t delta) {
   const uint64_t v = shadow(sh) + delta;
-  __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
+  if (RA_ACCESS_OK(sh, 8u, 2u)) __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
   return v;
 }
 

@@ -144,6 +144,21 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   a.err = reinterpret_cast<ra_device_error*>(scratch);
   a.skip_rank = -1;
   a.skip_round = -1;
+#ifdef RA_DEBUG_BOUNDS
+  {   // bounds-checked builds: the call's buffers and the part of the scratch it uses
+    DebugTable& t = debug_table();
+    t.count = 0;
+    t.report = debug_report();
+    auto add = [&](const void* p, size_t bytes) {
+      if (t.count < kDebugRanges) t.r[t.count++] = {(uint64_t)p, (uint64_t)p + bytes};
+    };
+    for (int r = 0; r < R; ++r) {
+      add(in[r], n * esize);
+      add(out[r], n * esize);
+    }
+    add(scratch, used);
+  }
+#endif
   e = launch_persistent(dtype, op, a, kPersistThreads, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
