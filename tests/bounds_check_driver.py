@@ -3,7 +3,10 @@ library (RA_GB300_DEBUG_BOUNDS=1 must be set before the binding is imported),
 drives every entry point, variant, barrier and AllGather kernel over small
 ragged shapes, checks the results against the oracle, and prints one JSON
 line: the checks' report after the clean calls, and after a call whose
-buffers were registered 16 bytes short (the checks must see that one)."""
+buffers were registered 16 bytes short (the checks must see that one).  It
+also runs the bounded waits of the kernels fed by TMA bulk copies to their
+limit: a copy the checks skip never arrives, so the wait on it runs out and
+reports (error code 2), and the next call on the handle is correct again."""
 
 import json
 import os
@@ -148,7 +151,45 @@ def main():
         torch.cuda.synchronize()
     ends = [v.data_ptr() + n * 4 for v in inp.views + out.views]
     shrunk_count, shrunk_first = ra.ra_debug_bounds_report(reset=True)
+
+    # bounded waits run out: the local kernel (AllReduce) and the ring
+    # variant's AllGather rounds wait on bulk copies that the checks skip
+    timeouts = {}
+    for variant, kind in (("local", "allreduce"), ("ring", "all_gather")):
+        R, n = 8, 8 * 4096
+        x = inputs.generate(R, n, "f32", "normal", seed=7)
+        o = elementops.get_op("f32", "sum")
+        with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
+            h.set_option(ra.Option.TIMEOUT_NS, 50_000_000)
+            h.set_option(ra.Option.DEBUG_SHRINK, 16)
+            bufs = DeviceRanks(R, n, np.float32, host=x)
+            outs = DeviceRanks(R, n, np.float32)
+            if kind == "allreduce":
+                h.allreduce(bufs.views, outs.views)
+            else:
+                h.all_gather(bufs.views)
+            status, err = h.device_status()
+            first = {"status": status.name, "code": int(err.code)}
+            # the handle is usable again, with the checks back to the full buffers
+            h.set_option(ra.Option.DEBUG_SHRINK, 0)
+            bufs = DeviceRanks(R, n, np.float32, host=x)
+            outs = DeviceRanks(R, n, np.float32)
+            if kind == "allreduce":
+                h.allreduce(bufs.views, outs.views)
+                want = ring.ring_allreduce(x, o)
+            else:
+                h.all_gather(bufs.views)
+                want = ring.ring_all_gather(x, o)
+            status2, _ = h.device_status()
+            torch.cuda.synchronize()
+            got = outs.host() if kind == "allreduce" else bufs.host()
+            first["after"] = status2.name
+            first["after_equal"] = all(np.array_equal(got[r].view(np.uint32), want[r].view(np.uint32))
+                                       for r in range(R))
+        timeouts[variant] = first
+    ra.ra_debug_bounds_report(reset=True)
     print(json.dumps({
+        "timeouts": timeouts,
         "calls": calls,
         "mismatches": mismatches[:10],
         "clean": {"count": clean_count, "first": clean_first},

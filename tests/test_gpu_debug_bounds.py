@@ -5,7 +5,10 @@ memory, and an access outside them is counted and skipped instead of
 faulting.  A child process drives every entry point, variant, barrier and
 AllGather kernel through it; there must be no such access, every result must
 be the oracle's, and a call whose buffers are registered 16 bytes short must
-be caught, at an address in one of the cut tails."""
+be caught, at an address in one of the cut tails.  With buffers registered
+short, the bulk copies the checks skip never arrive: the local kernel's and
+the TMA AllGather round's bounded waits then run out, report RA_ERR_TIMEOUT
+with code 2, and the handle's next call is correct."""
 
 import json
 import os
@@ -33,3 +36,6 @@ def test_bounds_checked_build_sees_no_stray_access():
     assert out["clean"]["count"] == 0, out["clean"]
     assert out["shrunk"]["count"] > 0, out["shrunk"]
     assert out["shrunk"]["first_in_a_cut_tail"], out["shrunk"]
+    for variant, t in out["timeouts"].items():
+        assert t["status"] == "ERR_TIMEOUT" and t["code"] == 2, (variant, t)
+        assert t["after"] == "OK" and t["after_equal"], (variant, t)
