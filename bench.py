@@ -435,13 +435,46 @@ def run_e2e(torch, ra, h, big_in, big_out, R, n, steps, dist):
     for r in (0, R - 1):
         if not np.array_equal(pin_out[r, :n].numpy().view(np.uint8), big_out[r, :n].cpu().numpy().view(np.uint8)):
             raise RuntimeError("e2e read-back differs from the device result")
+    floor_s = link_floor(torch, pin_in, pin_out, big_in, big_out, steps)
     return {"value": round(units / te / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": R * n * b, "d2h_bytes_per_step": R * n * b,
             "steps": steps, "ms_per_step": round(te * 1e3, 4),
+            "link_floor_ms": round(floor_s * 1e3, 4),
+            "frac_of_link_floor": round(floor_s / te, 4),
             "note": "every step: ra_allreduce_host on R page-locked host inputs and R page-locked host "
                     "outputs (all R inputs copied in, all R outputs copied back by the library, window "
                     "by window); steps alternate between two streams so that one step's uploads overlap "
-                    "the previous step's downloads"}
+                    "the previous step's downloads. link_floor_ms: the same bytes as bare copies in the "
+                    "same run, all uploads on one stream and all downloads on another, one copy per "
+                    "direction and step (no fold): the host link's own time for a step"}
+
+
+def link_floor(torch, pin_in, pin_out, dev_in, dev_out, steps):
+    """Seconds per step of the host link alone: one upload of all R input
+    rows and one download of all R output rows per step, uploads and
+    downloads on two streams so they run at once."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    scratch = torch.empty_like(dev_in)
+    for _ in range(2):
+        with torch.cuda.stream(up):
+            scratch.copy_(pin_in, non_blocking=True)
+        with torch.cuda.stream(down):
+            pin_out.copy_(dev_out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(up)
+    down.wait_event(e0)
+    for _ in range(steps):
+        with torch.cuda.stream(up):
+            scratch.copy_(pin_in, non_blocking=True)
+        with torch.cuda.stream(down):
+            pin_out.copy_(dev_out, non_blocking=True)
+    up.wait_stream(down)
+    e1.record(up)
+    torch.cuda.synchronize()
+    del scratch
+    return e0.elapsed_time(e1) / 1e3 / steps
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -675,8 +708,26 @@ def run_sweep(args):
             line[name] = {"us": round(t * 1e6, 2), "algbw": round(n * 4 / t / 1e9, 2),
                        "busbw": round(n * 4 / t / 1e9 * 2 * (R - 1) / R, 2),
                        "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
+        # reference, not a variant: a plain device copy (torch) of the same
+        # R n b bytes read and written, timed the same way -- what a copy
+        # reaches at this size
+        src, dst = ins[0].new_empty(R * n), outs[0].new_empty(R * n)
+        src.copy_(torch.cat(ins))
+        steps = 200 if n <= 2**20 else 30
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for _ in range(10):
+            dst.copy_(src)
+        torch.cuda.synchronize()
+        for a, bb in ev:
+            a.record()
+            dst.copy_(src)
+            bb.record()
+        torch.cuda.synchronize()
+        t = statistics.median([a.elapsed_time(bb) for a, bb in ev]) / 1e3
+        line["copy_same_bytes"] = {"us": round(t * 1e6, 2),
+                                   "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
         print(json.dumps(line), flush=True)
-        del ins, outs
+        del ins, outs, src, dst
         torch.cuda.empty_cache()
 
 

@@ -43,24 +43,31 @@
 
 namespace ra {
 
+// Signal row of one (channel, round): R slots, one per waiting rank.
+__device__ __forceinline__ int64_t counting_row(const PersistArgs& a, int g, int t) {
+  return ((int64_t)g * (a.rounds - 1) + t) * a.R;
+}
+
 // One counting-barrier round, on the signal layer (ra_signal.cuh): each
 // peer adds 1 to the waiter's signal of this (channel, round); the waiter
 // moves its shadow forward by R-1 and waits for the signal to meet it.
-// Returns false when this CTA must stop.
-__device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
+// `shadow_read` is thread 0's value of its shadow for this round, read when
+// the round began (sig::shadow_ahead), so that read is off the barrier's
+// path.  Returns false when this CTA must stop.
+__device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, uint64_t shadow_read,
+                                                 int* s_abort) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int64_t row = ((int64_t)g * (a.rounds - 1) + t) * a.R;
+    const int64_t row = counting_row(a, g, t);
     uint64_t* sigs = a.slots + row;
     fence_acq_rel_gpu();   // release: this round's stores of the whole CTA
     if (!(r == a.skip_rank && t == a.skip_round)) {
       for (int q = 0; q < a.R; ++q)
         if (q != r) sig::add(sigs + q, 1);
     }
-    const uint64_t target = sig::increase_shadow(a.shadows + row + r, (uint64_t)(a.R - 1));
+    const uint64_t target = sig::increase_shadow_from(a.shadows + row + r, shadow_read, (uint64_t)(a.R - 1));
     uint64_t seen = 0;
-    const sig::Wait w = sig::wait(sigs + r, target, 64, a.timeout_ns,
-                                  [&] { return load_relaxed_u32(&a.err->code) != 0u; }, &seen);
+    const sig::Wait w = sig::wait(sigs + r, target, 64, a.timeout_ns, &a.err->code, &seen);
     // one counting slot cannot say which peer is late: peer = -1
     if (w == sig::kTimedOut) record_wait_error(a.err, 1u, t, r, g, -1, seen, target);
     *s_abort = w != sig::kReached;
@@ -96,6 +103,8 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
     for (uint64_t it = 0;; ++it) {
       bool ok = true;
       uint64_t v = 0;
+      // lane 0's load of the error code is in flight with the slot loads
+      const uint32_t code = lane == 0 ? load_relaxed_u32(&a.err->code) : 0u;
       if (active) {
         v = signal_load_acquire(mine + lane);   // acquire, by the lane that observes the slot
         ok = rolling_reached(v, a.epoch);
@@ -104,7 +113,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
       if (missing == 0u) break;
       int stop = 0;
       if (lane == 0) {
-        if (load_relaxed_u32(&a.err->code) != 0u)
+        if (code != 0u)
           stop = 1;
         else if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters)
           stop = 2;
@@ -183,6 +192,11 @@ persistent_kernel(const PersistArgs a) {
   const int g = blockIdx.x / R;
   const int p = (r == 0) ? R - 1 : r - 1;
   for (int t = 0; t < a.rounds; ++t) {
+    // the counting barrier's waiter reads its shadow now; the value is used
+    // after the round's data work
+    uint64_t shadow_read = 0;
+    if (a.sync == kSyncCounting && threadIdx.x == 0 && t + 1 < a.rounds)
+      shadow_read = sig::shadow_ahead(a.shadows + counting_row(a, g, t) + r);
     bool reduce;
     int s;
     if (a.mode == kModeAllGather) {
@@ -214,7 +228,7 @@ persistent_kernel(const PersistArgs a) {
         continue;
       }
       const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
-                                              : counting_barrier(a, g, t, r, &s_abort);
+                                              : counting_barrier(a, g, t, r, shadow_read, &s_abort);
       if (!go) return;
     }
   }

@@ -42,9 +42,10 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
       const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
       for (uint64_t it = 0;; ++it) {
         if (it > 16) __nanosleep(64);
+        const uint32_t code = load_relaxed_u32(&a.err->code);   // in flight with the flag's load
         seen = signal_load_acquire(flag);
         if (rolling_reached(seen, target)) break;
-        if (load_relaxed_u32(&a.err->code) != 0u) {
+        if (code != 0u) {
           abort = 1;
           break;
         }

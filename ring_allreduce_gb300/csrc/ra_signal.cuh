@@ -17,8 +17,10 @@
 // Release is the caller's: one fence.acq_rel.gpu before a batch of adds
 // publishes everything the CTA wrote before it (the counting barrier issues
 // R-1 adds after one fence); the waits poll with acquire loads.  Every wait is bounded: it gives up after
-// `timeout_ns` (global timer) or an iteration limit, or when `abort()` says
-// another waiter has already given up.
+// `timeout_ns` (global timer) or an iteration limit, or when a stop word
+// (the error record's code) says another waiter has already given up.  Each
+// poll issues the stop word's load before the signal's, so both are in
+// flight together: one L2 round trip per poll, not two.
 #pragma once
 
 #include "ra_device.cuh"
@@ -59,21 +61,34 @@ __device__ __forceinline__ uint64_t increase_shadow(uint64_t* sh, uint64_t delta
   return v;
 }
 
+// The same in two steps, for a waiter that knows early which shadow it will
+// move: `shadow_ahead` issues the read (an ordered load, so the compiler
+// keeps it where it is written and its latency overlaps whatever comes
+// next); `increase_shadow_from` stores the moved value and returns it.
+__device__ __forceinline__ uint64_t shadow_ahead(const uint64_t* sh) { return signal_load_relaxed(sh); }
+
+__device__ __forceinline__ uint64_t increase_shadow_from(uint64_t* sh, uint64_t read, uint64_t delta) {
+  const uint64_t v = read + delta;
+  if (RA_ACCESS_OK(sh, 8u, 2u)) __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
+  return v;
+}
+
 // Wait until the signal reaches `least` (rolling, low `bits` bits), polling
 // with acquire loads: on kReached the load that saw it ordered what follows;
-// *seen holds the last value read.
-template <class Abort>
+// *seen holds the last value read.  Gives up (kAborted) once *stop is
+// nonzero, or (kTimedOut) after timeout_ns.
 __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bits, int64_t timeout_ns,
-                                     Abort&& abort, uint64_t* seen) {
+                                     const uint32_t* stop, uint64_t* seen) {
   uint64_t v = signal_load_acquire(sig);
   if (!reached(v, least, bits)) {
     const uint64_t t0 = globaltimer_ns();
     const uint64_t max_iters = (uint64_t)timeout_ns + 1000000ull;   // every poll costs far more than 1 ns
     for (uint64_t it = 0;; ++it) {
       if (it > 32) __nanosleep(100);
+      const uint32_t code = load_relaxed_u32(stop);   // in flight with the next load
       v = signal_load_acquire(sig);
       if (reached(v, least, bits)) break;
-      if (abort()) {
+      if (code != 0u) {
         *seen = v;
         return kAborted;
       }
@@ -87,10 +102,9 @@ __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bi
   return kReached;
 }
 
-template <class Abort>
 __device__ __forceinline__ Wait wait_meet_shadow(const uint64_t* sig, const uint64_t* sh, int64_t timeout_ns,
-                                                 Abort&& abort, uint64_t* seen) {
-  return wait(sig, shadow(sh), 64, timeout_ns, abort, seen);
+                                                 const uint32_t* stop, uint64_t* seen) {
+  return wait(sig, shadow(sh), 64, timeout_ns, stop, seen);
 }
 
 }  // namespace sig
