@@ -20,6 +20,13 @@ r16_i32    16   2^24       i32    uniform integers in [-2^20, 2^20]            s
 sweep       8   2^10..2^26 f32    N(0, 1), generator re-seeded for each size   sum   4
 sweep_R   2..32 2^24       f32    N(0, 1)                                      sum   4
 =========  ===  =========  =====  ==========================================  ====  ====
+
+The ``special`` distribution (floating-point dtypes, edge-case tests only) mixes
+IEEE special values into the draws: signed zeros, the smallest and largest
+subnormals, the smallest normal, +-1 and 1 + ulp, half an ulp of 1 and a quarter
+(so that sums hit rounding ties), half the largest finite value and the largest
+finite value (so that sums overflow), infinities and a quiet NaN, and values of
+random sign and significand spread over the whole exponent range.
 """
 
 import numpy as np
@@ -63,7 +70,59 @@ def _to_f16(v32):
     return t.to(torch.float16).numpy().copy()
 
 
+# significand bits (hidden bit included) and exponent range of the float
+# formats, for the ``special`` draws
+_FLOAT_FORMAT = {"f32": (24, -126, 127), "bf16": (8, -126, 127), "f16": (11, -14, 15), "f64": (53, -1022, 1023)}
+
+
+def _special_bits16(rng, n):
+    """bf16 bit patterns of the ``special`` distribution."""
+    table = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080,
+                      0x3F80, 0xBF80, 0x3F81, 0xBF81, 0x3B80, 0xBB80, 0x3B00, 0x3B00 | 0x8000,
+                      0x7F7F, 0xFF7F, 0x7EFF, 0xFEFF], dtype=np.uint16)
+    kind = rng.random(n)
+    pick = table[rng.integers(0, len(table), size=n)]
+    p, emin, emax = _FLOAT_FORMAT["bf16"]
+    wide = np.ldexp(rng.uniform(1.0, 2.0, size=n) * rng.choice([-1.0, 1.0], size=n),
+                    rng.integers(emin, emax, endpoint=True, size=n)).astype(np.float32)
+    spread = _to_bf16_bits(wide)
+    out = np.where(kind < 0.45, spread, pick)
+    out = np.where((kind >= 0.90) & (kind < 0.94), np.uint16(0x7F80), out)
+    out = np.where((kind >= 0.94) & (kind < 0.98), np.uint16(0xFF80), out)
+    out = np.where(kind >= 0.98, np.uint16(0x7FC0), out)
+    return out.astype(np.uint16)
+
+
+def _special_float(rng, n, dtype):
+    """f32 / f16 / f64 values of the ``special`` distribution."""
+    ft = {"f32": np.float32, "f16": np.float16, "f64": np.float64}[dtype]
+    fi = np.finfo(ft)
+    p, emin, emax = _FLOAT_FORMAT[dtype]
+    sub_max = ft(fi.smallest_normal) - ft(fi.smallest_subnormal)
+    one = ft(1.0)
+    table = np.array([0.0, -0.0, fi.smallest_subnormal, -fi.smallest_subnormal, sub_max, -sub_max,
+                      fi.smallest_normal, -fi.smallest_normal, 1.0, -1.0, one + fi.eps, -(one + fi.eps),
+                      np.ldexp(1.0, -p), -np.ldexp(1.0, -p), np.ldexp(1.0, -p - 1), -np.ldexp(1.0, -p - 1),
+                      fi.max, -fi.max, ft(fi.max) / ft(2), -(ft(fi.max) / ft(2))], dtype=ft)
+    kind = rng.random(n)
+    pick = table[rng.integers(0, len(table), size=n)]
+    with np.errstate(over="ignore"):
+        spread = np.ldexp(rng.uniform(1.0, 2.0, size=n) * rng.choice([-1.0, 1.0], size=n),
+                          rng.integers(emin, emax, endpoint=True, size=n)).astype(ft)
+    out = np.where(kind < 0.45, spread, pick)
+    out = np.where((kind >= 0.90) & (kind < 0.94), ft(np.inf), out)
+    out = np.where((kind >= 0.94) & (kind < 0.98), ft(-np.inf), out)
+    out = np.where(kind >= 0.98, ft(np.nan), out)
+    return out.astype(ft)
+
+
 def _draw(rng, n, dist, dtype):
+    if dist == "special":
+        if dtype == "bf16":
+            return _special_bits16(rng, n)
+        if dtype in ("f32", "f16", "f64"):
+            return _special_float(rng, n, dtype)
+        raise ValueError("the special distribution is for floating-point dtypes")
     if dist == "int8":
         v = rng.integers(-8, 8, endpoint=True, size=n).astype(np.float64)
     elif dist == "normal":
@@ -101,7 +160,7 @@ def _draw(rng, n, dist, dtype):
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
-DISTS = ("int8", "normal", "grad", "int20", "int40", "uniform")
+DISTS = ("int8", "normal", "grad", "int20", "int40", "uniform", "special")
 
 
 def generate(R, n, dtype, dist, seed):

@@ -405,3 +405,100 @@ def test_closed_form_int64(R):
     y = [np.arange(n, dtype=np.int64) + np.int64(10**12 * r) for r in range(R)]
     t = ring.ring_allreduce(y, elementops.get_op("i64", "sum"))
     assert all((v == 10**12 * R * (R - 1) // 2 + R * np.arange(n)).all() for v in t)
+
+
+# IEEE 754 facts for one addition a + b, written as bit patterns by hand:
+# (a, b, a + b).  Ties go to the even neighbour, the overflow threshold is the
+# largest finite value plus half its ulp, subnormals are exact, -0 + -0 = -0,
+# +0 + -0 = +0, inf - inf is NaN (any NaN).
+_NAN = None
+_IEEE_SUMS = {
+    "f32": [
+        (0x7F800000, 0xFF800000, _NAN),          # inf + -inf
+        (0x7F7FFFFF, 0x7F7FFFFF, 0x7F800000),    # max + max overflows
+        (0xFF7FFFFF, 0xFF7FFFFF, 0xFF800000),
+        (0x7F7FFFFF, 0x73000000, 0x7F800000),    # max + 2^103 (half its ulp): tie, odd max -> inf
+        (0x7F7FFFFF, 0x72FFFFFF, 0x7F7FFFFF),    # just below the threshold stays max
+        (0x80000000, 0x80000000, 0x80000000),    # -0 + -0
+        (0x00000000, 0x80000000, 0x00000000),    # +0 + -0
+        (0x80000000, 0x00000000, 0x00000000),
+        (0x00000001, 0x00000001, 0x00000002),    # subnormals add exactly
+        (0x00800000, 0x80000001, 0x007FFFFF),    # smallest normal - smallest subnormal
+        (0x3F800000, 0x33800000, 0x3F800000),    # 1 + 2^-24: tie to even -> 1
+        (0x3F800001, 0x33800000, 0x3F800002),    # (1 + 2^-23) + 2^-24: tie to even -> up
+        (0x7FC00000, 0x3F800000, _NAN),          # NaN + 1
+        (0x7F800000, 0x3F800000, 0x7F800000),    # inf + 1
+    ],
+    "bf16": [
+        (0x7F80, 0xFF80, _NAN),
+        (0x7F7F, 0x7F7F, 0x7F80),
+        (0xFF7F, 0xFF7F, 0xFF80),
+        (0x8000, 0x8000, 0x8000),
+        (0x0000, 0x8000, 0x0000),
+        (0x0001, 0x0001, 0x0002),
+        (0x0080, 0x8001, 0x007F),
+        (0x3F80, 0x3B80, 0x3F80),                # 1 + 2^-8: tie to even -> 1
+        (0x3F81, 0x3B80, 0x3F82),                # (1 + 2^-7) + 2^-8: tie to even -> up
+        (0x3F80, 0x3B81, 0x3F81),                # just above the tie rounds up
+        (0x7FC0, 0x3F80, _NAN),
+        (0x7F80, 0x3F80, 0x7F80),
+    ],
+    "f16": [
+        (0x7C00, 0xFC00, _NAN),
+        (0x7BFF, 0x7BFF, 0x7C00),
+        (0x7BFF, 0x4C00, 0x7C00),                # 65504 + 16 = 65520: tie, odd max -> inf
+        (0x7BFF, 0x4BFF, 0x7BFF),                # 65504 + 15.99: stays 65504
+        (0x8000, 0x8000, 0x8000),
+        (0x0000, 0x8000, 0x0000),
+        (0x0001, 0x0001, 0x0002),
+        (0x0400, 0x8001, 0x03FF),
+        (0x3C00, 0x1000, 0x3C00),                # 1 + 2^-11: tie to even -> 1
+        (0x3C01, 0x1000, 0x3C02),
+        (0x7E00, 0x3C00, _NAN),
+        (0x7C00, 0x3C00, 0x7C00),
+    ],
+    "f64": [
+        (0x7FF0000000000000, 0xFFF0000000000000, _NAN),
+        (0x7FEFFFFFFFFFFFFF, 0x7FEFFFFFFFFFFFFF, 0x7FF0000000000000),
+        (0x8000000000000000, 0x8000000000000000, 0x8000000000000000),
+        (0x0000000000000000, 0x8000000000000000, 0x0000000000000000),
+        (0x0000000000000001, 0x0000000000000001, 0x0000000000000002),
+        (0x0010000000000000, 0x8000000000000001, 0x000FFFFFFFFFFFFF),
+        (0x3FF0000000000000, 0x3CA0000000000000, 0x3FF0000000000000),   # 1 + 2^-53
+        (0x3FF0000000000001, 0x3CA0000000000000, 0x3FF0000000000002),
+        (0x7FF8000000000000, 0x3FF0000000000000, _NAN),
+        (0x7FF0000000000000, 0x3FF0000000000000, 0x7FF0000000000000),
+    ],
+}
+_BITS = {"f32": (np.uint32, np.float32), "bf16": (np.uint16, np.uint16), "f16": (np.uint16, np.float16),
+         "f64": (np.uint64, np.float64)}
+
+
+def _bits_is_nan(dtype, bits):
+    u = int(bits)
+    if dtype == "f32":
+        return (u & 0x7FFFFFFF) > 0x7F800000
+    if dtype == "bf16":
+        return (u & 0x7FFF) > 0x7F80
+    if dtype == "f16":
+        return (u & 0x7FFF) > 0x7C00
+    return (u & 0x7FFFFFFFFFFFFFFF) > 0x7FF0000000000000
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "f64"])
+def test_ieee_special_sums(dtype):
+    """Each case as a two-rank ring over one element (chunk 0 holds it and
+    starts at rank 0, so S = x_0 (+) x_1 with x_0 incoming): the oracle's
+    result is the IEEE result written above, in every rank's output."""
+    ubits, store = _BITS[dtype]
+    op = elementops.get_op(dtype, "sum")
+    for a, b, want in _IEEE_SUMS[dtype]:
+        x = [np.array([a], dtype=ubits).view(store), np.array([b], dtype=ubits).view(store)]
+        with np.errstate(all="ignore"):
+            out = ring.ring_allreduce(x, op)
+        for r in range(2):
+            got = out[r].view(ubits)[0]
+            if want is _NAN:
+                assert _bits_is_nan(dtype, got), (dtype, hex(a), hex(b), hex(int(got)))
+            else:
+                assert int(got) == want, (dtype, hex(a), hex(b), hex(int(got)), hex(want))
