@@ -166,7 +166,8 @@ typedef enum ra_option {
                                 ra_set_option drops the cached graph. */
   RA_OPT_BARRIER = 7,        /* ra_barrier of the persistent variant */
   RA_OPT_SLICES = 8,         /* sub-slices per channel slice of the pipelined
-                                variant, 1..64; 0 (default) = about 128 KiB each */
+                                variant, 1..64; 0 (default) = one per 36 KiB
+                                of the slice, at most 8 */
   RA_OPT_GATHER = 9,         /* kernel of the direct AllGather (and of the compact
                                 AllGather when chunk starts are 16-byte
                                 aligned): 0 (default) = chosen by the library,
@@ -177,6 +178,15 @@ typedef enum ra_option {
                                 chosen by the library, 1..8 = that many (fewer
                                 when a window would hold less than one 16-byte
                                 vector per rank) */
+  RA_OPT_WINDOW = 12,        /* sub-slices per window of the pipelined
+                                variant: each rank runs every ring round on a
+                                window of this many sub-slices before it
+                                starts the next window, so a round's partials
+                                are read back soon after they are written.
+                                0 (default) = 1 (every round on one sub-slice
+                                before the next); values at or above the
+                                sub-slice count mean all of them (every round
+                                over the whole slice) */
   RA_OPT_DEBUG_SHRINK = 11   /* bounds-checked builds only (see
                                 ra_debug_bounds_report): register each of the
                                 call's buffers this many bytes shorter than it

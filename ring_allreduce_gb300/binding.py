@@ -74,6 +74,7 @@ class Option(enum.IntEnum):
     GATHER = 9
     HOST_WINDOWS = 10
     DEBUG_SHRINK = 11
+    WINDOW = 12
 
 
 class DeviceError(ctypes.Structure):

@@ -136,6 +136,7 @@ struct PersistArgs {
   int R;
   int G;
   int J;                // sub-slices per channel slice (pipelined variant)
+  int W;                // sub-slices per window: every round runs on a window before the next (pipelined)
   int mode;
   int sync;             // Sync
   int rounds;           // ring rounds this call runs

@@ -103,8 +103,6 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
     for (uint64_t it = 0;; ++it) {
       bool ok = true;
       uint64_t v = 0;
-      // lane 0's load of the error code is in flight with the slot loads
-      const uint32_t code = lane == 0 ? load_relaxed_u32(&a.err->code) : 0u;
       if (active) {
         v = signal_load_acquire(mine + lane);   // acquire, by the lane that observes the slot
         ok = rolling_reached(v, a.epoch);
@@ -113,7 +111,8 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
       if (missing == 0u) break;
       int stop = 0;
       if (lane == 0) {
-        if (code != 0u)
+        // the error record's stop word, on every 8th poll (read by every waiter)
+        if ((it & 7u) == 7u && load_relaxed_u32(&a.err->code) != 0u)
           stop = 1;
         else if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters)
           stop = 2;

@@ -12,6 +12,16 @@
 // Different sub-slices of one rank can be in different rounds, so rounds
 // overlap along the ring, as NCCL pipelines a ring by slices.
 //
+// Order of the work: the sub-slices are taken W at a time (a window), and a
+// rank runs every round on a window before it starts the next one.  The
+// partial a rank writes for its successor in round t is then read a window's
+// round later instead of a whole slice's round later -- while it is still in
+// L2 -- and the place it is later overwritten with the complete value is
+// written again within 2(R-1) window rounds.  Within a window, the wait for
+// one sub-slice overlaps the work on the others.  W = J is the round-by-round
+// order.  The order changes nothing in the protocol below: every wait is on
+// one sub-slice and one round, whatever was done before it.
+//
 // Why waiting on the predecessor alone is safe.  A rank's output buffer is
 // the "message" its successor reads, and one place of it is written twice:
 // chunk (r - t) holds the partial of ReduceScatter round t and, R rounds
@@ -42,10 +52,10 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
       const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
       for (uint64_t it = 0;; ++it) {
         if (it > 16) __nanosleep(64);
-        const uint32_t code = load_relaxed_u32(&a.err->code);   // in flight with the flag's load
         seen = signal_load_acquire(flag);
         if (rolling_reached(seen, target)) break;
-        if (code != 0u) {
+        // the error record's stop word, on every 8th poll (read by every waiter)
+        if ((it & 7u) == 7u && load_relaxed_u32(&a.err->code) != 0u) {
           abort = 1;
           break;
         }
@@ -115,47 +125,50 @@ pipelined_kernel(const PersistArgs a) {
   uint64_t* mine = a.slots + ((int64_t)g * R + r) * J;
   const uint64_t* pred = a.slots + ((int64_t)g * R + p) * J;
   const uint64_t base = (a.epoch - 1) * (uint64_t)a.rounds;
-  for (int t = 0; t < a.rounds; ++t) {
-    bool reduce;
-    int s;
-    if (a.mode == kModeAllGather) {
-      reduce = false;
-      s = t + 1;
-    } else if (t < R - 1) {
-      reduce = true;
-      s = t + 1;
-    } else {
-      reduce = false;
-      s = t - (R - 1) + 1;
-    }
-    int c = reduce ? (r - s) : (r + 1 - s);
-    c %= R;
-    if (c < 0) c += R;
-    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
-    const int64_t end = min(off + a.plan.C, a.plan.n);
-    const Span<V> sp(off, end);
-    int64_t pb, pe;
-    split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
-    // failure injection: a flag counts finished rounds, so a rank that is
-    // to fall silent withholds every publication from that round on
-    const bool withhold = (r == a.skip_rank && t >= a.skip_round);
-    for (int j = 0; j < J; ++j) {
-      int64_t qb, qe;
-      split_vectors(pb, pe, j, J, &qb, &qe);
-      // round 0 reads inputs only; every later round reads what the
-      // predecessor wrote in its previous round on this sub-slice
-      if (t > 0 && !wait_flag(a, pred + j, base + t, t, r, g, p, &s_abort)) return;
-      const bool scalars = (g == 0 && j == 0);
-      if (off < end) {
-        if (reduce) {
-          const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
-          reduce_range<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), qb, qe, sp,
-                              scalars);
-        } else {
-          copy_range<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), qb, qe, sp, scalars);
-        }
+  for (int w0 = 0; w0 < J; w0 += a.W) {
+    const int w1 = min(J, w0 + a.W);
+    for (int t = 0; t < a.rounds; ++t) {
+      bool reduce;
+      int s;
+      if (a.mode == kModeAllGather) {
+        reduce = false;
+        s = t + 1;
+      } else if (t < R - 1) {
+        reduce = true;
+        s = t + 1;
+      } else {
+        reduce = false;
+        s = t - (R - 1) + 1;
       }
-      publish_flag(mine + j, base + t + 1, withhold);
+      int c = reduce ? (r - s) : (r + 1 - s);
+      c %= R;
+      if (c < 0) c += R;
+      const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
+      const int64_t end = min(off + a.plan.C, a.plan.n);
+      const Span<V> sp(off, end);
+      int64_t pb, pe;
+      split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
+      // failure injection: a flag counts finished rounds, so a rank that is
+      // to fall silent withholds every publication from that round on
+      const bool withhold = (r == a.skip_rank && t >= a.skip_round);
+      for (int j = w0; j < w1; ++j) {
+        int64_t qb, qe;
+        split_vectors(pb, pe, j, J, &qb, &qe);
+        // round 0 reads inputs only; every later round reads what the
+        // predecessor wrote in its previous round on this sub-slice
+        if (t > 0 && !wait_flag(a, pred + j, base + t, t, r, g, p, &s_abort)) return;
+        const bool scalars = (g == 0 && j == 0);
+        if (off < end) {
+          if (reduce) {
+            const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
+            reduce_range<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), qb, qe, sp,
+                                scalars);
+          } else {
+            copy_range<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), qb, qe, sp, scalars);
+          }
+        }
+        publish_flag(mine + j, base + t + 1, withhold);
+      }
     }
   }
 }
@@ -177,7 +190,8 @@ cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks)
 
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = pipelined_select(dtype, op);
-  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.W < 1 || a.rounds < 1)
+    return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PersistArgs*>(&a)};

@@ -361,15 +361,20 @@ def test_per_peer_barrier_matches_oracle(ra, dtype, op):
             assert_bitwise_equal(got[r], want[r], f"per-peer {dtype}/{op} R={R} n={n} rank {r}")
 
 
-@pytest.mark.parametrize("slices", [1, 2, 7, 64])
-def test_pipelined_sub_slices(ra, slices):
+@pytest.mark.parametrize("slices,window", [(0, 0), (1, 0), (2, 0), (7, 0), (64, 0), (7, 3), (5, 2), (64, 64),
+                                           (8, 64)])
+def test_pipelined_sub_slices(ra, slices, window):
+    """Sub-slice counts and windows (every round over a window of sub-slices
+    before the next window; a last window shorter than the others; one window
+    over all of them, the round-by-round order)."""
     o = elementops.get_op("bf16", "sum")
-    for R, n in ((8, 2**20 + 7), (3, 100003), (16, 2**16 + 3)):
-        x = inputs.generate(R, n, "bf16", "grad", seed=slices)
+    for R, n in ((8, 2**20 + 7), (3, 100003), (16, 2**16 + 3), (4, 2**22 + 5)):
+        x = inputs.generate(R, n, "bf16", "grad", seed=slices + 100 * window)
         want = ring.ring_allreduce(x, o)
-        got = run_gpu(ra, x, "bf16", "sum", "pipelined", options=[(ra.Option.SLICES, slices)])
+        got = run_gpu(ra, x, "bf16", "sum", "pipelined",
+                      options=[(ra.Option.SLICES, slices), (ra.Option.WINDOW, window)], repeat=2)
         for r in range(R):
-            assert_bitwise_equal(got[r], want[r], f"slices={slices} R={R}")
+            assert_bitwise_equal(got[r], want[r], f"slices={slices} window={window} R={R}")
 
 
 @pytest.mark.parametrize("R,G", [(2, 1), (5, 3), (8, 4)])
