@@ -106,7 +106,9 @@ typedef enum ra_variant {
   RA_VARIANT_PERSISTENT = 3,  /* one cooperative launch running every round;
                                  simulated ranks meet at a barrier between
                                  rounds (RA_OPT_BARRIER: counting, the
-                                 default, or per-peer) */
+                                 default, per-peer or cluster); at large n
+                                 each channel's slice goes through the rounds
+                                 in passes (RA_OPT_SLICES) */
   RA_VARIANT_PIPELINED = 4,   /* one cooperative launch running every round
                                  with no barrier: a rank starts a round on a
                                  sub-slice as soon as its predecessor has
@@ -166,8 +168,13 @@ typedef enum ra_option {
                                 ra_set_option drops the cached graph. */
   RA_OPT_BARRIER = 7,        /* ra_barrier of the persistent variant */
   RA_OPT_SLICES = 8,         /* sub-slices per channel slice of the pipelined
-                                variant, 1..64; 0 (default) = one per 36 KiB
-                                of the slice, at most 8 */
+                                variant, 1..64, and passes of the persistent
+                                variant with the counting or cluster barrier
+                                (each pass takes one sub-slice through every
+                                round), at most 8 there; 0 (default) = the
+                                fewest that keep n * b / J within 32 MiB, at
+                                most 8 (1 up to 32 MiB per rank).  The
+                                per-peer barrier always runs one pass. */
   RA_OPT_GATHER = 9,         /* kernel of the direct AllGather (and of the compact
                                 AllGather when chunk starts are 16-byte
                                 aligned): 0 (default) = chosen by the library,
@@ -295,9 +302,11 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
  * entries).  With dst == NULL only the sizes are returned.  *count gets the
  * entries, *channels the channel count G, *calls how many calls of that kind
  * and scheme ran since the array was last zeroed, *rounds:
- *   counting barrier  [G][rounds][R] (rounds = barrier rounds); every entry
- *                     equals calls * (R - 1), as does every shadow
- *                     (ra_read_shadows)
+ *   counting barrier  [G][rounds][R] (rounds = barrier rounds of a call:
+ *                     passes x (2R-3) for AllReduce, passes x (R-2) for
+ *                     ReduceScatter or AllGather, passes ordered before the
+ *                     rounds of a pass); every entry equals calls * (R - 1),
+ *                     as does every shadow (ra_read_shadows)
  *   per-peer barrier  [G][rounds][R waiters][R peers]; every entry equals
  *                     calls, except waiter == peer, which stays 0
  *   pipelined flags   [G][R][J] (rounds = ring rounds, J = count / (G R));

@@ -77,6 +77,7 @@ struct SlotRegion {
 
 enum Kind { kKindAllReduce = 0, kKindReduceScatter = 1, kKindAllGather = 2 };
 constexpr int kMaxSlices = 64;
+constexpr int kMaxPasses = 8;   // passes of the persistent variant (counting or cluster barrier)
 
 }  // namespace
 
@@ -561,10 +562,12 @@ int gmax_channels(const ra_ctx* h, int blocks_per_sm) {
   return (blocks_per_sm > 0 ? blocks_per_sm : 1) * h->num_sms / h->R + 1;
 }
 
+// Entries of a slot array: counting [G][J passes][barrier rounds][R];
+// per-peer [G][barrier rounds][R][R] (always one pass); flags [G][R][J].
 size_t region_entries(const ra_ctx* h, int sync, int rounds, int G, int J) {
   const size_t R = (size_t)h->R;
   const size_t br = (size_t)(rounds > 1 ? rounds - 1 : 0);
-  if (sync == ra::kSyncCounting) return (size_t)G * br * R;
+  if (sync == ra::kSyncCounting) return (size_t)G * (size_t)J * br * R;
   if (sync == ra::kSyncPerPeer) return (size_t)G * br * R * R;
   return (size_t)G * R * (size_t)J;
 }
@@ -669,6 +672,33 @@ ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   return RA_OK;
 }
 
+// Sub-slices of a channel's slice when RA_OPT_SLICES is 0 (pipelined
+// variant), and passes of the persistent variant: the fewest that keep the
+// partials one round writes over all ranks -- n b / J bytes -- within 32 MiB,
+// a quarter of L2, so the successor reads them back from L2; at most 8.
+// Each sub-slice or pass adds a wait (pipelined) or barrier (persistent) per
+// round, so more of them cost more than they save.  Measured on GB300, fp32,
+// every J from 1 to 8, three runs each: R = 8 at 2^23 per rank (32 MiB per
+// round): J = 1 best for the persistent variant; 2^24: J = 2-3 (persistent,
+// counting barrier, 384 -> 324 us; pipelined 383 -> 339); 2^25: J = 4-6
+// (747 -> 631-651); 2^26: J = 8 (1472 -> 1291); R = 2, 16, 32 at 2^24: J = 2-3.
+int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
+  (void)G;
+  if (h->slices > 0) return h->slices;
+  const int64_t round_bytes = pl.n * (int64_t)elem_bytes(h->dtype);
+  int64_t J = ceil_div(round_bytes, (int64_t)32 << 20);
+  if (J > 8) J = 8;
+  return (int)(J < 1 ? 1 : J);
+}
+
+// Passes of the persistent variant (counting or cluster barrier): as the
+// pipelined variant's sub-slices, at most kMaxPasses; each pass takes one
+// sub-slice of the channel's slice through every round, with its own barrier
+// rounds.
+int persistent_passes(const ra_ctx* h, const ra::Plan& pl, int G) {
+  return std::min(pipeline_slices(h, pl, G), kMaxPasses);
+}
+
 // Persistent variant with the R CTAs of each channel in one thread-block
 // cluster: no signal memory, no co-residency across channels.
 ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
@@ -685,13 +715,13 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   a.R = h->R;
   a.mode = mode;
   a.sync = ra::kSyncCluster;
-  a.J = 1;
   a.rounds = h->region[ra::kSyncCounting][kind].rounds;
   if (h->ctas > 0) {
     a.G = h->ctas;
   } else {
     a.G = (int)default_channels(h, a.plan, clusters);   // one wave of clusters
   }
+  a.J = persistent_passes(h, a.plan, a.G);
   if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
   a.epoch = 1;
   a.timeout_ns = h->timeout_ns;
@@ -715,15 +745,15 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   a.R = h->R;
   a.mode = mode;
   a.sync = sync;
-  a.J = 1;
   a.rounds = reg->rounds;
   a.G = persistent_channels(h, a.plan);
+  a.J = sync == ra::kSyncCounting ? persistent_passes(h, a.plan, a.G) : 1;
   const int cap = h->persist_blocks_per_sm * h->num_sms;
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "persistent grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
-  if (region_entries(h, sync, a.rounds, a.G, 1) > reg->cap)
+  if (region_entries(h, sync, a.rounds, a.G, a.J) > reg->cap)
     return fail(RA_ERR_UNSUPPORTED, "too many channels for the signal slots");
-  s = prepare_region(*reg, a.G, 1, st);
+  s = prepare_region(*reg, a.G, a.J, st);
   if (s != RA_OK) return s;
   a.slots = reg->d;
   a.shadows = reg->shadows;
@@ -740,26 +770,10 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   return RA_OK;
 }
 
-// Sub-slices of a channel's slice when RA_OPT_SLICES is 0: one per 36 KiB, at
-// most 8.  With the default window of one sub-slice (every round on a
-// sub-slice before the next), a round's partials are read back from L2.
-// Measured on GB300, fp32, 57 channels at R = 8: 2^24 per rank (147 KB
-// slices) 381 us with one sub-slice, 342 us with 4; 2^26 per rank 1477 us
-// with 1, 1312 us with 8, 1334 with 16; R = 2, 16, 32 at 2^24: 3-4 % faster
-// with 4.  Each sub-slice adds a publish and a wait per round (about 1.5 us),
-// so more and smaller ones lose.
-int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
-  if (h->slices > 0) return h->slices;
-  const int64_t slice_bytes = pl.C * (int64_t)elem_bytes(h->dtype) / G;
-  int64_t J = slice_bytes / (36 * 1024);
-  if (J > 8) J = 8;
-  return (int)(J < 1 ? 1 : J);
-}
-
 // Sub-slices per window: the rounds run over W sub-slices before the next W.
 // Default 1: every round on one sub-slice, then the next (measured fastest
-// at every J above 1 up to 8 in the sweep above; at J = 4, R = 8, 2^24:
-// W = 1 342 us, 2 381 us, 4 408 us).
+// for every J from 2 to 8; at J = 4, R = 8, 2^24 fp32 per rank: W = 1 342 us,
+// 2 381 us, 4 408 us).
 int pipeline_window(const ra_ctx* h, int J) {
   if (h->window > 0) return std::min(h->window, J);
   return 1;
@@ -898,14 +912,14 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   h->local_blocks_per_sm = lbps;
 
   // counting-barrier slots: per kind, the most channels that can be
-  // co-resident x barrier rounds x waiters (the other schemes allocate theirs
-  // on first use)
+  // co-resident x the most passes x barrier rounds x waiters (the other
+  // schemes allocate theirs on first use)
   const int gmax = gmax_channels(h, bps);
   const int rounds[3] = {2 * (R - 1), R - 1, R - 1};
   size_t total = 0;
   for (int k = 0; k < 3; ++k) {
     for (int sy = 0; sy < 3; ++sy) h->region[sy][k].rounds = rounds[k];
-    h->region[ra::kSyncCounting][k].cap = region_entries(h, ra::kSyncCounting, rounds[k], gmax, 1);
+    h->region[ra::kSyncCounting][k].cap = region_entries(h, ra::kSyncCounting, rounds[k], gmax, kMaxPasses);
     total += 2 * h->region[ra::kSyncCounting][k].cap;   // signals and shadows
   }
   if (total > 0) {
@@ -1400,7 +1414,10 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
   const size_t need = region_entries(h, h->last_sync, reg.rounds, reg.G, reg.J);
   *count = need;
   if (channels) *channels = reg.G;
-  if (rounds) *rounds = h->last_sync == ra::kSyncFlags ? reg.rounds : (reg.rounds > 1 ? reg.rounds - 1 : 0);
+  if (rounds) {
+    const int br = reg.rounds > 1 ? reg.rounds - 1 : 0;
+    *rounds = h->last_sync == ra::kSyncFlags ? reg.rounds : (h->last_sync == ra::kSyncCounting ? br * reg.J : br);
+  }
   if (calls) *calls = reg.calls;
   if (!dst || need == 0) return RA_OK;  // sizes only
   if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);
@@ -1416,7 +1433,7 @@ ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count)
   *count = 0;
   if (h->last_kind < 0 || h->last_sync != ra::kSyncCounting) return RA_OK;
   const SlotRegion& reg = h->region[ra::kSyncCounting][h->last_kind];
-  const size_t need = region_entries(h, ra::kSyncCounting, reg.rounds, reg.G, 1);
+  const size_t need = region_entries(h, ra::kSyncCounting, reg.rounds, reg.G, reg.J);
   *count = need;
   if (!dst || need == 0) return RA_OK;
   if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);

@@ -34,6 +34,13 @@
 // thread-block cluster and meet at the hardware cluster barrier instead
 // (R <= 16; no cooperative launch needed, as no cluster waits on another).
 //
+// Passes: a channel's slice may be cut into J sub-slices that each go
+// through every round, with its own barrier rounds, before the next one
+// starts (J = 1: every round over the whole slice).  The partial a rank
+// writes in a round is then still in L2 when its successor reads it in the
+// next.  The passes touch disjoint elements, so no barrier separates them;
+// each (channel, pass, round) has its own slots.
+//
 // No wait is unbounded: a poll that passes the time limit records
 // (round, rank, channel, observed, expected) in the handle's error record and
 // the CTA returns; every other CTA sees the record at its next poll and
@@ -43,9 +50,11 @@
 
 namespace ra {
 
-// Signal row of one (channel, round): R slots, one per waiting rank.
-__device__ __forceinline__ int64_t counting_row(const PersistArgs& a, int g, int t) {
-  return ((int64_t)g * (a.rounds - 1) + t) * a.R;
+// Signal row of one (virtual channel, round): R slots, one per waiting rank.
+// Virtual channel g J + j is pass j of channel g, so the rows are laid out
+// [channel][pass][round].
+__device__ __forceinline__ int64_t counting_row(const PersistArgs& a, int gv, int t) {
+  return ((int64_t)gv * (a.rounds - 1) + t) * a.R;
 }
 
 // One counting-barrier round, on the signal layer (ra_signal.cuh): each
@@ -142,6 +151,8 @@ __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// g, G: the (virtual) channel and the channel count -- pass j of channel c
+// is virtual channel c J + j of G J, the (c J + j)-th slice of the chunk.
 template <class D, int OP>
 __device__ __forceinline__ void reduce_slice(const typename D::T* inc, const typename D::T* loc,
                                              typename D::T* dst, int64_t off, int64_t end, int g, int G) {
@@ -186,49 +197,51 @@ __global__ void __launch_bounds__(kPersistThreads, 3)
 persistent_kernel(const PersistArgs a) {
   using T = typename D::T;
   __shared__ int s_abort;
-  const int R = a.R, G = a.G;
+  const int R = a.R, GV = a.G * a.J;
   const int r = blockIdx.x % R;
-  const int g = blockIdx.x / R;
   const int p = (r == 0) ? R - 1 : r - 1;
-  for (int t = 0; t < a.rounds; ++t) {
-    // the counting barrier's waiter reads its shadow now; the value is used
-    // after the round's data work
-    uint64_t shadow_read = 0;
-    if (a.sync == kSyncCounting && threadIdx.x == 0 && t + 1 < a.rounds)
-      shadow_read = sig::shadow_ahead(a.shadows + counting_row(a, g, t) + r);
-    bool reduce;
-    int s;
-    if (a.mode == kModeAllGather) {
-      reduce = false;
-      s = t + 1;
-    } else if (t < R - 1) {
-      reduce = true;
-      s = t + 1;
-    } else {
-      reduce = false;
-      s = t - (R - 1) + 1;
-    }
-    int c = reduce ? (r - s) : (r + 1 - s);
-    c %= R;
-    if (c < 0) c += R;
-    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
-    const int64_t end = min(off + a.plan.C, a.plan.n);
-    if (off < end) {
-      if (reduce) {
-        const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
-        reduce_slice<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), off, end, g, G);
+  // pass j of channel c is virtual channel c J + j of G J (one pass: c)
+  for (int g = blockIdx.x / R * a.J, gend = g + a.J; g < gend; ++g) {
+    for (int t = 0; t < a.rounds; ++t) {
+      // the counting barrier's waiter reads its shadow now; the value is used
+      // after the round's data work
+      uint64_t shadow_read = 0;
+      if (a.sync == kSyncCounting && threadIdx.x == 0 && t + 1 < a.rounds)
+        shadow_read = sig::shadow_ahead(a.shadows + counting_row(a, g, t) + r);
+      bool reduce;
+      int s;
+      if (a.mode == kModeAllGather) {
+        reduce = false;
+        s = t + 1;
+      } else if (t < R - 1) {
+        reduce = true;
+        s = t + 1;
       } else {
-        copy_slice<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), off, end, g, G);
+        reduce = false;
+        s = t - (R - 1) + 1;
       }
-    }
-    if (t + 1 < a.rounds) {
-      if (a.sync == kSyncCluster) {
-        cluster_barrier();
-        continue;
+      int c = reduce ? (r - s) : (r + 1 - s);
+      c %= R;
+      if (c < 0) c += R;
+      const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
+      const int64_t end = min(off + a.plan.C, a.plan.n);
+      if (off < end) {
+        if (reduce) {
+          const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
+          reduce_slice<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), off, end, g, GV);
+        } else {
+          copy_slice<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), off, end, g, GV);
+        }
       }
-      const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
-                                              : counting_barrier(a, g, t, r, shadow_read, &s_abort);
-      if (!go) return;
+      if (t + 1 < a.rounds) {
+        if (a.sync == kSyncCluster) {
+          cluster_barrier();
+          continue;
+        }
+        const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
+                                                : counting_barrier(a, g, t, r, shadow_read, &s_abort);
+        if (!go) return;
+      }
     }
   }
 }
@@ -285,7 +298,8 @@ cudaError_t persistent_cluster_capacity(int dtype, int op, int R, int threads, i
 
 cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = persistent_select(dtype, op);
-  if (!fn || a.R < 2 || a.R > 16 || a.G < 1 || a.rounds < 1 || a.sync != kSyncCluster) return cudaErrorInvalidValue;
+  if (!fn || a.R < 2 || a.R > 16 || a.G < 1 || a.J < 1 || a.rounds < 1 || a.sync != kSyncCluster)
+    return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -296,7 +310,8 @@ cudaError_t launch_persistent_cluster(int dtype, int op, const PersistArgs& a, i
 
 cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = persistent_select(dtype, op);
-  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.rounds < 1) return cudaErrorInvalidValue;
+  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.rounds < 1 || (a.sync == kSyncPerPeer && a.J != 1))
+    return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PersistArgs*>(&a)};

@@ -146,14 +146,13 @@ pipelined_kernel(const PersistArgs a) {
       const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
       const int64_t end = min(off + a.plan.C, a.plan.n);
       const Span<V> sp(off, end);
-      int64_t pb, pe;
-      split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
       // failure injection: a flag counts finished rounds, so a rank that is
       // to fall silent withholds every publication from that round on
       const bool withhold = (r == a.skip_rank && t >= a.skip_round);
       for (int j = w0; j < w1; ++j) {
+        // sub-slice j of channel g: slice g J + j of the chunk cut in G J
         int64_t qb, qe;
-        split_vectors(pb, pe, j, J, &qb, &qe);
+        split_vectors(sp.vb, sp.ve, g * J + j, G * J, &qb, &qe);
         // round 0 reads inputs only; every later round reads what the
         // predecessor wrote in its previous round on this sub-slice
         if (t > 0 && !wait_flag(a, pred + j, base + t, t, r, g, p, &s_abort)) return;

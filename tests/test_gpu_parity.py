@@ -212,6 +212,50 @@ def test_barrier_exactly_r_minus_1_arrivals(ra, R, G):
         assert_bitwise_equal(got[r], want[r])
 
 
+@pytest.mark.parametrize("kind", ["counting", "per_peer", "cluster"])
+@pytest.mark.parametrize("passes", [2, 3, 8])
+def test_persistent_passes(ra, kind, passes):
+    """The persistent variant with its channel slices cut into passes (each
+    through every round, with barrier rounds of its own): bitwise the
+    oracle's on aligned and ragged plans, two calls in a row; the counting
+    barrier's slots then hold k (R-1) in every (channel, pass, round), and
+    the per-peer barrier stays at one pass."""
+    o = elementops.get_op("bf16", "sum")
+    opts = [(ra.Option.SLICES, passes)]
+    if kind != "counting":
+        opts.append((ra.Option.BARRIER, ra.Barrier.PER_PEER if kind == "per_peer" else ra.Barrier.CLUSTER))
+    for R, n in ((8, 2**20 + 7), (3, 100003), (16, 2**16 + 3), (4, 2**22 + 5)):
+        x = inputs.generate(R, n, "bf16", "grad", seed=passes + R)
+        want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, "bf16", "sum", "persistent", options=opts, repeat=2)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"{kind} passes={passes} R={R}")
+    if kind == "cluster":
+        return
+    R, G = 5, 3
+    n = R * 9000 + 1
+    x = inputs.generate(R, n, "f32", "normal", 11)
+    inp, out = DeviceRanks(R, n, np.float32, host=x), DeviceRanks(R, n, np.float32)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="persistent") as h:
+        h.set_option(ra.Option.CTAS, G)
+        for key, value in opts:
+            h.set_option(key, value)
+        J = passes if kind == "counting" else 1
+        for k in range(1, 3):
+            h.allreduce(inp.views, out.views)
+            slots, ch, rounds, calls = h.read_signals()
+            assert (ch, rounds, calls) == (G, J * barrier.barrier_rounds(R), k)
+            if kind == "counting":
+                assert len(slots) == G * rounds * R
+                assert all(v == barrier.expected_slot_value(R, k) for v in slots), slots
+                assert h.read_shadows() == slots
+        assert h.device_status()[0] == ra.Status.OK
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r], f"{kind} passes={passes} arrivals run")
+
+
 def test_barrier_timeout_reports_missing_arrival(ra):
     """A rank that withholds its arrival makes its peers' waits run out:
     the call reports RA_ERR_TIMEOUT with one arrival missing, nothing
