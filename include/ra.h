@@ -102,7 +102,9 @@ typedef enum ra_variant {
                                  output once */
   RA_VARIANT_RING = 2,        /* one launch per ring round: R-1 reduce rounds
                                  (recvReduceSend ... recvReduceCopySend), then
-                                 R-1 AllGather rounds done with TMA bulk copies */
+                                 R-1 AllGather rounds done with TMA bulk copies;
+                                 at large n the chunks go through the rounds
+                                 in passes (RA_OPT_SLICES) */
   RA_VARIANT_PERSISTENT = 3,  /* one cooperative launch running every round;
                                  simulated ranks meet at a barrier between
                                  rounds (RA_OPT_BARRIER: counting, the
@@ -170,7 +172,8 @@ typedef enum ra_option {
   RA_OPT_SLICES = 8,         /* sub-slices per channel slice of the pipelined
                                 variant, 1..64, and passes of the persistent
                                 variant with the counting or cluster barrier
-                                (each pass takes one sub-slice through every
+                                and of the ring variant (each pass takes one
+                                part of every slice or chunk through every
                                 round), at most 8 there; 0 (default) = the
                                 fewest that keep n * b / J within 32 MiB, at
                                 most 8 (1 up to 32 MiB per rank).  The

@@ -471,11 +471,41 @@ ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* o
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "compact kernel launch");
 }
 
-ra_status run_ring_reduce(ra_ctx* h, const void* const* in, void* const* out, cudaStream_t st) {
+// Sub-slices of a channel's slice when RA_OPT_SLICES is 0 (pipelined
+// variant), and passes of the persistent variant: the fewest that keep the
+// partials one round writes over all ranks -- n b / J bytes -- within 32 MiB,
+// a quarter of L2, so the successor reads them back from L2; at most 8.
+// Each sub-slice or pass adds a wait (pipelined) or barrier (persistent) per
+// round, so more of them cost more than they save.  Measured on GB300, fp32,
+// every J from 1 to 8, three runs each: R = 8 at 2^23 per rank (32 MiB per
+// round): J = 1 best for the persistent variant; 2^24: J = 2-3 (persistent,
+// counting barrier, 384 -> 324 us; pipelined 383 -> 339); 2^25: J = 4-6
+// (747 -> 631-651); 2^26: J = 8 (1472 -> 1291); R = 2, 16, 32 at 2^24: J = 2-3.
+int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
+  (void)G;
+  if (h->slices > 0) return h->slices;
+  const int64_t round_bytes = pl.n * (int64_t)elem_bytes(h->dtype);
+  int64_t J = ceil_div(round_bytes, (int64_t)32 << 20);
+  if (J > 8) J = 8;
+  return (int)(J < 1 ? 1 : J);
+}
+
+// Passes of the persistent variant (counting or cluster barrier) and of the
+// ring variant: as the pipelined variant's sub-slices, at most kMaxPasses;
+// each pass takes one part of every channel slice (ring variant: of every
+// chunk) through every round before the next pass starts.
+int persistent_passes(const ra_ctx* h, const ra::Plan& pl, int G) {
+  return std::min(pipeline_slices(h, pl, G), kMaxPasses);
+}
+
+// The ReduceScatter rounds of pass j of J.
+ra_status run_ring_reduce(ra_ctx* h, const void* const* in, void* const* out, int j, int J, cudaStream_t st) {
   ra::RoundArgs a;
   a.p = make_ptrs(h, in, out);
   a.plan = make_plan(h->R, h->n);
   a.R = h->R;
+  a.j = j;
+  a.J = J;
   const int ctas = round_ctas_per_rank(h, a.plan);
   for (int s = 1; s < h->R; ++s) {
     a.s = s;
@@ -485,12 +515,15 @@ ra_status run_ring_reduce(ra_ctx* h, const void* const* in, void* const* out, cu
   return RA_OK;
 }
 
-ra_status run_ring_gather(ra_ctx* h, void* const* buf, cudaStream_t st) {
+// The AllGather rounds of pass j of J.
+ra_status run_ring_gather(ra_ctx* h, void* const* buf, int j, int J, cudaStream_t st) {
   ra::CopyArgs a;
   std::memset(&a, 0, sizeof(a));
   for (int r = 0; r < h->R; ++r) a.buf[r] = buf[r];
   a.plan = make_plan(h->R, h->n);
   a.R = h->R;
+  a.j = j;
+  a.J = J;
   a.elem_bytes = (int)elem_bytes(h->dtype);
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -509,11 +542,17 @@ void drop_ring_graph(ra_ctx* h) {
   h->ring_kind = -1;
 }
 
+// Every round of every pass, pass after pass (a pass runs all its rounds
+// before the next starts).
 ra_status run_ring_launches(ra_ctx* h, int kind, const void* const* in, void* const* out, cudaStream_t st) {
-  if (kind == kKindAllGather) return run_ring_gather(h, out, st);
-  ra_status s = run_ring_reduce(h, in, out, st);
-  if (s != RA_OK || kind == kKindReduceScatter) return s;
-  return run_ring_gather(h, out, st);
+  const int J = persistent_passes(h, make_plan(h->R, h->n), 1);
+  for (int j = 0; j < J; ++j) {
+    ra_status s = RA_OK;
+    if (kind != kKindAllGather) s = run_ring_reduce(h, in, out, j, J, st);
+    if (s == RA_OK && kind != kKindReduceScatter) s = run_ring_gather(h, out, j, J, st);
+    if (s != RA_OK) return s;
+  }
+  return RA_OK;
 }
 
 // Ring variant: replay the cached graph of this call's launches when the
@@ -670,33 +709,6 @@ ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
     reg.calls = 0;
   }
   return RA_OK;
-}
-
-// Sub-slices of a channel's slice when RA_OPT_SLICES is 0 (pipelined
-// variant), and passes of the persistent variant: the fewest that keep the
-// partials one round writes over all ranks -- n b / J bytes -- within 32 MiB,
-// a quarter of L2, so the successor reads them back from L2; at most 8.
-// Each sub-slice or pass adds a wait (pipelined) or barrier (persistent) per
-// round, so more of them cost more than they save.  Measured on GB300, fp32,
-// every J from 1 to 8, three runs each: R = 8 at 2^23 per rank (32 MiB per
-// round): J = 1 best for the persistent variant; 2^24: J = 2-3 (persistent,
-// counting barrier, 384 -> 324 us; pipelined 383 -> 339); 2^25: J = 4-6
-// (747 -> 631-651); 2^26: J = 8 (1472 -> 1291); R = 2, 16, 32 at 2^24: J = 2-3.
-int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
-  (void)G;
-  if (h->slices > 0) return h->slices;
-  const int64_t round_bytes = pl.n * (int64_t)elem_bytes(h->dtype);
-  int64_t J = ceil_div(round_bytes, (int64_t)32 << 20);
-  if (J > 8) J = 8;
-  return (int)(J < 1 ? 1 : J);
-}
-
-// Passes of the persistent variant (counting or cluster barrier): as the
-// pipelined variant's sub-slices, at most kMaxPasses; each pass takes one
-// sub-slice of the channel's slice through every round, with its own barrier
-// rounds.
-int persistent_passes(const ra_ctx* h, const ra::Plan& pl, int G) {
-  return std::min(pipeline_slices(h, pl, G), kMaxPasses);
 }
 
 // Persistent variant with the R CTAs of each channel in one thread-block

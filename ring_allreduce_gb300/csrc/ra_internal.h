@@ -94,6 +94,7 @@ struct RoundArgs {
   Plan plan;
   int R;
   int s;
+  int j, J;             // pass j of J: the j-th of J parts of each chunk's whole vectors
 };
 
 // Ring variant, one AllGather round s (1..R-1) on out[]; grid.y = rank.
@@ -102,6 +103,7 @@ struct CopyArgs {
   Plan plan;
   int R;
   int s;
+  int j, J;             // pass j of J: the j-th of J parts of each chunk's 16-byte body
   int elem_bytes;
   int64_t timeout_ns;
   ra_device_error* err;

@@ -16,7 +16,11 @@
 //     tiles in flight per CTA; the unaligned head and tail bytes of a chunk
 //     are copied by the CTA's threads.
 // One launch covers all R ranks of a round (grid.y = rank); the stream
-// order between launches is the round order of the ring.  Rounds are
+// order between launches is the round order of the ring.  At large n the
+// chunks go through the rounds in J passes: pass j launches every round on
+// the j-th of J parts of each chunk, before pass j+1 starts, so the partial
+// a round writes is read back by the next round while it is still in L2
+// (the element-wise head and tail of a chunk belong to pass 0).  Rounds are
 // launched with programmatic dependent launch: a round's CTAs may be
 // scheduled while the previous round drains and wait (griddepcontrol.wait)
 // for its completion before they read.
@@ -44,14 +48,16 @@ rs_round_kernel(const RoundArgs a) {
   const T* loc = static_cast<const T*>(a.p.in[r]);
   T* dst = static_cast<T*>(a.p.out[r]);
   const Span<V> sp(off, end);
+  int64_t qb, qe;
+  split_vectors(sp.vb, sp.ve, a.j, a.J, &qb, &qe);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t v = sp.vb + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < sp.ve; v += stride) {
+  for (int64_t v = qb + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < qe; v += stride) {
     const uint4 x = reinterpret_cast<const uint4*>(inc)[v];
     const uint4 y = ld_stream(reinterpret_cast<const uint4*>(loc) + v);
     // plain store: the next round reads this partial, possibly from L2
     reinterpret_cast<uint4*>(dst)[v] = combine_vec<D, OP>(x, y);
   }
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && a.j == 0) {
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
       const int64_t i = sp.scalar_at(t);
@@ -81,7 +87,8 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 }
 
 cudaError_t launch_rs_round(int dtype, int op, const RoundArgs& a, int ctas_per_rank, cudaStream_t st) {
-  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
+  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || a.J < 1 || a.j < 0 || a.j >= a.J || ctas_per_rank < 1)
+    return cudaErrorInvalidValue;
   dim3 grid(ctas_per_rank, a.R);
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
     return launch_pdl(rs_round_kernel<decltype(d), decltype(o)::value>, grid, dim3(kRoundThreads), 0, st, a);
@@ -121,14 +128,19 @@ ag_round_kernel(const CopyArgs a) {
   const uint8_t* src = static_cast<const uint8_t*>(a.buf[p]);
   uint8_t* dst = static_cast<uint8_t*>(a.buf[r]);
 
-  // 16-byte aligned body [a0, a1); the rest is copied byte by byte
-  int64_t a0 = (b0 + 15) & ~int64_t(15);
-  int64_t a1 = b1 & ~int64_t(15);
-  if (a0 >= a1) { a0 = b1; a1 = b1; }
-  if (blockIdx.x == 0) {
-    for (int64_t i = b0 + threadIdx.x; i < a0; i += blockDim.x) st_g(dst + i, ld_g(src + i));
-    for (int64_t i = max(a1, a0) + threadIdx.x; i < b1; i += blockDim.x) st_g(dst + i, ld_g(src + i));
+  // 16-byte aligned body [c0, c1); the rest is copied byte by byte (pass 0)
+  int64_t c0 = (b0 + 15) & ~int64_t(15);
+  int64_t c1 = b1 & ~int64_t(15);
+  if (c0 >= c1) { c0 = b1; c1 = b1; }
+  if (blockIdx.x == 0 && a.j == 0) {
+    for (int64_t i = b0 + threadIdx.x; i < c0; i += blockDim.x) st_g(dst + i, ld_g(src + i));
+    for (int64_t i = max(c1, c0) + threadIdx.x; i < b1; i += blockDim.x) st_g(dst + i, ld_g(src + i));
   }
+  // this pass's part of the body, in whole 16-byte units: [a0, a1)
+  int64_t u0, u1;
+  split_vectors(0, (c1 - c0) / 16, a.j, a.J, &u0, &u1);
+  const int64_t a0 = c0 + 16 * u0;
+  const int64_t a1 = c0 + 16 * u1;
   const int64_t body = a1 - a0;
   const int64_t ntiles = (body + kTileBytes - 1) / kTileBytes;
   if ((int64_t)blockIdx.x >= ntiles || threadIdx.x != 0) return;
@@ -185,7 +197,8 @@ cudaError_t prepare_ag_round() {
 }
 
 cudaError_t launch_ag_round(const CopyArgs& a, int ctas_per_rank, cudaStream_t st) {
-  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || ctas_per_rank < 1) return cudaErrorInvalidValue;
+  if (a.R < 2 || a.R > kMaxRanks || a.s < 1 || a.s >= a.R || a.J < 1 || a.j < 0 || a.j >= a.J || ctas_per_rank < 1)
+    return cudaErrorInvalidValue;
   dim3 grid(ctas_per_rank, a.R);
   return launch_pdl(ag_round_kernel, grid, dim3(kCopyThreads), kCopySmem, st, a);
 }

@@ -256,6 +256,34 @@ def test_persistent_passes(ra, kind, passes):
         assert_bitwise_equal(got[r], want[r], f"{kind} passes={passes} arrivals run")
 
 
+@pytest.mark.parametrize("passes", [2, 3, 8])
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "all_gather"])
+def test_ring_passes(ra, passes, kind):
+    """The ring variant with its chunks taken through the rounds in passes
+    (each pass launches every round on one part of every chunk): bitwise the
+    oracle's for every collective, on aligned and ragged plans (bf16 chunk
+    starts off 16 bytes), graph captured on the first call and replayed on
+    the second."""
+    o = elementops.get_op("bf16", "sum")
+    for R, n in ((8, 2**20 + 7), (3, 100003), (16, 2**16 + 3), (4, 2**22 + 5)):
+        x = inputs.generate(R, n, "bf16", "grad", seed=passes + 3 * R)
+        if kind == "all_gather":
+            x = ring.ring_reduce_scatter(x, o)
+            want = ring.ring_allreduce(inputs.generate(R, n, "bf16", "grad", seed=passes + 3 * R), o)
+        elif kind == "reduce_scatter":
+            want = ring.ring_reduce_scatter(x, o)
+        else:
+            want = ring.ring_allreduce(x, o)
+        got = run_gpu(ra, x, "bf16", "sum", "ring", kind=kind, inplace=(kind == "all_gather"),
+                      options=[(ra.Option.SLICES, passes)], repeat=2)
+        for r in range(R):
+            if kind == "reduce_scatter":
+                off, L = ring.chunk_plan(R, n)[ring.owned_chunk(R, r)]
+                assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"{kind} passes={passes} R={R}")
+            else:
+                assert_bitwise_equal(got[r], want[r], f"{kind} passes={passes} R={R}")
+
+
 def test_barrier_timeout_reports_missing_arrival(ra):
     """A rank that withholds its arrival makes its peers' waits run out:
     the call reports RA_ERR_TIMEOUT with one arrival missing, nothing
