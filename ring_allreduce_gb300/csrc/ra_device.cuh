@@ -287,6 +287,24 @@ __device__ __forceinline__ void st_l2(uint4* p, uint4 v) {
   if (RA_ACCESS_OK(p, 16u, 2u)) __stcg(p, v);
 }
 
+// Drop dead data from L2 without writing it back.  After a warp has read
+// the 32 consecutive 16-byte vectors [v0, v0 + nv) of a partial that nobody
+// reads again before it is overwritten, the 128-byte lines lying wholly
+// inside that range are invalidated in L2 (discard.global.L2: a dirty line
+// is dropped instead of written to DRAM; the memory reads as undefined until
+// it is written again).  Lines the range only partly covers are left alone:
+// their other bytes may belong to another warp, CTA or chunk.  Every lane of
+// the warp calls this, after its own read of the range has completed.
+__device__ __forceinline__ void discard_read_lines(const uint4* v0, int64_t nv) {
+  __syncwarp();   // every lane's load of the range has returned
+  const uintptr_t a = reinterpret_cast<uintptr_t>(v0);
+  const uintptr_t lo = (a + 127u) & ~uintptr_t(127);
+  const uintptr_t hi = (a + 16u * (uintptr_t)nv) & ~uintptr_t(127);
+  const uintptr_t line = lo + 128u * (threadIdx.x & 31u);
+  if (line < hi && RA_ACCESS_OK(reinterpret_cast<const void*>(line), 128u, 2u))
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+}
+
 // One element, read once (evict-first), through the coherent path.
 template <class T> __device__ __forceinline__ T ld_stream_scalar(const T* p) {
   if (!RA_ACCESS_OK(p, sizeof(T), 1u)) return T();

@@ -153,17 +153,29 @@ __device__ __forceinline__ void cluster_barrier() {
 
 // g, G: the (virtual) channel and the channel count -- pass j of channel c
 // is virtual channel c J + j of G J, the (c J + j)-th slice of the chunk.
+// `dead_inc`: the incoming data is a partial of the ring that nobody reads
+// again (its place is overwritten by the complete value in AllGather), so
+// its L2 lines are dropped once read instead of being written back to DRAM.
 template <class D, int OP>
 __device__ __forceinline__ void reduce_slice(const typename D::T* inc, const typename D::T* loc,
-                                             typename D::T* dst, int64_t off, int64_t end, int g, int G) {
+                                             typename D::T* dst, int64_t off, int64_t end, int g, int G,
+                                             bool dead_inc) {
   constexpr int V = D::kVec;
   const Span<V> sp(off, end);
   int64_t pb, pe;
   split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
-  for (int64_t v = pb + threadIdx.x; v < pe; v += blockDim.x) {
-    const uint4 x = ld_l2(reinterpret_cast<const uint4*>(inc) + v);
-    const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
-    st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+  const uint4* inc4 = reinterpret_cast<const uint4*>(inc);
+  // a warp takes 32 consecutive vectors per step (all lanes loop the same
+  // number of times, so the warp can drop the lines it has read together)
+  const int lane = threadIdx.x & 31;
+  for (int64_t w = pb + (threadIdx.x - lane); w < pe; w += blockDim.x) {
+    const int64_t v = w + lane;
+    if (v < pe) {
+      const uint4 x = ld_l2(inc4 + v);
+      const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
+      st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+    }
+    if (dead_inc) discard_read_lines(inc4 + w, pe - w < 32 ? pe - w : 32);
   }
   if (g == 0) {
     const int64_t ns = sp.scalar_count();
@@ -228,7 +240,9 @@ persistent_kernel(const PersistArgs a) {
       if (off < end) {
         if (reduce) {
           const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
-          reduce_slice<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), off, end, g, GV);
+          // from round 2 on the incoming data is the predecessor's partial
+          reduce_slice<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), off, end, g, GV,
+                              s != 1);
         } else {
           copy_slice<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), off, end, g, GV);
         }

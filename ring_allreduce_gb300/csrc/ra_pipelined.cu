@@ -81,13 +81,23 @@ __device__ __forceinline__ void publish_flag(uint64_t* flag, uint64_t value, boo
   }
 }
 
+// `dead_inc`: the incoming data is the predecessor's partial, which nobody
+// reads again before the complete value overwrites it in AllGather; its L2
+// lines are dropped once read instead of being written back to DRAM.
 template <class D, int OP>
 __device__ __forceinline__ void reduce_range(const typename D::T* inc, const typename D::T* loc, typename D::T* dst,
-                                             int64_t qb, int64_t qe, const Span<D::kVec>& sp, bool scalars) {
-  for (int64_t v = qb + threadIdx.x; v < qe; v += blockDim.x) {
-    const uint4 x = ld_l2(reinterpret_cast<const uint4*>(inc) + v);
-    const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
-    st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+                                             int64_t qb, int64_t qe, const Span<D::kVec>& sp, bool scalars,
+                                             bool dead_inc) {
+  const uint4* inc4 = reinterpret_cast<const uint4*>(inc);
+  const int lane = threadIdx.x & 31;
+  for (int64_t w = qb + (threadIdx.x - lane); w < qe; w += blockDim.x) {
+    const int64_t v = w + lane;
+    if (v < qe) {
+      const uint4 x = ld_l2(inc4 + v);
+      const uint4 y = ld_l2(reinterpret_cast<const uint4*>(loc) + v);
+      st_l2(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+    }
+    if (dead_inc) discard_read_lines(inc4 + w, qe - w < 32 ? qe - w : 32);
   }
   if (scalars) {
     const int64_t ns = sp.scalar_count();
@@ -161,7 +171,7 @@ pipelined_kernel(const PersistArgs a) {
           if (reduce) {
             const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
             reduce_range<D, OP>(inc, static_cast<const T*>(a.p.in[r]), static_cast<T*>(a.p.out[r]), qb, qe, sp,
-                                scalars);
+                                scalars, s != 1);
           } else {
             copy_range<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), qb, qe, sp, scalars);
           }

@@ -51,11 +51,21 @@ rs_round_kernel(const RoundArgs a) {
   int64_t qb, qe;
   split_vectors(sp.vb, sp.ve, a.j, a.J, &qb, &qe);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t v = qb + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < qe; v += stride) {
-    const uint4 x = reinterpret_cast<const uint4*>(inc)[v];
-    const uint4 y = ld_stream(reinterpret_cast<const uint4*>(loc) + v);
-    // plain store: the next round reads this partial, possibly from L2
-    reinterpret_cast<uint4*>(dst)[v] = combine_vec<D, OP>(x, y);
+  const uint4* inc4 = reinterpret_cast<const uint4*>(inc);
+  // from round 2 on the incoming data is the predecessor's partial, which
+  // nobody reads again before AllGather overwrites it with the complete
+  // value: its L2 lines are dropped once read, not written back to DRAM
+  const bool dead_inc = s != 1;
+  const int lane = threadIdx.x & 31;
+  for (int64_t w = qb + (int64_t)blockIdx.x * blockDim.x + (threadIdx.x - lane); w < qe; w += stride) {
+    const int64_t v = w + lane;
+    if (v < qe) {
+      const uint4 x = ld_g(inc4 + v);
+      const uint4 y = ld_stream(reinterpret_cast<const uint4*>(loc) + v);
+      // plain store: the next round reads this partial, possibly from L2
+      st_g(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+    }
+    if (dead_inc) discard_read_lines(inc4 + w, qe - w < 32 ? qe - w : 32);
   }
   if (blockIdx.x == 0 && a.j == 0) {
     const int64_t ns = sp.scalar_count();
