@@ -330,14 +330,7 @@ def run_gpu_arm(args):
         "vs_baseline": None,
         "dtype": dtype,
         "data": "synthetic",
-        "config": {
-            "workload": WORKLOAD_TEXT.get(args.workload, args.workload) if args.n is None
-            else f"{args.workload} with n={n}",
-            "R": R, "n_per_rank": n, "op": op, "variant": variant_name,
-            "l2": f"inputs larger than L2: {R * n * b / 2**20:.0f} MiB of inputs, "
-                  f"{R * n * b / 2**20:.0f} MiB of outputs per step, no flush",
-            "parallelism": f"replicas x{ws} (each GPU runs its own {R}-rank ring)",
-        },
+        "config": workload_config(args, R, n, op, b, ws),
         "busbw": round(busbw, 3),
         "hbm_frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         "roofline": {
@@ -355,7 +348,7 @@ def run_gpu_arm(args):
             "traffic": traffic,
             "traffic_source": os.path.relpath(prof_path, ROOT) if prof_path else None,
         },
-        "gpu_launches": args.steps * (2 * (R - 1) if variant_name == "ring" else 1),
+        "gpu_launches": args.steps * (2 * (R - 1) * ring_passes(n * b) if variant_name == "ring" else 1),
     }
     if clk is not None:
         result["clocks"] = clk
@@ -394,6 +387,26 @@ def run_gpu_arm(args):
         print(json.dumps(result), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def ring_passes(round_bytes):
+    """Passes the ring variant takes its chunks through the rounds in (the
+    library's default: the fewest that keep n b / J within 32 MiB, at most
+    8); each pass launches all 2(R-1) round kernels."""
+    return max(1, min(8, -(-round_bytes // (32 << 20))))
+
+
+def workload_config(args, R, n, op, b, ws):
+    """The `config` of a bench line: the workload, identical for the GPU arm
+    and the reference arm (which times the oracle on a sample of it)."""
+    return {
+        "workload": WORKLOAD_TEXT.get(args.workload, args.workload) if args.n is None
+        else f"{args.workload} with n={n}",
+        "R": R, "n_per_rank": n, "op": op, "variant": args.variant,
+        "l2": f"inputs larger than L2: {R * n * b / 2**20:.0f} MiB of inputs, "
+              f"{R * n * b / 2**20:.0f} MiB of outputs per step, no flush",
+        "parallelism": f"replicas x{ws} (each GPU runs its own {R}-rank ring)",
+    }
 
 
 def run_e2e(torch, ra, h, big_in, big_out, R, n, steps, dist):
@@ -546,9 +559,7 @@ def run_reference_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload), "R": w["R"],
-                   "n_per_rank": w["n"], "op": w["ops"][0], "variant": "cpu oracle",
-                   "parallelism": "host, one thread"},
+        "config": workload_config(args, w["R"], args.n or w["n"], w["ops"][0], b, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
