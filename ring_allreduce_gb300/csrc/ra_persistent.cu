@@ -193,8 +193,17 @@ __device__ __forceinline__ void copy_slice(const typename D::T* src, typename D:
   const Span<V> sp(off, end);
   int64_t pb, pe;
   split_vectors(sp.vb, sp.ve, g, G, &pb, &pe);
-  for (int64_t v = pb + threadIdx.x; v < pe; v += blockDim.x)
-    st_l2(reinterpret_cast<uint4*>(dst) + v, ld_l2(reinterpret_cast<const uint4*>(src) + v));
+  const uint4* src4 = reinterpret_cast<const uint4*>(src);
+  uint4* dst4 = reinterpret_cast<uint4*>(dst);
+  const int64_t step = blockDim.x;
+  // two vectors a CTA's width apart per iteration: two loads in flight
+  for (int64_t v = pb + threadIdx.x; v < pe; v += 2 * step) {
+    const uint4 a0 = ld_l2(src4 + v);
+    uint4 a1;
+    if (v + step < pe) a1 = ld_l2(src4 + v + step);
+    st_l2(dst4 + v, a0);
+    if (v + step < pe) st_l2(dst4 + v + step, a1);
+  }
   if (g == 0) {
     const int64_t ns = sp.scalar_count();
     for (int64_t t = threadIdx.x; t < ns; t += blockDim.x) {
