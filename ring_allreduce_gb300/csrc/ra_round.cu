@@ -57,15 +57,28 @@ rs_round_kernel(const RoundArgs a) {
   // value: its L2 lines are dropped once read, not written back to DRAM
   const bool dead_inc = s != 1;
   const int lane = threadIdx.x & 31;
-  for (int64_t w = qb + (int64_t)blockIdx.x * blockDim.x + (threadIdx.x - lane); w < qe; w += stride) {
-    const int64_t v = w + lane;
-    if (v < qe) {
-      const uint4 x = ld_g(inc4 + v);
-      const uint4 y = ld_stream(reinterpret_cast<const uint4*>(loc) + v);
-      // plain store: the next round reads this partial, possibly from L2
-      st_g(reinterpret_cast<uint4*>(dst) + v, combine_vec<D, OP>(x, y));
+  const uint4* loc4 = reinterpret_cast<const uint4*>(loc);
+  uint4* dst4 = reinterpret_cast<uint4*>(dst);
+  // two steps of the grid (a grid's width apart) per iteration: four loads
+  // in flight per thread
+  for (int64_t w = qb + (int64_t)blockIdx.x * blockDim.x + (threadIdx.x - lane); w < qe; w += 2 * stride) {
+    const int64_t v0 = w + lane, v1 = v0 + stride;
+    uint4 x0, y0, x1, y1;
+    if (v0 < qe) {
+      x0 = ld_g(inc4 + v0);
+      y0 = ld_stream(loc4 + v0);
     }
-    if (dead_inc) discard_read_lines(inc4 + w, qe - w < 32 ? qe - w : 32);
+    if (v1 < qe) {
+      x1 = ld_g(inc4 + v1);
+      y1 = ld_stream(loc4 + v1);
+    }
+    // plain stores: the next round reads this partial, possibly from L2
+    if (v0 < qe) st_g(dst4 + v0, combine_vec<D, OP>(x0, y0));
+    if (v1 < qe) st_g(dst4 + v1, combine_vec<D, OP>(x1, y1));
+    if (dead_inc) {
+      discard_read_lines(inc4 + w, qe - w < 32 ? qe - w : 32);
+      if (w + stride < qe) discard_read_lines(inc4 + w + stride, qe - w - stride < 32 ? qe - w - stride : 32);
+    }
   }
   if (blockIdx.x == 0 && a.j == 0) {
     const int64_t ns = sp.scalar_count();
