@@ -481,8 +481,7 @@ ra_status run_compact(ra_ctx* h, int mode, const void* const* in, void* const* o
 // round): J = 1 best for the persistent variant; 2^24: J = 2-3 (persistent,
 // counting barrier, 384 -> 324 us; pipelined 383 -> 339); 2^25: J = 4-6
 // (747 -> 631-651); 2^26: J = 8 (1472 -> 1291); R = 2, 16, 32 at 2^24: J = 2-3.
-int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
-  (void)G;
+int pipeline_slices(const ra_ctx* h, const ra::Plan& pl) {
   if (h->slices > 0) return h->slices;
   const int64_t round_bytes = pl.n * (int64_t)elem_bytes(h->dtype);
   int64_t J = ceil_div(round_bytes, (int64_t)32 << 20);
@@ -494,8 +493,8 @@ int pipeline_slices(const ra_ctx* h, const ra::Plan& pl, int G) {
 // ring variant: as the pipelined variant's sub-slices, at most kMaxPasses;
 // each pass takes one part of every channel slice (ring variant: of every
 // chunk) through every round before the next pass starts.
-int persistent_passes(const ra_ctx* h, const ra::Plan& pl, int G) {
-  return std::min(pipeline_slices(h, pl, G), kMaxPasses);
+int persistent_passes(const ra_ctx* h, const ra::Plan& pl) {
+  return std::min(pipeline_slices(h, pl), kMaxPasses);
 }
 
 // The ReduceScatter rounds of pass j of J.
@@ -545,7 +544,7 @@ void drop_ring_graph(ra_ctx* h) {
 // Every round of every pass, pass after pass (a pass runs all its rounds
 // before the next starts).
 ra_status run_ring_launches(ra_ctx* h, int kind, const void* const* in, void* const* out, cudaStream_t st) {
-  const int J = persistent_passes(h, make_plan(h->R, h->n), 1);
+  const int J = persistent_passes(h, make_plan(h->R, h->n));
   for (int j = 0; j < J; ++j) {
     ra_status s = RA_OK;
     if (kind != kKindAllGather) s = run_ring_reduce(h, in, out, j, J, st);
@@ -733,7 +732,7 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   } else {
     a.G = (int)default_channels(h, a.plan, clusters);   // one wave of clusters
   }
-  a.J = persistent_passes(h, a.plan, a.G);
+  a.J = persistent_passes(h, a.plan);
   if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
   a.epoch = 1;
   a.timeout_ns = h->timeout_ns;
@@ -759,7 +758,7 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   a.sync = sync;
   a.rounds = reg->rounds;
   a.G = persistent_channels(h, a.plan);
-  a.J = sync == ra::kSyncCounting ? persistent_passes(h, a.plan, a.G) : 1;
+  a.J = sync == ra::kSyncCounting ? persistent_passes(h, a.plan) : 1;
   const int cap = h->persist_blocks_per_sm * h->num_sms;
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "persistent grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
@@ -811,7 +810,7 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   }
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "pipelined grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
-  a.J = pipeline_slices(h, a.plan, a.G);
+  a.J = pipeline_slices(h, a.plan);
   a.W = pipeline_window(h, a.J);
   if (region_entries(h, ra::kSyncFlags, a.rounds, a.G, a.J) > reg->cap)
     return fail(RA_ERR_UNSUPPORTED, "too many channels or sub-slices for the progress flags");
