@@ -275,6 +275,8 @@ int round_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
   return (int)(c < 1 ? 1 : c);
 }
 
+// AllGather round: at most one CTA per 16 KB of a chunk, and up to 3 CTAs
+// (64 KB of staging each) per SM over the R ranks.
 int copy_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
   if (h->ctas > 0) return h->ctas;
   const int64_t tiles = ceil_div(pl.C * (int64_t)elem_bytes(h->dtype), 16384) + 1;
