@@ -126,7 +126,15 @@ def main():
         if R <= 16:
             run(R, n, "f32", "sum", "persistent", "allreduce", options=[(ra.Option.BARRIER, ra.Barrier.CLUSTER)])
         run(R, n, "f32", "sum", "pipelined", "allreduce", options=[(ra.Option.SLICES, 3)])
-        calls += 6
+        run(R, n, "bf16", "sum", "pipelined", "allreduce", options=[(ra.Option.SLICES, 5), (ra.Option.WINDOW, 2)])
+        # passes: every round on one part of every chunk (slice) before the next part
+        for kind in ("allreduce", "reduce_scatter", "all_gather"):
+            run(R, n, "bf16", "sum", "ring", kind, options=[(ra.Option.SLICES, 3)])
+            run(R, n, "bf16", "sum", "persistent", kind, options=[(ra.Option.SLICES, 3)])
+        if R <= 16:
+            run(R, n, "f32", "sum", "persistent", "allreduce",
+                options=[(ra.Option.SLICES, 2), (ra.Option.BARRIER, ra.Barrier.CLUSTER)])
+        calls += 13 if R <= 16 else 12
     # the allocation-free entry point
     R, n = 4, 10007
     x = inputs.generate(R, n, "f32", "normal", seed=5)
