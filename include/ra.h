@@ -232,7 +232,9 @@ ra_status ra_destroy(ra_handle h);
 
 /* Ring ReduceScatter (section 5 of the ring page).  On completion chunk
  * (r+1) mod R of out[r] holds the complete S of that chunk; the other chunks
- * of out[r] hold unspecified values (partials of the ring). */
+ * of out[r] hold unspecified values (partials of the ring, or, where the
+ * round-by-round variants dropped a partial from L2 once its successor had
+ * read it, whatever memory then returns). */
 ra_status ra_reduce_scatter(ra_handle h, const void* const* in, void* const* out, void* stream);
 
 /* Ring AllGather (section 6), in place: buf[r] must hold in its chunk

@@ -343,6 +343,19 @@ def test_argument_checks_on_device(ra):
         with pytest.raises(ra.RAError) as e:
             h.allreduce(inp.ptrs(), mixed)
         assert e.value.status == ra.Status.ERR_INVALID
+        # option values outside their ranges are refused and change nothing
+        for key, value in ((ra.Option.SLICES, -1), (ra.Option.SLICES, 65), (ra.Option.WINDOW, -1),
+                           (ra.Option.WINDOW, 65), (ra.Option.VARIANT, 99), (ra.Option.BARRIER, 7),
+                           (ra.Option.TIMEOUT_NS, 10), (ra.Option.CTAS, -2), (ra.Option.GATHER, 3),
+                           (ra.Option.HOST_WINDOWS, 9)):
+            before = h.get_option(key)
+            with pytest.raises(ra.RAError) as e:
+                h.set_option(key, value)
+            assert e.value.status == ra.Status.ERR_INVALID, (key, value)
+            assert h.get_option(key) == before, key
+        with pytest.raises(ra.RAError) as e:
+            h.set_option(999, 1)
+        assert e.value.status == ra.Status.ERR_INVALID
         # nothing was enqueued: the device is fine and a good call works
         h.allreduce(inp.ptrs(), out.ptrs())
         assert h.device_status()[0] == ra.Status.OK
