@@ -289,18 +289,18 @@ int copy_ctas_per_rank(const ra_ctx* h, const ra::Plan& pl) {
 // one per 128 vectors of a chunk up to 16 -- a round's latency falls as its
 // slice shrinks (measured at R = 8: 53.6 -> 36.9 us per call at 2^18 fp32 per
 // rank), while tiny chunks gain nothing from more CTAs -- then enough for 4
-// vectors per thread at 512 threads, up to `most` (one wave).
-int64_t default_channels(const ra_ctx* h, const ra::Plan& pl, int64_t most) {
+// vectors per thread (`threads` per CTA), up to `most` (one wave).
+int64_t default_channels(const ra_ctx* h, const ra::Plan& pl, int64_t most, int threads) {
   const int64_t vecs = ceil_div(pl.C, vec_elems(h->dtype)) + 1;
   int64_t G = std::max<int64_t>(std::min<int64_t>(16, ceil_div(vecs, 128)),
-                                ceil_div(vecs, (int64_t)ra::kPersistThreads * 4));
+                                ceil_div(vecs, (int64_t)threads * 4));
   if (G > most) G = most;
   return G < 1 ? 1 : G;
 }
 
 int persistent_channels(const ra_ctx* h, const ra::Plan& pl) {
   const int cap = h->persist_blocks_per_sm * h->num_sms / h->R;
-  const int G = h->ctas > 0 ? h->ctas : (int)default_channels(h, pl, cap);
+  const int G = h->ctas > 0 ? h->ctas : (int)default_channels(h, pl, cap, ra::kPersistThreads);
   return G < 1 ? 1 : G;
 }
 
@@ -732,7 +732,7 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   if (h->ctas > 0) {
     a.G = h->ctas;
   } else {
-    a.G = (int)default_channels(h, a.plan, clusters);   // one wave of clusters
+    a.G = (int)default_channels(h, a.plan, clusters, ra::kPersistThreads);   // one wave of clusters
   }
   a.J = persistent_passes(h, a.plan);
   if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
@@ -808,7 +808,7 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   if (h->ctas > 0) {
     a.G = h->ctas;
   } else {
-    a.G = (int)default_channels(h, a.plan, cap / h->R);
+    a.G = (int)default_channels(h, a.plan, cap / h->R, ra::kPipeThreads);
   }
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "pipelined grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
@@ -825,7 +825,7 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   a.err = h->d_err;
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
   a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
-  cudaError_t e = ra::launch_pipelined(h->dtype, h->op, a, ra::kPersistThreads, st);
+  cudaError_t e = ra::launch_pipelined(h->dtype, h->op, a, ra::kPipeThreads, st);
   if (e != cudaSuccess) return cuda_fail(e, "pipelined kernel launch");
   reg->calls += 1;
   h->last_sync = ra::kSyncFlags;
@@ -896,7 +896,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   int bps = 0, pbps = 0;
   e = ra::persistent_blocks_per_sm(dtype, op, ra::kPersistThreads, &bps);
-  if (e == cudaSuccess) e = ra::pipelined_blocks_per_sm(dtype, op, ra::kPersistThreads, &pbps);
+  if (e == cudaSuccess) e = ra::pipelined_blocks_per_sm(dtype, op, ra::kPipeThreads, &pbps);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   e = ra::prepare_ag_round();
   if (e == cudaSuccess) e = ra::prepare_bcast();

@@ -186,6 +186,13 @@ size_t local_smem_bytes(int R);
 constexpr int kDirectThreads = 256;
 constexpr int kRoundThreads = 256;
 constexpr int kCopyThreads = 32;
-constexpr int kPersistThreads = 512;
+// Persistent kernel: CTAs of 256 threads, 6 per SM (one channel each; a
+// channel's barrier wait then overlaps five other channels' work on the SM).
+// Pipelined kernel: 512 threads, 3 per SM.  Measured on GB300 at R = 8, 2^24
+// fp32: persistent with the cluster barrier 286 -> 253 us at 256 threads,
+// counting barrier unchanged there, R = 16 605 -> 570 us, one-channel calls
+// 8-11 % faster; the pipelined kernel was 2-5 % slower at 256 or 128 threads.
+constexpr int kPersistThreads = 256;
+constexpr int kPipeThreads = 512;
 
 }  // namespace ra

@@ -214,7 +214,7 @@ __device__ __forceinline__ void copy_slice(const typename D::T* src, typename D:
 }
 
 template <class D, int OP>
-__global__ void __launch_bounds__(kPersistThreads, 3)
+__global__ void __launch_bounds__(kPersistThreads, 6)
 persistent_kernel(const PersistArgs a) {
   using T = typename D::T;
   __shared__ int s_abort;

@@ -123,7 +123,7 @@ __device__ __forceinline__ void copy_range(const typename D::T* src, typename D:
 }
 
 template <class D, int OP>
-__global__ void __launch_bounds__(kPersistThreads, 3)
+__global__ void __launch_bounds__(kPipeThreads, 3)
 pipelined_kernel(const PersistArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
