@@ -30,26 +30,52 @@ namespace ra {
 
 // ------------------------------------------------------------ reduce round
 
+// Ask the bulk-copy unit to bring the 16-byte vectors [v0, v0 + nv) into L2
+// ahead of their reads (cp.async.bulk.prefetch.L2: asynchronous; nothing in
+// the SM waits for it or receives data, and L2 stays coherent, so it cannot
+// change what a later load returns).  Requests of at most 64 KB each.
+__device__ __forceinline__ void prefetch_l2(const uint4* v0, int64_t nv) {
+  const char* p = reinterpret_cast<const char*>(v0);
+  for (int64_t left = nv * 16; left > 0;) {
+    const uint32_t piece = left > 65536 ? 65536u : (uint32_t)left;
+    if (RA_ACCESS_OK(p, piece, 1u))
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(piece) : "memory");
+    p += piece;
+    left -= piece;
+  }
+}
+
 template <class D, int OP>
 __global__ void __launch_bounds__(kRoundThreads)
 rs_round_kernel(const RoundArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
   griddep_launch_dependents();   // the next round may be scheduled ...
-  griddep_wait();                // ... but this one reads what the previous round wrote
   const int R = a.R, s = a.s, r = blockIdx.y;
   int c = r - s;
   if (c < 0) c += R;
   const int p = (r == 0) ? R - 1 : r - 1;
   const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
   const int64_t end = min(off + a.plan.C, a.plan.n);
-  if (off >= end) return;
   const T* inc = static_cast<const T*>(s == 1 ? a.p.in[p] : a.p.out[p]);
   const T* loc = static_cast<const T*>(a.p.in[r]);
   T* dst = static_cast<T*>(a.p.out[r]);
   const Span<V> sp(off, end);
-  int64_t qb, qe;
-  split_vectors(sp.vb, sp.ve, a.j, a.J, &qb, &qe);
+  int64_t qb = 0, qe = 0;
+  if (off < end) split_vectors(sp.vb, sp.ve, a.j, a.J, &qb, &qe);
+  // The inputs do not depend on the previous round (the own input never; the
+  // predecessor's in round 1): each CTA starts the DRAM reads of its share of
+  // them into L2 before the wait, so they overlap the previous round's drain.
+  if (threadIdx.x == 0 && qe > qb) {
+    int64_t cb, ce;
+    split_vectors(qb, qe, blockIdx.x, gridDim.x, &cb, &ce);
+    if (ce > cb) {
+      prefetch_l2(reinterpret_cast<const uint4*>(loc) + cb, ce - cb);
+      if (s == 1) prefetch_l2(reinterpret_cast<const uint4*>(inc) + cb, ce - cb);
+    }
+  }
+  griddep_wait();                // ... but this one reads what the previous round wrote
+  if (off >= end) return;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const uint4* inc4 = reinterpret_cast<const uint4*>(inc);
   // from round 2 on the incoming data is the predecessor's partial, which
