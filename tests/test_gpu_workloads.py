@@ -20,7 +20,7 @@ from rahelpers import DeviceRanks, assert_bitwise_equal
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
 
-VARIANTS = ["direct", "ring", "persistent", "pipelined"]
+VARIANTS = ["direct", "ring", "persistent", "pipelined", "local"]
 
 
 @pytest.fixture(scope="module")
@@ -97,7 +97,7 @@ def test_r16_i32(ra, op):
 @pytest.mark.parametrize("n", inputs.SWEEP_N)
 def test_sweep_r8_f32(ra, n):
     x = inputs.generate(8, n, "f32", "normal", inputs.SWEEP_SEED)
-    _check_allreduce(ra, x, "f32", "sum", VARIANTS if n <= 2**24 else ["direct", "persistent", "pipelined"])
+    _check_allreduce(ra, x, "f32", "sum", VARIANTS)
 
 
 @pytest.mark.parametrize("R", [R for R in inputs.SWEEP_R if R != 8])
