@@ -60,8 +60,9 @@ __device__ __forceinline__ bool readable(int64_t e, int64_t n) {
 // B: how many of a vector's R operand loads ReduceScatter issues before
 // folding them (all R when R <= B, as the direct kernel does; batches of B
 // otherwise, which keeps the registers of R = 32 to a few CTAs per SM).
-// B = 1: one load at a time, each folded as it arrives.  AllGather does not
-// depend on B.
+// B = 1: one load at a time, each folded as it arrives.  The AllGather
+// branch does not use B, but it shares the kernel's register allocation,
+// which B sets; it runs in the B = 1 instantiation.
 template <class D, int OP, int B>
 __global__ void __launch_bounds__(kCompactThreads)
 compact_kernel(const CompactArgs a) {
@@ -95,28 +96,32 @@ compact_kernel(const CompactArgs a) {
       return ld_ro(reinterpret_cast<const uint4*>(a.p.in[q]) + g);
     };
     auto fold = [&](int64_t g) {
-      if (B == 1) {
-        uint4 acc = load(0, g);
-        for (int j = 1; j < R; ++j) acc = combine_vec<D, OP>(acc, load(j, g));
+      if constexpr (B == 1) {
+        uint4 acc = ld_ro(reinterpret_cast<const uint4*>(a.p.in[k]) + g);
+        for (int j = 1; j < R; ++j) {
+          const int q = (k + j >= R) ? k + j - R : k + j;
+          acc = combine_vec<D, OP>(acc, ld_ro(reinterpret_cast<const uint4*>(a.p.in[q]) + g));
+        }
+        return acc;
+      } else {
+        uint4 x[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          if (j < R) x[j] = load(j, g);
+        uint4 acc = x[0];
+#pragma unroll
+        for (int j = 1; j < B; ++j)
+          if (j < R) acc = combine_vec<D, OP>(acc, x[j]);
+        for (int j0 = B; j0 < R; j0 += B) {
+#pragma unroll
+          for (int t = 0; t < B; ++t)
+            if (j0 + t < R) x[t] = load(j0 + t, g);
+#pragma unroll
+          for (int t = 0; t < B; ++t)
+            if (j0 + t < R) acc = combine_vec<D, OP>(acc, x[t]);
+        }
         return acc;
       }
-      uint4 x[B];
-#pragma unroll
-      for (int j = 0; j < B; ++j)
-        if (j < R) x[j] = load(j, g);
-      uint4 acc = x[0];
-#pragma unroll
-      for (int j = 1; j < B; ++j)
-        if (j < R) acc = combine_vec<D, OP>(acc, x[j]);
-      for (int j0 = B; j0 < R; j0 += B) {
-#pragma unroll
-        for (int t = 0; t < B; ++t)
-          if (j0 + t < R) x[t] = load(j0 + t, g);
-#pragma unroll
-        for (int t = 0; t < B; ++t)
-          if (j0 + t < R) acc = combine_vec<D, OP>(acc, x[t]);
-      }
-      return acc;
     };
     // A warp folds 32 consecutive vectors and writes the 31 outputs whose
     // both halves it holds: ~3 % extra loads, no lane folding twice.
@@ -183,16 +188,16 @@ cudaError_t launch_compact(int dtype, int op, const CompactArgs& a, int ctas_per
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
     using D = decltype(d);
     constexpr int OP = decltype(o)::value;
-    // fp64 additions are a scarce unit on this GPU: an 8-rank ragged fp64
-    // sum keeps them busy most of the time, and there folding each operand
-    // as it arrives (B = 1) measured 3-6 % faster than batched loads
-    if constexpr (std::is_same<D, DF64>::value && OP == kOpSum) {
-      if (a.mode == kModeReduceScatter)
-        compact_kernel<D, OP, 1><<<grid, kCompactThreads, 0, st>>>(a);
-      else
-        compact_kernel<D, OP, 2><<<grid, kCompactThreads, 0, st>>>(a);
-    } else {
-      if (a.mode == kModeAllGather || a.R <= 2)
+    // AllGather runs in the B = 1 instantiation: in the B = 2 one (fewer
+    // registers, more CTAs per SM) the ragged bf16 AllGather measured 6 %
+    // slower, in the B = 8 one the 4-rank fp64 one 8 % slower.  fp64 additions are a scarce unit on this GPU: an 8-rank ragged
+    // fp64 sum keeps them busy most of the time, and there folding each
+    // operand as it arrives (B = 1) measured 3-6 % faster than batched loads.
+    constexpr bool fp64_sum = std::is_same<D, DF64>::value && OP == kOpSum;
+    if (a.mode == kModeAllGather || fp64_sum) {
+      compact_kernel<D, OP, 1><<<grid, kCompactThreads, 0, st>>>(a);
+    } else if constexpr (!fp64_sum) {
+      if (a.R <= 2)
         compact_kernel<D, OP, 2><<<grid, kCompactThreads, 0, st>>>(a);
       else if (a.R <= 4)
         compact_kernel<D, OP, 4><<<grid, kCompactThreads, 0, st>>>(a);
