@@ -345,6 +345,10 @@ def run_gpu_arm(args):
             "bytes_per_launch": compulsory,
             "bytes_model": "compulsory 2*R*n*b (each input read once, each output written once)",
             "launch_ms_avg": round(launch_avg_s * 1e3, 6),
+            # the same bytes over the whole step (ms_per_step, back to back:
+            # includes the drain of the previous launch's writes from L2)
+            "achieved_step": round(compulsory / t_step / 1e9, 1),
+            "frac_step": round(compulsory / t_step / 1e9 / peak, 4),
             "traffic": traffic,
             "traffic_source": os.path.relpath(prof_path, ROOT) if prof_path else None,
         },
@@ -503,27 +507,100 @@ def _oracle_step_seconds(workload, n_sample):
     return time.perf_counter() - t, x, op
 
 
+def host_cores():
+    """Cores this process may run on (its CPU affinity)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_threaded_allreduce(x, op, threads):
+    """The oracle's ring AllReduce, as it stands, run on `threads` element
+    ranges at once (host threads; numpy releases the interpreter lock inside
+    its array operations).
+
+    Element i of chunk k is folded in the ring order that starts at rank k,
+    whatever the other elements do, so the elements [k C + a, k C + b) of
+    every chunk k form an AllReduce of their own: stacked chunk after chunk
+    (a rank vector of R (b - a) elements, whose chunk plan is again one piece
+    per chunk) and run through the oracle, they come out with the bits the
+    whole call gives them.  A short last chunk is padded with zeros to the
+    range; the padded places fold among themselves and are dropped.  Returns
+    the R outputs; the CPU tests check them bitwise against the oracle."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+
+    from oracle import ring
+    R, n = len(x), len(x[0])
+    plan = ring.chunk_plan(R, n)
+    C = max(L for _, L in plan) if n else 0
+    out = [np.empty_like(np.asarray(v)) for v in x]
+    if n == 0:
+        return out
+    threads = max(1, min(threads, C))
+    cuts = [C * t // threads for t in range(threads + 1)]
+
+    def piece(t):
+        a, b = cuts[t], cuts[t + 1]
+        w = b - a
+        if w <= 0:
+            return
+        sub = []
+        for r in range(R):
+            v = np.zeros(R * w, dtype=x[r].dtype)
+            for k, (o, L) in enumerate(plan):
+                hi = min(b, L)
+                if hi > a:
+                    v[k * w:k * w + hi - a] = x[r][o + a:o + hi]
+            sub.append(v)
+        res = ring.ring_allreduce(sub, op)
+        for r in range(R):
+            for k, (o, L) in enumerate(plan):
+                hi = min(b, L)
+                if hi > a:
+                    out[r][o + a:o + hi] = res[r][k * w:k * w + hi - a]
+
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        list(pool.map(piece, range(threads)))
+    return out
+
+
+def _timed_calls(fn, budget_s):
+    fn()   # warm-up call, not timed
+    times = []
+    t_start = time.perf_counter()
+    while (time.perf_counter() - t_start < budget_s and len(times) < 1000) or len(times) < 2:
+        t = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t)
+    return times
+
+
 def cpu_baseline(workload, budget_s=15.0, n_sample=None):
     """Time the oracle, as it stands, on R ranks of a sample of the
-    workload; value is algbw on the sample."""
+    workload, on one thread (value) and split over element ranges on every
+    core this process may use (`threaded`); values are algbw on the sample."""
     from oracle import ring
     from ring_allreduce_gb300 import inputs
     w = inputs.WORKLOADS[workload]
     b = inputs.itemsize(w["dtype"])
     n_sample = n_sample or w["n"]
-    _, x, op = _oracle_step_seconds(workload, n_sample)      # warm-up call, not timed
-    times = []
-    t_start = time.perf_counter()
-    while (time.perf_counter() - t_start < budget_s and len(times) < 1000) or len(times) < 2:
-        t = time.perf_counter()
-        ring.ring_allreduce(x, op)
-        times.append(time.perf_counter() - t)
-    t_mean = statistics.mean(times)
+    _, x, op = _oracle_step_seconds(workload, n_sample)
+    cores = host_cores()
+    times = _timed_calls(lambda: ring.ring_allreduce(x, op), budget_s * 2 / 3)
+    times_mt = _timed_calls(lambda: oracle_threaded_allreduce(x, op, cores), budget_s / 3)
+    t_mean, t_mt = statistics.mean(times), statistics.mean(times_mt)
+    what = 'the full workload' if n_sample == w['n'] else 'same recipe and seed as the workload'
     return {"value": round(n_sample * b / t_mean / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"R={w['R']} ranks x n={n_sample} per rank ("
-                      f"{'the full workload' if n_sample == w['n'] else 'same recipe and seed as the workload'}), "
+            "sample": f"R={w['R']} ranks x n={n_sample} per rank ({what}), "
                       f"{len(times)} oracle calls, {sum(times):.1f} s; numpy, one thread",
-            "ms_per_call": round(t_mean * 1e3, 3)}
+            "ms_per_call": round(t_mean * 1e3, 3),
+            "host_cores": cores,
+            "threaded": {"value": round(n_sample * b / t_mt / 1e9, 6), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle split over element ranges, one host thread per core",
+                         "sample": f"the same inputs, {len(times_mt)} calls, {sum(times_mt):.1f} s",
+                         "ms_per_call": round(t_mt * 1e3, 3)}}
 
 
 def run_reference_arm(args):
@@ -533,16 +610,22 @@ def run_reference_arm(args):
     from ring_allreduce_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
     b = inputs.itemsize(w["dtype"])
-    # size the sample so warm-up + K steps take about a minute
-    budget = 60.0 / max(1, args.steps + args.warmup)
-    n_sample = 2**12
-    while n_sample * 2 <= min(w["n"], 2**22):
-        t, _, _ = _oracle_step_seconds(args.workload, n_sample * 2)
-        if t > budget:
-            break
-        n_sample *= 2
+    n_full = args.n or w["n"]
+    # the whole workload when warm-up + K steps of it take at most three
+    # minutes (25 calls of the R = 8 x 2^24 fp32 headline: ~4 s), else the
+    # largest power-of-two sample that does, named in `config`
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    t_full, x, op = _oracle_step_seconds(args.workload, n_full)
+    n_sample = n_full
+    if t_full > budget:
+        n_sample = 2**12
+        while n_sample * 2 < n_full:
+            t, _, _ = _oracle_step_seconds(args.workload, n_sample * 2)
+            if t > budget:
+                break
+            n_sample *= 2
+        _, x, op = _oracle_step_seconds(args.workload, n_sample)
     from oracle import ring
-    _, x, op = _oracle_step_seconds(args.workload, n_sample)
     for _ in range(args.warmup):
         ring.ring_allreduce(x, op)
     times = []
@@ -552,15 +635,19 @@ def run_reference_arm(args):
         times.append(time.perf_counter() - t)
     t_step = statistics.mean(times)
     value = n_sample * b / t_step / 1e9
-    sample = (f"R={w['R']} ranks x n={n_sample} per rank (same recipe and seed as the workload) per step; "
-              f"numpy oracle, one thread")
+    what = "the full workload" if n_sample == n_full else "a sample: same recipe and seed as the workload"
+    sample = f"R={w['R']} ranks x n={n_sample} per rank ({what}) per step; numpy oracle, one thread"
+    cfg_args = argparse.Namespace(**vars(args))
+    if n_sample != n_full:
+        cfg_args.n = n_sample
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
         "data": "synthetic",
-        "config": workload_config(args, w["R"], args.n or w["n"], w["ops"][0], b, ws),
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": workload_config(cfg_args, w["R"], n_sample, w["ops"][0], b, ws),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "host_cores": host_cores()},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -334,15 +334,21 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
  * counting barrier between rounds) with results bitwise equal to
  * ra_allreduce's.
  *
- * Arguments as for ra_allreduce, with R in [2, 32]; the scratch a call
- * needs, (2R-3) * R slots per channel, always fits for one channel, and the
- * channel count is limited to what fits.  Host-side argument errors return
- * RA_ERR_INVALID and enqueue nothing.  No cudaMalloc, cudaFree or other
- * allocating call is made.
+ * Arguments as for ra_allreduce, with R in [2, 32] and n <= 2^40; the
+ * scratch a call needs, (2R-3) * R slots per channel, always fits for one
+ * channel, and the channel count is limited to what fits (every co-resident
+ * channel up to R = 10, 8 channels at R = 32).  Every buffer must be device
+ * (or managed) memory of the current device: each is checked with
+ * cudaPointerGetAttributes, which allocates nothing.  Host-side argument
+ * errors (including host memory, unknown addresses and another device's
+ * memory) return RA_ERR_INVALID and enqueue nothing.  No cudaMalloc,
+ * cudaFree or other allocating call is made.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call clears the part of the array it uses (an async memset
+ * device, with that device current) and keeps it for the life of the
+ * process; make that first call before any stream capture, and do not use
+ * this entry point on a device after cudaDeviceReset (the module, and with
+ * it the array, may then be loaded at another address).  Every call clears the part of the array it uses (an async memset
  * on `stream`) before its kernel, so nothing carries over from the previous
  * call.  All calls share the one array: calls that overlap on the GPU (other
  * streams, other threads) race on it and give wrong results.  A barrier wait

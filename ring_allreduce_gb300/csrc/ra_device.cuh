@@ -379,6 +379,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// The end of a bounded wait, kept on two clocks: the global timer, and the
+// SM's own cycle counter in case that timer stands still.  The cycle budget
+// is 3 cycles per nanosecond of the limit (saturating): at GB300's highest
+// SM clock (2.07 GHz) it runs out at 1.45 x the limit, at 1 GHz at 3 x, so a
+// wait never outlasts a small multiple of its limit whatever the poll costs.
+__device__ __forceinline__ uint64_t sm_cycles() {
+  uint64_t c;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+  return c;
+}
+
+struct Deadline {
+  uint64_t t0, c0;
+  int64_t ns, cycles;
+  __device__ __forceinline__ explicit Deadline(int64_t timeout_ns) {
+    t0 = globaltimer_ns();
+    c0 = sm_cycles();
+    ns = timeout_ns;
+    cycles = timeout_ns > ((int64_t)1 << 60) ? ((int64_t)1 << 62) : 3 * timeout_ns;
+  }
+  __device__ __forceinline__ bool passed() const {
+    return (int64_t)(globaltimer_ns() - t0) > ns || (int64_t)(sm_cycles() - c0) > cycles;
+  }
+};
+
 // Release / acquire in the fence form: one fence.acq_rel.gpu before a
 // batch of relaxed SignalAdds makes everything ordered before the fence
 // (this thread's writes and those of the CTA it synchronised with) visible

@@ -55,16 +55,14 @@ struct LocalShared {
 };
 
 // Bounded wait on a stage's mbarrier: gives up after timeout_ns of the
-// global timer, after timeout_ns + 10^6 polls should that timer stand still
-// (a poll takes well over a nanosecond), or once *abort is set; false when it
-// gave up.
+// global timer (or of the SM's cycle counter, should that timer stand still:
+// see Deadline), or once *abort is set; false when it gave up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int64_t timeout_ns,
                                              const volatile int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  const uint64_t max_polls = (uint64_t)timeout_ns + 1000000ull;
-  for (uint64_t it = 0; !mbar_try_wait(bar, parity); ++it) {
-    if ((int64_t)(globaltimer_ns() - t0) > timeout_ns || it > max_polls || (abort && *abort)) return false;
+  const Deadline limit(timeout_ns);
+  while (!mbar_try_wait(bar, parity)) {
+    if (limit.passed() || (abort && *abort)) return false;
   }
   return true;
 }

@@ -106,8 +106,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
     const int lane = threadIdx.x;
     const uint64_t* mine = round_slots + (int64_t)r * R;
     const bool active = lane < R && lane != r;
-    const uint64_t t0 = globaltimer_ns();
-    const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+    const Deadline limit(a.timeout_ns);
     int abort = 0;
     for (uint64_t it = 0;; ++it) {
       bool ok = true;
@@ -123,7 +122,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
         // the error record's stop word, on every 8th poll (read by every waiter)
         if ((it & 7u) == 7u && load_relaxed_u32(&a.err->code) != 0u)
           stop = 1;
-        else if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters)
+        else if (limit.passed())
           stop = 2;
       }
       stop = __shfl_sync(0xffffffffu, stop, 0);

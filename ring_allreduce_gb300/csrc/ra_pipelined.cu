@@ -48,8 +48,7 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
     int abort = 0;
     uint64_t seen = signal_load_acquire(flag);   // acquire: the predecessor's sub-slice is visible
     if (!rolling_reached(seen, target)) {
-      const uint64_t t0 = globaltimer_ns();
-      const uint64_t max_iters = (uint64_t)a.timeout_ns + 1000000ull;
+      const Deadline limit(a.timeout_ns);
       for (uint64_t it = 0;; ++it) {
         if (it > 16) __nanosleep(64);
         seen = signal_load_acquire(flag);
@@ -59,7 +58,7 @@ __device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* 
           abort = 1;
           break;
         }
-        if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || it > max_iters) {
+        if (limit.passed()) {
           record_wait_error(a.err, 4u, t, r, g, pred, seen, target);
           abort = 1;
           break;

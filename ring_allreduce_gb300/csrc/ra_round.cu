@@ -153,14 +153,13 @@ constexpr int kStages = 8;
 constexpr int kCopySmem = kTileBytes * kStages;
 
 // Bounded wait for a bulk load: gives up after timeout_ns of the global
-// timer, or after timeout_ns + 10^6 polls should that timer stand still (a
-// poll takes well over a nanosecond); false when it gave up.
+// timer (or of the SM's cycle counter, should that timer stand still: see
+// Deadline); false when it gave up.
 __device__ __forceinline__ bool wait_tile(uint64_t* bar, uint32_t parity, int64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  const uint64_t max_polls = (uint64_t)timeout_ns + 1000000ull;
-  for (uint64_t it = 0; !mbar_try_wait(bar, parity); ++it) {
-    if ((int64_t)(globaltimer_ns() - t0) > timeout_ns || it > max_polls) return false;
+  const Deadline limit(timeout_ns);
+  while (!mbar_try_wait(bar, parity)) {
+    if (limit.passed()) return false;
   }
   return true;
 }

@@ -17,7 +17,8 @@
 // Release is the caller's: one fence.acq_rel.gpu before a batch of adds
 // publishes everything the CTA wrote before it (the counting barrier issues
 // R-1 adds after one fence); the waits poll with acquire loads.  Every wait is bounded: it gives up after
-// `timeout_ns` (global timer) or an iteration limit, or when a stop word
+// `timeout_ns` (global timer, with the SM's cycle counter as a second clock,
+// see Deadline), or when a stop word
 // (the error record's code) says another waiter has already given up.  The
 // stop word is read on every 8th poll only: every waiter of a launch reads
 // the same word, and reading it on each poll (serially, or issued alongside
@@ -82,8 +83,7 @@ __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bi
                                      const uint32_t* stop, uint64_t* seen) {
   uint64_t v = signal_load_acquire(sig);
   if (!reached(v, least, bits)) {
-    const uint64_t t0 = globaltimer_ns();
-    const uint64_t max_iters = (uint64_t)timeout_ns + 1000000ull;   // every poll costs far more than 1 ns
+    const Deadline limit(timeout_ns);
     for (uint64_t it = 0;; ++it) {
       if (it > 32) __nanosleep(100);
       v = signal_load_acquire(sig);
@@ -92,7 +92,7 @@ __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bi
         *seen = v;
         return kAborted;
       }
-      if ((int64_t)(globaltimer_ns() - t0) > timeout_ns || it > max_iters) {
+      if (limit.passed()) {
         *seen = v;
         return kTimedOut;
       }

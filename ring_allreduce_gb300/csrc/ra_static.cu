@@ -62,6 +62,25 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
+// A buffer the kernel may be given: device or managed memory that the
+// current device can use.  cudaPointerGetAttributes allocates nothing; host
+// memory, an address CUDA does not know and another device's memory are
+// turned into RA_ERR_INVALID here instead of a memory fault in the kernel.
+ra_status check_pointer(const void* p, const char* name, int r, int dev) {
+  cudaPointerAttributes at;
+  const cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return record_error(RA_ERR_INVALID, "%s[%d]=%p: not a CUDA pointer (%s)", name, r, p, cudaGetErrorName(e));
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return record_error(RA_ERR_INVALID, "%s[%d]=%p: not device memory", name, r, p);
+  if (at.type == cudaMemoryTypeDevice && at.device != dev)
+    return record_error(RA_ERR_INVALID, "%s[%d]=%p: memory of device %d, the current device is %d", name, r, p,
+                        at.device, dev);
+  return RA_OK;
+}
+
 }  // namespace
 }  // namespace ra
 
@@ -73,6 +92,7 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   if (op != RA_SUM && op != RA_MAX) return record_error(RA_ERR_INVALID, "unknown op %d", (int)op);
   if (!in || !out) return record_error(RA_ERR_INVALID, "NULL pointer array");
   if (n == 0) return RA_OK;
+  if (n > ((size_t)1 << 40)) return record_error(RA_ERR_INVALID, "n=%zu above 2^40 elements", n);
   const size_t esize = (dtype == RA_BF16 || dtype == RA_F16) ? 2 : ((dtype == RA_F64 || dtype == RA_I64) ? 8 : 4);
   const size_t bytes = n * esize;
   for (int r = 0; r < R; ++r) {
@@ -98,6 +118,11 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
     return record_error(RA_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
   }
   if (!coop || bps < 1) return record_error(RA_ERR_UNSUPPORTED, "device has no cooperative launch");
+  for (int r = 0; r < R; ++r) {
+    ra_status ps = in[r] == out[r] ? RA_OK : check_pointer(in[r], "in", r, dev);
+    if (ps == RA_OK) ps = check_pointer(out[r], "out", r, dev);
+    if (ps != RA_OK) return ps;
+  }
   uint64_t* scratch = nullptr;
   ra_status s = scratch_address(dev, &scratch);
   if (s != RA_OK) return s;

@@ -45,3 +45,49 @@ def test_aggregate_over_two_gloo_ranks():
 def test_aggregate_single_process_is_identity():
     import bench
     assert bench.aggregate(0.25, 7.0, None) == (0.25, 7.0)
+
+
+@pytest.mark.parametrize("R,n,dtype,threads", [
+    (4, 4096, "f32", 3),          # divisible
+    (8, 1000003, "f32", 16),      # ragged: a short last chunk
+    (5, 13, "bf16", 4),           # tiny chunks, more threads than a range holds
+    (7, 30, "i32", 2),            # trailing chunks short and empty (C = 5: 6 chunks hold 30)
+    (6, 0, "f32", 4),             # nothing to do
+    (3, 20011, "f64", 5),
+])
+def test_threaded_cpu_baseline_is_the_oracle_bit_for_bit(R, n, dtype, threads):
+    """bench.py's multi-core CPU figure runs the oracle on element ranges in
+    parallel; every output must carry the bits of one oracle call on the
+    whole input (the fold order of an element depends on its chunk only)."""
+    import numpy as np
+    import bench
+    from oracle import elementops, ring
+    from ring_allreduce_gb300 import inputs
+    dist = {"f32": "normal", "bf16": "grad", "i32": "int20", "f64": "normal"}[dtype]
+    x = inputs.generate(R, n, dtype, dist, seed=77 + R)
+    op = elementops.get_op(dtype, "sum")
+    want = ring.ring_allreduce(x, op)
+    got = bench.oracle_threaded_allreduce(x, op, threads)
+    for r in range(R):
+        assert np.ascontiguousarray(got[r]).view(np.uint8).tobytes() == \
+            np.ascontiguousarray(want[r]).view(np.uint8).tobytes(), f"rank {r}"
+
+
+def test_threaded_cpu_baseline_catches_a_wrong_start_rank():
+    """The split must keep each element in its own chunk: folding a range as
+    if it sat in the next chunk (a start rank one off) changes the bits of
+    the ring-start pattern (2^24, 1, 1, -2^24 gives 0 only from rank k)."""
+    import numpy as np
+    import bench
+    from oracle import elementops, ring
+    R, n = 4, 16
+    x = [np.zeros(n, np.float32) for _ in range(R)]
+    for k in range(R):   # chunk k (4 elements): x_k = 2^24, x_{k+1} = 1, x_{k+2} = 1, x_{k+3} = -2^24
+        for j, v in enumerate((2.0**24, 1.0, 1.0, -2.0**24)):
+            x[(k + j) % R][4 * k:4 * k + 4] = v
+    op = elementops.get_op("f32", "sum")
+    got = bench.oracle_threaded_allreduce(x, op, 3)
+    assert all(np.all(got[r] == 0.0) for r in range(R))
+    assert np.all(ring.ring_allreduce(x, op)[0] == 0.0)
+    rotated = [x[(r + 1) % R] for r in range(R)]   # every element's fold starts one rank later
+    assert np.all(bench.oracle_threaded_allreduce(rotated, op, 3)[0] == 2.0)

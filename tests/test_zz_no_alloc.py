@@ -7,10 +7,13 @@ error record) from a fixed array inside the library instead of from
 ra_create.
 
 Checked here through the C ABI: two calls in a row give, bitwise, what the
-handle-based ra_allreduce gives on the same inputs (the tolerance of every
-parity test here is 0 ulp), leave the guard bands around every buffer alone,
-and the second call does not change the device's free memory.  This file is
-collected last, so a stop at the first failure has run everything else.
+oracle's ring simulation gives on the same inputs, and what the handle-based
+ra_allreduce gives (the tolerance of every parity test here is 0 ulp), leave
+the guard bands around every buffer alone, and the second call does not
+change the device's free memory.  One case is large enough that the array's
+size, not the GPU, limits the channel count (R = 32: 8 channels), so the
+signals and shadows at the array's far end are used.  This file is collected
+last, so a stop at the first failure has run everything else.
 """
 
 import ctypes
@@ -18,16 +21,18 @@ import ctypes
 import numpy as np
 import pytest
 
+from oracle import elementops, ring
 from ring_allreduce_gb300 import inputs
 from rahelpers import DeviceRanks, assert_bitwise_equal
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-CASES = [  # (R, n, dtype, op): ragged n, several channels, every dtype
+CASES = [  # (R, n, dtype, op): ragged n, several channels, three dtypes
     (8, 2**20 + 7, "f32", "sum"),
     (5, 300001, "bf16", "sum"),
     (16, 2**18 + 3, "i32", "max"),
+    (32, 2**22 + 5, "f32", "sum"),   # 8 channels: the array's size is the limit
 ]
 
 
@@ -54,13 +59,14 @@ def test_noalloc_matches_allreduce_two_calls_in_a_row(ra, R, n, dtype, op):
     st = inputs.storage_dtype(dtype)
     inp = DeviceRanks(R, n, st, host=x)
 
-    # the existing entry point, through a handle
+    # the oracle's ring, and the existing entry point through a handle
+    want = ring.ring_allreduce(x, elementops.get_op(dtype, op))
     ref_out = DeviceRanks(R, n, st)
     with ra.RingAllReduce(R, n, dtype, op) as h:
         h.allreduce(inp.views, ref_out.views)
         status, err = h.device_status()
         assert status == ra.Status.OK, err.as_dict()
-    want = ref_out.host()
+    handle = ref_out.host()
 
     outs = [DeviceRanks(R, n, st) for _ in range(2)]   # allocated before either call
     lib = ra.load_library()
@@ -78,7 +84,8 @@ def test_noalloc_matches_allreduce_two_calls_in_a_row(ra, R, n, dtype, op):
         assert inp.guards_intact() and out.guards_intact(), f"call {call}: write outside a buffer"
         got = out.host()
         for r in range(R):
-            assert_bitwise_equal(got[r], want[r], f"call {call} {dtype}/{op} R={R} n={n} rank {r}")
+            assert_bitwise_equal(got[r], want[r], f"call {call} {dtype}/{op} R={R} n={n} rank {r} vs the oracle")
+            assert_bitwise_equal(got[r], handle[r], f"call {call} {dtype}/{op} R={R} n={n} rank {r} vs ra_allreduce")
 
 
 def test_noalloc_rejects_bad_arguments(ra):
@@ -93,3 +100,20 @@ def test_noalloc_rejects_bad_arguments(ra):
     bad[1] = bad[0]
     assert lib.ra_allreduce_noalloc(4, 1024, 0, 0, _ptrs(inp), bad, stream) == ra.Status.ERR_INVALID
     assert "overlap" in ra.ra_last_error()
+    # more than 2^40 elements: rejected before n * element size is formed
+    assert lib.ra_allreduce_noalloc(4, 2**40 + 1, 0, 0, _ptrs(inp), _ptrs(out), stream) == ra.Status.ERR_INVALID
+    assert "2^40" in ra.ra_last_error()
+    # host memory (a numpy array) and an address CUDA does not know: rejected on
+    # the host, nothing is launched
+    host = np.zeros(4 * 1024 + 16, dtype=np.float32)
+    base = (host.ctypes.data + 15) // 16 * 16
+    bad = _ptrs(out)
+    bad[2] = base
+    assert lib.ra_allreduce_noalloc(4, 1024, 0, 0, _ptrs(inp), bad, stream) == ra.Status.ERR_INVALID
+    assert "out[2]" in ra.ra_last_error()
+    bad = _ptrs(inp)
+    bad[3] = 0x10000   # 16-byte aligned, never allocated
+    assert lib.ra_allreduce_noalloc(4, 1024, 0, 0, bad, _ptrs(out), stream) == ra.Status.ERR_INVALID
+    assert "in[3]" in ra.ra_last_error()
+    torch.cuda.synchronize()
+    assert inp.guards_intact() and out.guards_intact()
