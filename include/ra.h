@@ -197,6 +197,14 @@ typedef enum ra_option {
                                 before the next); values at or above the
                                 sub-slice count mean all of them (every round
                                 over the whole slice) */
+  RA_OPT_SIGNAL_BITS = 14,   /* width, 16..64 (default 64), of the signal
+                                comparisons of the persistent variant's
+                                barriers and the pipelined variant's flags:
+                                a wait compares the low bits in rolling order
+                                (x < x + 1 across wrap-around), as the GIN
+                                article's waitSignal(..., bits) does; a device
+                                whose signals are 56-bit counters would use 56.
+                                ra_read_signals returns the low bits too. */
   RA_OPT_DEBUG_SHRINK = 11   /* bounds-checked builds only (see
                                 ra_debug_bounds_report): register each of the
                                 call's buffers this many bytes shorter than it
@@ -302,9 +310,11 @@ ra_status ra_get_option(ra_handle h, int key, long long* value);
  * handle can be used again. */
 ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
 
-/* Synchronise the device and copy the signal array of the last persistent
+/* Synchronise the device and read the signal array of the last persistent
  * or pipelined launch (its kind and scheme) into dst (host array of cap
- * entries).  With dst == NULL only the sizes are returned.  *count gets the
+ * entries): readSignal on the device, so each entry is the low
+ * RA_OPT_SIGNAL_BITS bits of its signal (all 64 by default).  With dst ==
+ * NULL only the sizes are returned.  *count gets the
  * entries, *channels the channel count G, *calls how many calls of that kind
  * and scheme ran since the array was last zeroed, *rounds:
  *   counting barrier  [G][rounds][R] (rounds = barrier rounds of a call:
@@ -315,7 +325,10 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err);
  *   per-peer barrier  [G][rounds][R waiters][R peers]; every entry equals
  *                     calls, except waiter == peer, which stays 0
  *   pipelined flags   [G][R][J] (rounds = ring rounds, J = count / (G R));
- *                     every entry equals calls * rounds */
+ *                     every entry equals calls * rounds (SignalAdd of 1 per
+ *                     finished round), as does every waiter's shadow of its
+ *                     predecessor's flag (ra_read_shadows, laid out by
+ *                     waiter) */
 ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
                           int* channels, int* rounds, long long* calls);
 
@@ -359,13 +372,27 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
 ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op op, const void* const* in,
                                void* const* out, void* stream);
 
-/* The counting barrier's shadows after the last persistent call (when it
- * used the counting barrier), laid out as its signals: each waiter moves its
- * own shadow forward by R-1 per call and waits for its signal to meet it
- * ("comm: lift the GIN scale-out ceiling ...", section "Fix"), so after a
- * successful call every shadow equals its signal.  With dst == NULL only
- * *count is set. */
+/* The waiters' shadows after the last persistent call with the counting
+ * barrier or the last pipelined call, laid out as the signals: each waiter
+ * moves its own shadow forward by R-1 per call (counting barrier) or by 1 per
+ * round (a pipelined rank's shadow of its predecessor's flag) and waits for
+ * the signal to meet it ("comm: lift the GIN scale-out ceiling ...", section
+ * "Fix"; the GIN article's increaseSignalShadow / waitSignalMeetShadow), so
+ * after a successful call every shadow equals its signal.  The raw 64-bit
+ * values.  With dst == NULL only *count is set. */
 ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count);
+
+/* Set every signal of the counting barrier and of the pipelined flags that
+ * the handle holds to `signal_value` (resetSignal, then SignalAdd of the
+ * value) and every shadow to `shadow_value`, on the device, and synchronise.
+ * For tests of wrap-around and of the comparison width (RA_OPT_SIGNAL_BITS):
+ * the barrier and the flags compare each signal with its waiter's shadow,
+ * never with a count from 0, so any start value works as long as signal and
+ * shadow agree on the compared bits.  The slots keep the channel and pass
+ * layout of the last call; a call with another layout zeroes them again.
+ * The per-peer barrier's slots, which count calls, are left alone.  Do not
+ * call it while a call of the handle may be running. */
+ra_status ra_seed_signals(ra_handle h, uint64_t signal_value, uint64_t shadow_value);
 
 /* Builds with bounds checks (libra_gb300_debug.so, compiled with
  * -DRA_DEBUG_BOUNDS) only.  There every global access of every kernel is first

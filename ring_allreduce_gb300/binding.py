@@ -17,7 +17,8 @@ __all__ = [
     "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_allreduce_host", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
-    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_allreduce_noalloc",
+    "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_seed_signals",
+    "ra_allreduce_noalloc",
     "ra_debug_bounds_report",
     "ra_last_error",
     "ra_status_string", "RingAllReduce", "PreparedCall", "EXPORTED",
@@ -75,6 +76,7 @@ class Option(enum.IntEnum):
     HOST_WINDOWS = 10
     DEBUG_SHRINK = 11
     WINDOW = 12
+    SIGNAL_BITS = 14
 
 
 class DeviceError(ctypes.Structure):
@@ -116,6 +118,7 @@ EXPORTED = {
     "ra_allreduce_noalloc": (_ST, [ctypes.c_int, _SZ, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
                                    ctypes.POINTER(_P), _P]),
     "ra_read_shadows": (_ST, [_P, ctypes.POINTER(ctypes.c_uint64), _SZ, ctypes.POINTER(_SZ)]),
+    "ra_seed_signals": (_ST, [_P, ctypes.c_uint64, ctypes.c_uint64]),
     "ra_debug_bounds_report": (_ST, [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_ulonglong),
                                      ctypes.c_int]),
     "ra_last_error": (ctypes.c_char_p, []),
@@ -292,8 +295,14 @@ def ra_read_signals(h):
     return list(buf)[:count.value], ch.value, rd.value, calls.value
 
 
+def ra_seed_signals(h, signal_value, shadow_value):
+    """Set the counting-barrier and pipelined-flag signals to one value and
+    their shadows to another (wrap-around tests)."""
+    _check(_lib.ra_seed_signals(h, ctypes.c_uint64(int(signal_value)), ctypes.c_uint64(int(shadow_value))))
+
+
 def ra_read_shadows(h):
-    """The counting barrier's shadows of the last persistent call, flat."""
+    """The waiters' shadows of the last counting-barrier or pipelined call, flat."""
     count = _SZ()
     _check(_lib.ra_read_shadows(h, None, 0, ctypes.byref(count)))
     buf = (ctypes.c_uint64 * max(count.value, 1))()
@@ -387,6 +396,9 @@ class RingAllReduce:
 
     def read_shadows(self):
         return ra_read_shadows(self.h)
+
+    def seed_signals(self, signal_value, shadow_value):
+        ra_seed_signals(self.h, signal_value, shadow_value)
 
     def close(self):
         if self.h:

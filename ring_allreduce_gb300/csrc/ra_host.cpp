@@ -101,6 +101,7 @@ struct ra_ctx {
   int gather = 0;   // RA_OPT_GATHER
   int variant = RA_VARIANT_AUTO;
   long long timeout_ns = 1000000000LL;
+  int signal_bits = 64;   // RA_OPT_SIGNAL_BITS
   int ctas = 0;
   int check_pointers = 1;
   long long skip = -1;
@@ -622,14 +623,17 @@ ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
   if (!reg.d) {
     const int bps = sync == ra::kSyncFlags ? h->pipe_blocks_per_sm : h->persist_blocks_per_sm;
     const size_t cap = region_entries(h, sync, reg.rounds, gmax_channels(h, bps), kMaxSlices);
+    // the pipelined flags come with their waiters' shadows, laid out as the flags
+    const size_t words = sync == ra::kSyncFlags ? 2 * cap : cap;
     if (cap > 0) {
-      cudaError_t e = cudaMalloc(&reg.d, cap * sizeof(uint64_t));
-      if (e == cudaSuccess) e = cudaMemset(reg.d, 0, cap * sizeof(uint64_t));
+      cudaError_t e = cudaMalloc(&reg.d, words * sizeof(uint64_t));
+      if (e == cudaSuccess) e = cudaMemset(reg.d, 0, words * sizeof(uint64_t));
       if (e != cudaSuccess) {
         if (reg.d) cudaFree(reg.d);
         reg.d = nullptr;
         return cuda_fail(e, "signal slot allocation");
       }
+      if (sync == ra::kSyncFlags) reg.shadows = reg.d + cap;
     }
     reg.cap = cap;
     reg.owned = true;
@@ -699,12 +703,23 @@ void debug_compact(const ra_ctx* h, const void* const* full, const void* const* 
   for (int r = 0; r < h->R; ++r) debug_user(h, compact[r], len[(r + 1) % h->R] * b);
 }
 
+// resetSignal on every signal of a region (and its shadows to 0), on the stream.
+cudaError_t reset_region(const SlotRegion& reg, cudaStream_t st) {
+  if (!reg.d || !reg.cap) return cudaSuccess;
+  ra::SignalIoArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.signals = reg.d;
+  a.shadows = reg.shadows;
+  a.count = reg.cap;
+  a.op = ra::kSigReset;
+  a.bits = 64;
+  return ra::launch_signal_io(a, st);
+}
+
 ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   if (reg.G != G || reg.J != J) {
-    if (reg.cap) {
-      cudaError_t e = cudaMemsetAsync(reg.d, 0, region_words(reg) * sizeof(uint64_t), st);
-      if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
-    }
+    cudaError_t e = reset_region(reg, st);
+    if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
     reg.G = G;
     reg.J = J;
     reg.calls = 0;
@@ -737,6 +752,7 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   a.J = persistent_passes(h, a.plan);
   if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
   a.epoch = 1;
+  a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
   a.skip_rank = -1;
@@ -771,6 +787,7 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   a.slots = reg->d;
   a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
+  a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
@@ -819,8 +836,9 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   s = prepare_region(*reg, a.G, a.J, st);
   if (s != RA_OK) return s;
   a.slots = reg->d;
-  a.shadows = nullptr;
+  a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
+  a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
@@ -835,9 +853,10 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
 
 ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(h->d_err, 0, sizeof(ra_device_error), st);
+  debug_begin(h);
   for (auto& row : h->region)
     for (auto& reg : row)
-      if (e == cudaSuccess && reg.d && reg.cap) e = cudaMemsetAsync(reg.d, 0, region_words(reg) * sizeof(uint64_t), st);
+      if (e == cudaSuccess) e = reset_region(reg, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "device state reset");
   for (auto& row : h->region)
@@ -1319,6 +1338,10 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       if (value < 0 || value > kMaxSlices) return fail(RA_ERR_INVALID, "window %lld outside [0, %d]", value, kMaxSlices);
       h->window = (int)value;
       return RA_OK;
+    case RA_OPT_SIGNAL_BITS:
+      if (value < 16 || value > 64) return fail(RA_ERR_INVALID, "signal bits %lld outside [16, 64]", value);
+      h->signal_bits = (int)value;
+      return RA_OK;
     case RA_OPT_GATHER:
       if (value < 0 || value > 2) return fail(RA_ERR_INVALID, "gather kernel %lld outside [0, 2]", value);
       h->gather = (int)value;
@@ -1360,6 +1383,7 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_BARRIER: *value = h->barrier; return RA_OK;
     case RA_OPT_SLICES: *value = h->slices; return RA_OK;
     case RA_OPT_WINDOW: *value = h->window; return RA_OK;
+    case RA_OPT_SIGNAL_BITS: *value = h->signal_bits; return RA_OK;
     case RA_OPT_GATHER: *value = h->gather; return RA_OK;
     case RA_OPT_HOST_WINDOWS: *value = h->host_windows; return RA_OK;
     case RA_OPT_DEBUG_SHRINK: *value = h->debug_shrink; return RA_OK;
@@ -1409,7 +1433,9 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) 
               "device wait gave up: %s, round %d, rank %d, channel %d, peer %d, observed %llu of %llu "
               "(%llu missing)",
               what, rec.round, rec.rank, rec.channel, rec.peer, (unsigned long long)rec.observed,
-              (unsigned long long)rec.expected, (unsigned long long)(rec.expected - rec.observed));
+              (unsigned long long)rec.expected,
+              (unsigned long long)((rec.expected - rec.observed) &
+                                   (h->signal_bits >= 64 ? ~0ull : ((1ull << h->signal_bits) - 1ull))));
 }
 
 ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count, int* channels, int* rounds,
@@ -1434,9 +1460,49 @@ ra_status ra_read_signals(ra_handle h, uint64_t* dst, size_t cap, size_t* count,
   if (calls) *calls = reg.calls;
   if (!dst || need == 0) return RA_OK;  // sizes only
   if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);
+  // readSignal on the device: the low RA_OPT_SIGNAL_BITS bits of each
+  uint64_t* d_out = nullptr;
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpy(dst, reg.d, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMalloc(&d_out, need * sizeof(uint64_t));
+  if (e == cudaSuccess) {
+    ra::SignalIoArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.signals = reg.d;
+    a.out = d_out;
+    a.count = need;
+    a.op = ra::kSigRead;
+    a.bits = h->signal_bits;
+    debug_begin(h);
+    debug_add(d_out, need * sizeof(uint64_t));
+    e = ra::launch_signal_io(a, 0);
+  }
+  if (e == cudaSuccess) e = cudaMemcpy(dst, d_out, need * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  if (d_out) cudaFree(d_out);
   if (e != cudaSuccess) return cuda_fail(e, "signal read");
+  return RA_OK;
+}
+
+ra_status ra_seed_signals(ra_handle h, uint64_t signal_value, uint64_t shadow_value) {
+  if (!h) return fail(RA_ERR_INVALID, "NULL handle");
+  DeviceGuard g(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  debug_begin(h);
+  for (int sync : {(int)ra::kSyncCounting, (int)ra::kSyncFlags})
+    for (auto& reg : h->region[sync]) {
+      if (e != cudaSuccess || !reg.d || !reg.cap) continue;
+      ra::SignalIoArgs a;
+      std::memset(&a, 0, sizeof(a));
+      a.signals = reg.d;
+      a.shadows = reg.shadows;
+      a.count = reg.cap;
+      a.op = ra::kSigSeed;
+      a.bits = 64;
+      a.signal_value = signal_value;
+      a.shadow_value = shadow_value;
+      e = ra::launch_signal_io(a, 0);
+    }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "signal seed");
   return RA_OK;
 }
 
@@ -1444,9 +1510,10 @@ ra_status ra_read_shadows(ra_handle h, uint64_t* dst, size_t cap, size_t* count)
   if (!h || !count) return fail(RA_ERR_INVALID, "NULL argument");
   DeviceGuard g(h->device);
   *count = 0;
-  if (h->last_kind < 0 || h->last_sync != ra::kSyncCounting) return RA_OK;
-  const SlotRegion& reg = h->region[ra::kSyncCounting][h->last_kind];
-  const size_t need = region_entries(h, ra::kSyncCounting, reg.rounds, reg.G, reg.J);
+  if (h->last_kind < 0 || h->last_sync == ra::kSyncPerPeer || h->last_sync == ra::kSyncCluster) return RA_OK;
+  const SlotRegion& reg = h->region[h->last_sync][h->last_kind];
+  if (!reg.shadows) return RA_OK;
+  const size_t need = region_entries(h, h->last_sync, reg.rounds, reg.G, reg.J);
   *count = need;
   if (!dst || need == 0) return RA_OK;
   if (cap < need) return fail(RA_ERR_INVALID, "need %zu entries, got %zu", need, cap);

@@ -144,13 +144,30 @@ struct PersistArgs {
   int rounds;           // ring rounds this call runs
   uint64_t* slots;      // counting: [G][rounds-1][R]; per-peer: [G][rounds-1][R][R];
                         // flags: [G][R][J]
-  uint64_t* shadows;    // counting: each waiter's shadow, laid out as slots
+  uint64_t* shadows;    // counting: each waiter's shadow, laid out as slots; flags: rank r's
+                        // shadows of its predecessor's flags, [G][R][J] by waiter
   uint64_t epoch;       // calls on this slot array since it was zeroed, this one included
+  int bits;             // width of the signal comparisons (rolling order on the low bits), <= 64
   int64_t timeout_ns;
   ra_device_error* err;
   int skip_rank;        // failure injection: rank withholding one arrival, -1 = none
   int skip_round;
 };
+
+// Signal maintenance on the signal layer (ra_persistent.cu): reset, seed or
+// read every signal of an array (and its shadows, when given).
+enum SigOp : int { kSigReset = 0, kSigSeed = 1, kSigRead = 2 };
+struct SignalIoArgs {
+  uint64_t* signals;
+  uint64_t* shadows;      // may be null
+  uint64_t* out;          // kSigRead: the values read
+  size_t count;
+  int op;
+  int bits;               // kSigRead: low bits returned
+  uint64_t signal_value;  // kSigSeed
+  uint64_t shadow_value;
+};
+cudaError_t launch_signal_io(const SignalIoArgs& a, cudaStream_t st);
 
 cudaError_t launch_direct(int dtype, int op, const DirectArgs& a, int ctas_per_chunk, cudaStream_t st);
 // 16-byte vectors a thread of the direct kernel takes per step.
@@ -194,5 +211,6 @@ constexpr int kCopyThreads = 32;
 // 8-11 % faster; the pipelined kernel was 2-5 % slower at 256 or 128 threads.
 constexpr int kPersistThreads = 256;
 constexpr int kPipeThreads = 512;
+constexpr int kPipeMaxSlices = 64;   // sub-slices of a pipelined channel slice
 
 }  // namespace ra

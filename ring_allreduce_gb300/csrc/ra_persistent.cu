@@ -76,9 +76,10 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
     }
     const uint64_t target = sig::increase_shadow_from(a.shadows + row + r, shadow_read, (uint64_t)(a.R - 1));
     uint64_t seen = 0;
-    const sig::Wait w = sig::wait(sigs + r, target, 64, a.timeout_ns, &a.err->code, &seen);
-    // one counting slot cannot say which peer is late: peer = -1
-    if (w == sig::kTimedOut) record_wait_error(a.err, 1u, t, r, g, -1, seen, target);
+    const sig::Wait w = sig::wait(sigs + r, target, a.bits, a.timeout_ns, &a.err->code, &seen);
+    // one counting slot cannot say which peer is late: peer = -1; values in
+    // the compared width (the low `bits` bits)
+    if (w == sig::kTimedOut) record_wait_error(a.err, 1u, t, r, g, -1, seen, sig::low_bits(target, a.bits));
     *s_abort = w != sig::kReached;
   }
   __syncthreads();
@@ -87,10 +88,11 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
 
 // Per-peer barrier round, the design the counting barrier replaced ("comm:
 // lift the GIN scale-out ceiling ...", section "Problem" and the comparison in
-// section "Performance"): every waiter has one slot per peer; a peer stores
-// the call's epoch into its own slot of each waiter, and the waiter checks all
-// R-1 slots, one lane of warp 0 per peer.  A wait that runs out can name the
-// peer that did not arrive.
+// section "Performance"): every waiter has one signal per peer; a peer adds 1
+// to its own signal of each waiter (SignalAdd), so after the k-th call on the
+// slots every one holds k (the call's epoch), and the waiter reads all R-1
+// (readSignal, one lane of warp 0 per peer) until each has reached the epoch.
+// A wait that runs out can name the peer that did not arrive.
 __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
   __syncthreads();
   const int R = a.R;
@@ -99,7 +101,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
     fence_acq_rel_gpu();   // release: this round's stores of the whole CTA
     if (!(r == a.skip_rank && t == a.skip_round)) {
       for (int q = 0; q < R; ++q)
-        if (q != r) signal_store_relaxed(round_slots + (int64_t)q * R + r, a.epoch);
+        if (q != r) sig::add(round_slots + (int64_t)q * R + r, 1);
     }
   }
   if (threadIdx.x < 32) {
@@ -112,8 +114,8 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
       bool ok = true;
       uint64_t v = 0;
       if (active) {
-        v = signal_load_acquire(mine + lane);   // acquire, by the lane that observes the slot
-        ok = rolling_reached(v, a.epoch);
+        v = sig::read(mine + lane, a.bits);   // acquire, by the lane that observes the slot
+        ok = sig::reached(v, a.epoch, a.bits);
       }
       const unsigned missing = __ballot_sync(0xffffffffu, !ok);
       if (missing == 0u) break;
@@ -338,6 +340,41 @@ cudaError_t launch_persistent(int dtype, int op, const PersistArgs& a, int threa
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<PersistArgs*>(&a)};
   return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
+}
+
+// ------------------------------------------------ signal maintenance
+// The handle's signals and shadows between calls, on the signal layer: no
+// kernel of the handle runs meanwhile (the calls are ordered on the stream),
+// so a reset cannot race an update.
+//   kSigReset  resetSignal on every signal; shadows to 0
+//   kSigSeed   resetSignal, then SignalAdd(value) on every signal; shadows
+//              to 0, then moved forward by the shadow value
+//   kSigRead   readSignal(bits) of every signal into out[]
+__global__ void signal_io_kernel(const SignalIoArgs a) {
+  const size_t step = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.count; i += step) {
+    if (a.op == kSigRead) {
+      const uint64_t v = sig::read(a.signals + i, a.bits);
+      if (RA_ACCESS_OK(a.out + i, 8u, 2u)) a.out[i] = v;
+      continue;
+    }
+    sig::reset(a.signals + i);
+    if (a.op == kSigSeed) sig::add(a.signals + i, a.signal_value);
+    if (a.shadows) {
+      sig::reset(a.shadows + i);
+      if (a.op == kSigSeed) sig::increase_shadow(a.shadows + i, a.shadow_value);
+    }
+  }
+}
+
+cudaError_t launch_signal_io(const SignalIoArgs& a, cudaStream_t st) {
+  if (!a.signals || (a.op == kSigRead && !a.out) || a.bits < 1 || a.bits > 64) return cudaErrorInvalidValue;
+  if (a.count == 0) return cudaSuccess;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
+  const size_t blocks = (a.count + 255) / 256;
+  signal_io_kernel<<<(unsigned)(blocks > 1024 ? 1024 : blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace ra

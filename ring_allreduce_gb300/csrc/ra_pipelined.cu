@@ -32,51 +32,43 @@
 // the overwrite can never overtake the read it would spoil.  Reads of inputs
 // in round 1 need no wait at all.
 //
-// Flags are never cleared between calls: the k-th call on a flag array
-// starts from (k-1) * rounds, compared in 64-bit rolling order.  Waits are
-// bounded; one that runs out records (round, rank, channel, predecessor,
-// observed, expected) and the CTA returns, and every other waiter returns
-// at its next poll.  Data another CTA wrote is read through L2.
-#include "ra_device.cuh"
+// Flags are signals of the signal layer (ra_signal.cuh): a rank publishes a
+// finished round with SignalAdd(1) on its flag of the sub-slice.  The waiter
+// keeps a shadow of each predecessor flag it waits on -- in device memory
+// between calls, in shared memory during the launch -- moves it forward by 1
+// before each wait (increaseSignalShadow) and waits for the flag to meet it
+// (waitSignalMeetShadow), in rolling order on the low RA_OPT_SIGNAL_BITS
+// bits.  At the end of a call the shadow is moved past the last round (which
+// nobody waits on), so after every call shadow == flag == calls x rounds and
+// nothing is cleared between calls.  Waits are bounded; one that runs out
+// records (round, rank, channel, predecessor, observed, expected) and the CTA
+// returns, and every other waiter returns at its next poll.  Data another CTA
+// wrote is read through L2.
+#include "ra_signal.cuh"
 
 namespace ra {
 
-// Thread 0 waits until *flag reaches target; false when the CTA must stop.
-__device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* flag, uint64_t target, int t,
-                                          int r, int g, int pred, int* s_abort) {
+// Thread 0 moves its shadow of the predecessor's flag forward by one round
+// and waits until the flag meets it; false when the CTA must stop.
+__device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* flag, uint64_t* shadow, int t, int r,
+                                          int g, int pred, int* s_abort) {
   if (threadIdx.x == 0) {
-    int abort = 0;
-    uint64_t seen = signal_load_acquire(flag);   // acquire: the predecessor's sub-slice is visible
-    if (!rolling_reached(seen, target)) {
-      const Deadline limit(a.timeout_ns);
-      for (uint64_t it = 0;; ++it) {
-        if (it > 16) __nanosleep(64);
-        seen = signal_load_acquire(flag);
-        if (rolling_reached(seen, target)) break;
-        // the error record's stop word, on every 8th poll (read by every waiter)
-        if ((it & 7u) == 7u && load_relaxed_u32(&a.err->code) != 0u) {
-          abort = 1;
-          break;
-        }
-        if (limit.passed()) {
-          record_wait_error(a.err, 4u, t, r, g, pred, seen, target);
-          abort = 1;
-          break;
-        }
-      }
-    }
-    *s_abort = abort;
+    sig::increase_shadow(shadow, 1);
+    uint64_t seen = 0;
+    const sig::Wait w = sig::wait_meet_shadow(flag, shadow, a.bits, a.timeout_ns, &a.err->code, &seen);
+    if (w == sig::kTimedOut) record_wait_error(a.err, 4u, t, r, g, pred, seen, sig::low_bits(*shadow, a.bits));
+    *s_abort = w != sig::kReached;
   }
   __syncthreads();
   return *s_abort == 0;
 }
 
 // All threads' stores of the sub-slice are done; thread 0 publishes.
-__device__ __forceinline__ void publish_flag(uint64_t* flag, uint64_t value, bool withhold) {
+__device__ __forceinline__ void publish_flag(uint64_t* flag, bool withhold) {
   __syncthreads();
   if (threadIdx.x == 0) {
     fence_acq_rel_gpu();   // release
-    if (!withhold) signal_store_relaxed(flag, value);
+    if (!withhold) sig::add(flag, 1);
   }
 }
 
@@ -127,13 +119,16 @@ pipelined_kernel(const PersistArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
   __shared__ int s_abort;
+  __shared__ uint64_t s_shadow[kPipeMaxSlices];   // thread 0's shadows of the predecessor's flags
   const int R = a.R, G = a.G, J = a.J;
   const int r = blockIdx.x % R;
   const int g = blockIdx.x / R;
   const int p = (r == 0) ? R - 1 : r - 1;
   uint64_t* mine = a.slots + ((int64_t)g * R + r) * J;
   const uint64_t* pred = a.slots + ((int64_t)g * R + p) * J;
-  const uint64_t base = (a.epoch - 1) * (uint64_t)a.rounds;
+  uint64_t* const my_shadows = a.shadows + ((int64_t)g * R + r) * J;   // waiter r's, in device memory
+  if (threadIdx.x == 0)
+    for (int j = 0; j < J; ++j) s_shadow[j] = sig::shadow(my_shadows + j);
   for (int w0 = 0; w0 < J; w0 += a.W) {
     const int w1 = min(J, w0 + a.W);
     for (int t = 0; t < a.rounds; ++t) {
@@ -164,7 +159,7 @@ pipelined_kernel(const PersistArgs a) {
         split_vectors(sp.vb, sp.ve, g * J + j, G * J, &qb, &qe);
         // round 0 reads inputs only; every later round reads what the
         // predecessor wrote in its previous round on this sub-slice
-        if (t > 0 && !wait_flag(a, pred + j, base + t, t, r, g, p, &s_abort)) return;
+        if (t > 0 && !wait_flag(a, pred + j, &s_shadow[j], t, r, g, p, &s_abort)) return;
         const bool scalars = (g == 0 && j == 0);
         if (off < end) {
           if (reduce) {
@@ -175,10 +170,14 @@ pipelined_kernel(const PersistArgs a) {
             copy_range<D>(static_cast<const T*>(a.p.out[p]), static_cast<T*>(a.p.out[r]), qb, qe, sp, scalars);
           }
         }
-        publish_flag(mine + j, base + t + 1, withhold);
+        publish_flag(mine + j, withhold);
       }
     }
   }
+  // every publication of the call, the last round's too (nobody waits on
+  // it): the shadows in device memory meet the flags again for the next call
+  if (threadIdx.x == 0)
+    for (int j = 0; j < J; ++j) sig::increase_shadow(my_shadows + j, (uint64_t)a.rounds);
 }
 
 static const void* pipelined_select(int dtype, int op) {
@@ -198,7 +197,8 @@ cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks)
 
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
   const void* fn = pipelined_select(dtype, op);
-  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.W < 1 || a.rounds < 1)
+  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.J > kPipeMaxSlices || a.W < 1 || a.rounds < 1 ||
+      !a.shadows)
     return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
