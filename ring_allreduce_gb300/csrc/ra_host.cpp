@@ -73,6 +73,10 @@ struct SlotRegion {
   int J = 0;            // sub-slices (pipelined flags)
   int rounds = 0;       // ring rounds of this kind
   long long calls = 0;  // completed-or-enqueued calls since the last reset
+  // pipelined flags: the value every waiter's shadow starts the next call at
+  // (0 after a reset, the seeded value after ra_seed_signals, moved by the
+  // ring rounds with every call)
+  uint64_t shadow_base = 0;
 };
 
 enum Kind { kKindAllReduce = 0, kKindReduceScatter = 1, kKindAllGather = 2 };
@@ -720,6 +724,7 @@ ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
   if (reg.G != G || reg.J != J) {
     cudaError_t e = reset_region(reg, st);
     if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
+    reg.shadow_base = 0;
     reg.G = G;
     reg.J = J;
     reg.calls = 0;
@@ -787,6 +792,7 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   a.slots = reg->d;
   a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
+  a.shadow_base = 0;
   a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -838,14 +844,17 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   a.slots = reg->d;
   a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
+  a.shadow_base = 0;
   a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
   a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
+  a.shadow_base = reg->shadow_base;
   cudaError_t e = ra::launch_pipelined(h->dtype, h->op, a, ra::kPipeThreads, st);
   if (e != cudaSuccess) return cuda_fail(e, "pipelined kernel launch");
   reg->calls += 1;
+  reg->shadow_base += (uint64_t)a.rounds;
   h->last_sync = ra::kSyncFlags;
   h->last_kind = kind;
   return RA_OK;
@@ -860,7 +869,10 @@ ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "device state reset");
   for (auto& row : h->region)
-    for (auto& reg : row) reg.calls = 0;
+    for (auto& reg : row) {
+      reg.calls = 0;
+      reg.shadow_base = 0;
+    }
   return RA_OK;
 }
 
@@ -1500,6 +1512,7 @@ ra_status ra_seed_signals(ra_handle h, uint64_t signal_value, uint64_t shadow_va
       a.signal_value = signal_value;
       a.shadow_value = shadow_value;
       e = ra::launch_signal_io(a, 0);
+      reg.shadow_base = shadow_value;
     }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "signal seed");

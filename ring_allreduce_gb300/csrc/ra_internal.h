@@ -147,6 +147,7 @@ struct PersistArgs {
   uint64_t* shadows;    // counting: each waiter's shadow, laid out as slots; flags: rank r's
                         // shadows of its predecessor's flags, [G][R][J] by waiter
   uint64_t epoch;       // calls on this slot array since it was zeroed, this one included
+  uint64_t shadow_base; // flags: the value every waiter's shadow starts this call at
   int bits;             // width of the signal comparisons (rolling order on the low bits), <= 64
   int64_t timeout_ns;
   ra_device_error* err;

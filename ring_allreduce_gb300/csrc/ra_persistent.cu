@@ -60,10 +60,10 @@ __device__ __forceinline__ int64_t counting_row(const PersistArgs& a, int gv, in
 // One counting-barrier round, on the signal layer (ra_signal.cuh): each
 // peer adds 1 to the waiter's signal of this (channel, round); the waiter
 // moves its shadow forward by R-1 and waits for the signal to meet it.
-// `shadow_read` is thread 0's value of its shadow for this round, read when
+// `shadow` is thread 0's shadow for this round, read from device memory when
 // the round began (sig::shadow_ahead), so that read is off the barrier's
 // path.  Returns false when this CTA must stop.
-__device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, uint64_t shadow_read,
+__device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, int t, int r, sig::Shadow shadow,
                                                  int* s_abort) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -74,9 +74,10 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
       for (int q = 0; q < a.R; ++q)
         if (q != r) sig::add(sigs + q, 1);
     }
-    const uint64_t target = sig::increase_shadow_from(a.shadows + row + r, shadow_read, (uint64_t)(a.R - 1));
+    const uint64_t target = sig::increase_shadow(shadow, (uint64_t)(a.R - 1));
+    sig::store_shadow(a.shadows + row + r, shadow);
     uint64_t seen = 0;
-    const sig::Wait w = sig::wait(sigs + r, target, a.bits, a.timeout_ns, &a.err->code, &seen);
+    const sig::Wait w = sig::wait_meet_shadow(sigs + r, shadow, a.bits, a.timeout_ns, &a.err->code, &seen);
     // one counting slot cannot say which peer is late: peer = -1; values in
     // the compared width (the low `bits` bits)
     if (w == sig::kTimedOut) record_wait_error(a.err, 1u, t, r, g, -1, seen, sig::low_bits(target, a.bits));
@@ -227,9 +228,9 @@ persistent_kernel(const PersistArgs a) {
     for (int t = 0; t < a.rounds; ++t) {
       // the counting barrier's waiter reads its shadow now; the value is used
       // after the round's data work
-      uint64_t shadow_read = 0;
+      sig::Shadow shadow{0};
       if (a.sync == kSyncCounting && threadIdx.x == 0 && t + 1 < a.rounds)
-        shadow_read = sig::shadow_ahead(a.shadows + counting_row(a, g, t) + r);
+        shadow = sig::shadow_ahead(a.shadows + counting_row(a, g, t) + r);
       bool reduce;
       int s;
       if (a.mode == kModeAllGather) {
@@ -263,7 +264,7 @@ persistent_kernel(const PersistArgs a) {
           continue;
         }
         const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
-                                                : counting_barrier(a, g, t, r, shadow_read, &s_abort);
+                                                : counting_barrier(a, g, t, r, shadow, &s_abort);
         if (!go) return;
       }
     }
@@ -361,8 +362,9 @@ __global__ void signal_io_kernel(const SignalIoArgs a) {
     sig::reset(a.signals + i);
     if (a.op == kSigSeed) sig::add(a.signals + i, a.signal_value);
     if (a.shadows) {
-      sig::reset(a.shadows + i);
-      if (a.op == kSigSeed) sig::increase_shadow(a.shadows + i, a.shadow_value);
+      sig::Shadow s{0};
+      if (a.op == kSigSeed) sig::increase_shadow(s, a.shadow_value);
+      sig::store_shadow(a.shadows + i, s);
     }
   }
 }

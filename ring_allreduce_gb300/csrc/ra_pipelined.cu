@@ -34,13 +34,12 @@
 //
 // Flags are signals of the signal layer (ra_signal.cuh): a rank publishes a
 // finished round with SignalAdd(1) on its flag of the sub-slice.  The waiter
-// keeps a shadow of each predecessor flag it waits on -- in device memory
-// between calls, in shared memory during the launch -- moves it forward by 1
-// before each wait (increaseSignalShadow) and waits for the flag to meet it
+// keeps a shadow of each predecessor flag it waits on -- in a register during
+// the launch, in device memory between calls -- moved forward by 1 per round
+// (increaseSignalShadow), and waits for the flag to meet it
 // (waitSignalMeetShadow), in rolling order on the low RA_OPT_SIGNAL_BITS
-// bits.  At the end of a call the shadow is moved past the last round (which
-// nobody waits on), so after every call shadow == flag == calls x rounds and
-// nothing is cleared between calls.  Waits are bounded; one that runs out
+// bits.  After every call shadow == flag == its start value + calls x rounds,
+// and nothing is cleared between calls.  Waits are bounded; one that runs out
 // records (round, rank, channel, predecessor, observed, expected) and the CTA
 // returns, and every other waiter returns at its next poll.  Data another CTA
 // wrote is read through L2.
@@ -48,22 +47,26 @@
 
 namespace ra {
 
-// Thread 0 moves its shadow of the predecessor's flag forward by one round
-// and waits until the flag meets it; false when the CTA must stop.
-__device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* flag, uint64_t* shadow, int t, int r,
+// Thread 0 waits until the predecessor's flag of the sub-slice meets its
+// shadow of it, which stands `t` rounds past where it started the call
+// (moved forward by one per round: increaseSignalShadow); false when the
+// CTA must stop.
+__device__ __forceinline__ bool wait_flag(const PersistArgs& a, const uint64_t* flag, sig::Shadow start, int t, int r,
                                           int g, int pred, int* s_abort) {
   if (threadIdx.x == 0) {
-    sig::increase_shadow(shadow, 1);
+    sig::Shadow shadow = start;
+    sig::increase_shadow(shadow, (uint64_t)t);
     uint64_t seen = 0;
     const sig::Wait w = sig::wait_meet_shadow(flag, shadow, a.bits, a.timeout_ns, &a.err->code, &seen);
-    if (w == sig::kTimedOut) record_wait_error(a.err, 4u, t, r, g, pred, seen, sig::low_bits(*shadow, a.bits));
+    if (w == sig::kTimedOut) record_wait_error(a.err, 4u, t, r, g, pred, seen, sig::low_bits(shadow.v, a.bits));
     *s_abort = w != sig::kReached;
   }
   __syncthreads();
   return *s_abort == 0;
 }
 
-// All threads' stores of the sub-slice are done; thread 0 publishes.
+// All threads' stores of the sub-slice are done; thread 0 publishes the
+// finished round (SignalAdd of 1).
 __device__ __forceinline__ void publish_flag(uint64_t* flag, bool withhold) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -119,16 +122,26 @@ pipelined_kernel(const PersistArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
   __shared__ int s_abort;
-  __shared__ uint64_t s_shadow[kPipeMaxSlices];   // thread 0's shadows of the predecessor's flags
   const int R = a.R, G = a.G, J = a.J;
   const int r = blockIdx.x % R;
   const int g = blockIdx.x / R;
   const int p = (r == 0) ? R - 1 : r - 1;
   uint64_t* mine = a.slots + ((int64_t)g * R + r) * J;
   const uint64_t* pred = a.slots + ((int64_t)g * R + p) * J;
-  uint64_t* const my_shadows = a.shadows + ((int64_t)g * R + r) * J;   // waiter r's, in device memory
-  if (threadIdx.x == 0)
-    for (int j = 0; j < J; ++j) s_shadow[j] = sig::shadow(my_shadows + j);
+  // Waiter r's shadows of the predecessor's J flags.  They start every call
+  // equal -- reset or seeded together, each moved by the call's rounds -- at
+  // a value the host keeps with the flags and passes in (a.shadow_base), so
+  // the waiter holds its shadow in a register for the launch (reading it
+  // back from device memory here measured 5-12 % slower calls on GB300).
+  // Thread j keeps the copy of sub-slice j in device memory where it stands
+  // after the call -- moved past every round's publication, the last one
+  // too, which nobody waits on -- since nothing reads it during the launch.
+  const sig::Shadow start{a.shadow_base};
+  if (threadIdx.x < J) {
+    sig::Shadow s = start;
+    sig::increase_shadow(s, (uint64_t)a.rounds);
+    sig::store_shadow(a.shadows + ((int64_t)g * R + r) * J + threadIdx.x, s);
+  }
   for (int w0 = 0; w0 < J; w0 += a.W) {
     const int w1 = min(J, w0 + a.W);
     for (int t = 0; t < a.rounds; ++t) {
@@ -159,7 +172,7 @@ pipelined_kernel(const PersistArgs a) {
         split_vectors(sp.vb, sp.ve, g * J + j, G * J, &qb, &qe);
         // round 0 reads inputs only; every later round reads what the
         // predecessor wrote in its previous round on this sub-slice
-        if (t > 0 && !wait_flag(a, pred + j, &s_shadow[j], t, r, g, p, &s_abort)) return;
+        if (t > 0 && !wait_flag(a, pred + j, start, t, r, g, p, &s_abort)) return;
         const bool scalars = (g == 0 && j == 0);
         if (off < end) {
           if (reduce) {
@@ -174,10 +187,6 @@ pipelined_kernel(const PersistArgs a) {
       }
     }
   }
-  // every publication of the call, the last round's too (nobody waits on
-  // it): the shadows in device memory meet the flags again for the next call
-  if (threadIdx.x == 0)
-    for (int j = 0; j < J; ++j) sig::increase_shadow(my_shadows + j, (uint64_t)a.rounds);
 }
 
 static const void* pipelined_select(int dtype, int op) {

@@ -14,13 +14,13 @@
 //   * each signal has a shadow its owner moves at will; increaseSignalShadow
 //     and waitSignalMeetShadow wait for the value to catch up with it
 //     (`increase_shadow`, `wait_meet_shadow`).
-// Who uses what: the counting barrier of the persistent kernel (add, wait,
-// and its shadows in device memory through shadow_ahead /
-// increase_shadow_from), the per-peer barrier (add, read), the pipelined
-// kernel's progress flags (add; each waiter keeps its shadows of the flags it
-// waits on in shared memory for the launch: increase_shadow,
+// Who uses what: the counting barrier of the persistent kernel (add; each
+// waiter's shadow read ahead from device memory, increase_shadow by R-1,
+// store_shadow, wait_meet_shadow), the per-peer barrier (add, read), the
+// pipelined kernel's progress flags (add; the waiter's shadow of its
+// predecessor's flag, held in a register for the launch: increase_shadow,
 // wait_meet_shadow), and the handle's signal maintenance kernel (reset, add,
-// read, increase_shadow; ra_persistent.cu).  The comparison width `bits`
+// read, increase_shadow, store_shadow; ra_persistent.cu).  The comparison width `bits`
 // (RA_OPT_SIGNAL_BITS) is 64 unless a call asks for fewer, as a counter of
 // 56 bits would.
 // Release is the caller's: one fence.acq_rel.gpu before a batch of adds
@@ -41,15 +41,14 @@ namespace sig {
 
 enum Wait : int { kReached = 0, kAborted = 1, kTimedOut = 2 };
 
-__device__ __forceinline__ uint64_t low_bits(uint64_t v, int bits) {
-  return bits >= 64 ? v : (v & ((1ull << bits) - 1ull));
-}
+// The low `bits` bits (1 <= bits <= 64).
+__device__ __forceinline__ uint64_t low_bits(uint64_t v, int bits) { return v & (~0ull >> (64 - bits)); }
 
-// Rolling comparison on the low `bits` bits: has `value` reached `least`?
+// Rolling comparison on the low `bits` bits (1 <= bits <= 64): has `value`
+// reached `least`?  The difference, modulo 2^bits, lies in the lower half;
+// shifted up to the top of 64 bits, that is its sign bit being clear.
 __device__ __forceinline__ bool reached(uint64_t value, uint64_t least, int bits = 64) {
-  if (bits >= 64) return (int64_t)(value - least) >= 0;
-  const uint64_t d = low_bits(value - least, bits);
-  return d < (1ull << (bits - 1));
+  return (int64_t)((value - least) << (64 - bits)) >= 0;
 }
 
 // SignalAdd.
@@ -63,36 +62,32 @@ __device__ __forceinline__ uint64_t read(const uint64_t* sig, int bits = 64) {
 // resetSignal: 0; no other update of the signal may race it.
 __device__ __forceinline__ void reset(uint64_t* sig) { signal_store_relaxed(sig, 0); }
 
-// Shadows belong to one waiter (one thread), so plain accesses do, in
-// device memory (where they persist across launches, read and written
-// through L2) or in shared memory (for the length of a launch).
-__device__ __forceinline__ uint64_t shadow(const uint64_t* sh) {
-  if (__isShared(sh)) return *sh;
-  return (uint64_t)ld_l2_scalar(reinterpret_cast<const int64_t*>(sh));
+// A waiter's shadow of a signal: a value its owner (one thread) moves at
+// will and waits for the signal to meet.  The owner holds it in a register
+// while it runs; where it persists between launches (device memory) is the
+// owner's business: load_shadow / shadow_ahead / store_shadow.
+struct Shadow {
+  uint64_t v;
+};
+
+// The shadow kept in device memory, read through L2.
+__device__ __forceinline__ Shadow load_shadow(const uint64_t* sh) {
+  return Shadow{(uint64_t)ld_l2_scalar(reinterpret_cast<const int64_t*>(sh))};
 }
 
-// increaseSignalShadow: move the shadow forward by `delta`; returns it.
-__device__ __forceinline__ uint64_t increase_shadow(uint64_t* sh, uint64_t delta) {
-  const uint64_t v = shadow(sh) + delta;
-  if (__isShared(sh)) {
-    *sh = v;
-  } else if (RA_ACCESS_OK(sh, 8u, 2u)) {
-    __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
-  }
-  return v;
+// The same read issued early, as an ordered load, for a waiter that knows
+// which shadow it will move next: the compiler keeps the load where it is
+// written, so its latency overlaps whatever comes next.
+__device__ __forceinline__ Shadow shadow_ahead(const uint64_t* sh) { return Shadow{signal_load_relaxed(sh)}; }
+
+__device__ __forceinline__ void store_shadow(uint64_t* sh, Shadow s) {
+  if (RA_ACCESS_OK(sh, 8u, 2u)) __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)s.v);
 }
 
-// The same in two steps, for a waiter that knows early which shadow in
-// device memory it will move: `shadow_ahead` issues the read (an ordered
-// load, so the compiler keeps it where it is written and its latency
-// overlaps whatever comes next); `increase_shadow_from` stores the moved
-// value and returns it.
-__device__ __forceinline__ uint64_t shadow_ahead(const uint64_t* sh) { return signal_load_relaxed(sh); }
-
-__device__ __forceinline__ uint64_t increase_shadow_from(uint64_t* sh, uint64_t read, uint64_t delta) {
-  const uint64_t v = read + delta;
-  if (RA_ACCESS_OK(sh, 8u, 2u)) __stcg(reinterpret_cast<unsigned long long*>(sh), (unsigned long long)v);
-  return v;
+// increaseSignalShadow: move the shadow forward by `delta`; returns its value.
+__device__ __forceinline__ uint64_t increase_shadow(Shadow& s, uint64_t delta) {
+  s.v += delta;
+  return s.v;
 }
 
 // waitSignal: wait until the signal reaches `least` (rolling, low `bits`
@@ -124,9 +119,9 @@ __device__ __forceinline__ Wait wait(const uint64_t* sig, uint64_t least, int bi
 }
 
 // waitSignalMeetShadow: wait until the signal reaches its shadow.
-__device__ __forceinline__ Wait wait_meet_shadow(const uint64_t* sig, const uint64_t* sh, int bits,
-                                                 int64_t timeout_ns, const uint32_t* stop, uint64_t* seen) {
-  return wait(sig, shadow(sh), bits, timeout_ns, stop, seen);
+__device__ __forceinline__ Wait wait_meet_shadow(const uint64_t* sig, const Shadow& s, int bits, int64_t timeout_ns,
+                                                 const uint32_t* stop, uint64_t* seen) {
+  return wait(sig, s.v, bits, timeout_ns, stop, seen);
 }
 
 }  // namespace sig

@@ -165,6 +165,7 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
   a.slots = scratch + kStaticErrWords;
   a.shadows = a.slots + G * per_channel;
   a.epoch = 1;
+  a.shadow_base = 0;
   a.bits = 64;
   a.timeout_ns = 1000000000LL;
   a.err = reinterpret_cast<ra_device_error*>(scratch);
