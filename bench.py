@@ -218,7 +218,12 @@ def _device_ranks(torch, R, n, np_dtype, host=None):
     return big, [big[r, :n] for r in range(R)]
 
 
-def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True):
+def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True, queued=False):
+    """CUDA-event times of `steps` calls after `warmup` (total ms, per-call
+    ms).  queued: a spin kernel holds the stream while the host enqueues
+    every timed call, so the device runs them back to back and the per-call
+    times are device time -- without it a call shorter than the host's own
+    cost of issuing it (a few microseconds from Python) measures the host."""
     stream = torch.cuda.current_stream()
     call = h.prepare("allreduce", ins, outs, stream)
     for _ in range(warmup):
@@ -228,6 +233,8 @@ def _time_variant(torch, ra, h, ins, outs, steps, warmup, per_launch=True):
         if per_launch else []
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    if queued:
+        torch.cuda._sleep(int(1e6 + 40000 * steps))   # ~20 us of SM cycles per call to enqueue
     t0.record(stream)
     for i in range(steps):
         if per_launch:
@@ -661,6 +668,7 @@ SWEEP_VARIANTS = [
     ("persistent_per_peer", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
     ("persistent_cluster", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
     ("pipelined", "pipelined", lambda ra: []),
+    ("pipelined_ll", "pipelined", lambda ra: [(ra.Option.PROTOCOL, ra.Protocol.LL)]),
     ("local", "local", lambda ra: []),
 ]
 
@@ -683,7 +691,8 @@ def run_barriers(args):
         for name, v, opts in (("counting", "persistent", []),
                               ("per_peer", "persistent", [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
                               ("cluster", "persistent", [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
-                              ("pipelined", "pipelined", [])):
+                              ("pipelined", "pipelined", []),
+                              ("pipelined_ll", "pipelined", [(ra.Option.PROTOCOL, ra.Protocol.LL)])):
             if name == "cluster" and R > 16:
                 line[name] = None
                 continue
@@ -692,10 +701,11 @@ def run_barriers(args):
             for key, value in opts:
                 h.set_option(key, value)
             _, lm = _time_variant(torch, ra, h, ins, outs, 500, 20)
+            _, lq = _time_variant(torch, ra, h, ins, outs, 300, 5, queued=True)
             assert h.device_status()[0] == ra.Status.OK
             h.close()
-            t = statistics.median(lm)
-            line[name] = {"us_per_call": round(t * 1e3, 2)}
+            line[name] = {"us_per_call": round(statistics.median(lm) * 1e3, 2),
+                          "device_us": round(statistics.median(lq) * 1e3, 2)}
         print(json.dumps(line), flush=True)
 
 
@@ -799,13 +809,30 @@ def run_sweep(args):
             for key, value in opts(ra):
                 h.set_option(key, value)
             steps = 200 if n <= 2**20 else 30
-            _, lm = _time_variant(torch, ra, h, ins, outs, steps, 10)
+            try:
+                _, lm = _time_variant(torch, ra, h, ins, outs, steps, 10)
+            except ra.RAError as e:
+                # flag-in-data messages are for small chunks: above its inbox
+                # limit the call is refused before any launch
+                assert e.status == ra.Status.ERR_UNSUPPORTED, e
+                h.close()
+                line[name] = None
+                continue
             assert h.device_status()[0] == ra.Status.OK
             h.close()
             t = statistics.median(lm) / 1e3
             line[name] = {"us": round(t * 1e6, 2), "algbw": round(n * 4 / t / 1e9, 2),
                        "busbw": round(n * 4 / t / 1e9 * 2 * (R - 1) / R, 2),
                        "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
+            if n <= 2**20:
+                # small calls: also their device time, issued back to back
+                h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
+                for key, value in opts(ra):
+                    h.set_option(key, value)
+                _, lq = _time_variant(torch, ra, h, ins, outs, 200, 5, queued=True)
+                assert h.device_status()[0] == ra.Status.OK
+                h.close()
+                line[name]["device_us"] = round(statistics.median(lq) * 1e3, 2)
         # reference, not a variant: a plain device copy (torch) of the same
         # R n b bytes read and written, timed the same way -- what a copy
         # reaches at this size
@@ -824,6 +851,15 @@ def run_sweep(args):
         t = statistics.median([a.elapsed_time(bb) for a, bb in ev]) / 1e3
         line["copy_same_bytes"] = {"us": round(t * 1e6, 2),
                                    "frac_compulsory": round(2 * R * n * 4 / t / 1e9 / peak, 4)}
+        if n <= 2**20:
+            torch.cuda._sleep(int(1e6 + 40000 * steps))
+            for a, bb in ev:
+                a.record()
+                dst.copy_(src)
+                bb.record()
+            torch.cuda.synchronize()
+            line["copy_same_bytes"]["device_us"] = round(
+                statistics.median([a.elapsed_time(bb) for a, bb in ev]) * 1e3, 2)
         print(json.dumps(line), flush=True)
         del ins, outs, src, dst
         torch.cuda.empty_cache()

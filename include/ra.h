@@ -116,7 +116,13 @@ typedef enum ra_variant {
                                  sub-slice as soon as its predecessor has
                                  finished the previous round on it
                                  (per-predecessor progress flags; rounds of
-                                 different sub-slices overlap) */
+                                 different sub-slices overlap; RA_OPT_PROTOCOL
+                                 chooses how the messages travel).  Not
+                                 capturable into a CUDA graph: each call
+                                 passes the kernel where its flags start, and
+                                 a replay would reuse that value
+                                 (RA_ERR_UNSUPPORTED while the stream
+                                 captures) */
   RA_VARIANT_LOCAL = 5        /* one launch, each CTA running every ring round
                                  for one slice of every chunk: the ranks'
                                  messages pass through shared memory, the
@@ -133,12 +139,36 @@ typedef enum ra_barrier {
                                  barrier a counting barrier", section "Fix") */
   RA_BARRIER_PER_PEER = 1,    /* one signal per (channel, round, waiter, peer),
                                  the design that page replaced; a wait that runs
-                                 out can name the missing peer */
+                                 out can name the missing peer.  Each call
+                                 passes the kernel its epoch, so it is not
+                                 capturable into a CUDA graph
+                                 (RA_ERR_UNSUPPORTED while the stream
+                                 captures) */
   RA_BARRIER_CLUSTER = 2      /* the R CTAs of a channel form one thread-block
                                  cluster and meet at the hardware cluster
                                  barrier (R <= 16, else RA_ERR_UNSUPPORTED);
                                  no signal memory, no cooperative launch */
 } ra_barrier;
+
+/* How the pipelined variant's messages travel (RA_OPT_PROTOCOL). */
+typedef enum ra_protocol {
+  RA_PROTOCOL_SIMPLE = 0,     /* a rank's partial goes to its output buffer,
+                                 then a progress flag is published (a release
+                                 fence and a SignalAdd) that the successor
+                                 polls before reading the partial */
+  RA_PROTOCOL_LL = 1          /* flag-in-data messages for small chunks: each
+                                 8-byte word carries 32 bits of data and a
+                                 32-bit flag naming the call and the round,
+                                 written by one store into the successor's row
+                                 of an inbox the handle allocates on first use
+                                 ((2R-3) x R x C x w words of 8 bytes, w = 2
+                                 for 8-byte elements, else 1; at most 64 MiB,
+                                 else RA_ERR_UNSUPPORTED); the successor polls
+                                 the words themselves, so a ring hop is one
+                                 store and one poll, with no fence and no
+                                 separate flag.  Twice the bytes per element
+                                 (four times for 16-bit elements). */
+} ra_protocol;
 
 typedef enum ra_option {
   RA_OPT_VARIANT = 1,        /* ra_variant, default RA_VARIANT_AUTO */
@@ -205,6 +235,21 @@ typedef enum ra_option {
                                 article's waitSignal(..., bits) does; a device
                                 whose signals are 56-bit counters would use 56.
                                 ra_read_signals returns the low bits too. */
+  RA_OPT_PROTOCOL = 15,      /* ra_protocol of the pipelined variant, default
+                                RA_PROTOCOL_SIMPLE.  With RA_PROTOCOL_LL,
+                                RA_OPT_CTAS is the channels per rank (0:
+                                chosen), RA_OPT_SKIP_ARRIVAL names a rank that
+                                sends nothing from that round on, and
+                                RA_OPT_SLICES, RA_OPT_WINDOW and
+                                RA_OPT_SIGNAL_BITS do not apply. */
+  RA_OPT_LL_FLAG = 16,       /* the flag the next RA_PROTOCOL_LL call's first
+                                message carries, 1..2^32-1 (1 after creation).
+                                Each call moves it on by its ring rounds; a
+                                call whose flags would pass 2^32-1 first
+                                zeroes the inbox and starts again at 1, so no
+                                word left in the inbox ever carries a flag
+                                being waited for.  Setting it is for tests of
+                                that restart. */
   RA_OPT_DEBUG_SHRINK = 11   /* bounds-checked builds only (see
                                 ra_debug_bounds_report): register each of the
                                 call's buffers this many bytes shorter than it
@@ -217,14 +262,17 @@ typedef enum ra_option {
 typedef struct ra_device_error {
   uint32_t code;      /* 0 = none; 1 = counting-barrier wait ran out; 2 = bulk-copy wait
                          ran out; 3 = per-peer barrier wait ran out; 4 = pipelined
-                         flag wait ran out */
-  int32_t round;      /* barrier round (0-based), ring round (code 4) or AllGather round (code 2) */
+                         flag wait ran out; 5 = RA_PROTOCOL_LL message wait ran
+                         out */
+  int32_t round;      /* barrier round (0-based), ring round (codes 4, 5) or AllGather round (code 2) */
   int32_t rank;       /* waiting rank */
   int32_t channel;    /* channel: the CTA index within its rank */
-  int32_t peer;       /* rank that did not arrive when it can be named (codes 3, 4), else -1 */
+  int32_t peer;       /* rank that did not arrive when it can be named (codes 3, 4, 5), else -1 */
   int32_t reserved;
-  uint64_t observed;  /* arrivals (codes 1, 3) or progress (code 4) seen last */
-  uint64_t expected;  /* what was waited for: expected - observed were missing */
+  uint64_t observed;  /* arrivals (codes 1, 3), progress (code 4) or a message word's flag
+                         (code 5) seen last */
+  uint64_t expected;  /* what was waited for (codes 1-4: expected - observed were missing;
+                         code 5: the flag of the awaited message) */
 } ra_device_error;
 
 typedef struct ra_ctx* ra_handle;

@@ -14,7 +14,7 @@ import os
 from . import build as _build
 
 __all__ = [
-    "Status", "DType", "Op", "Variant", "Barrier", "Option", "DeviceError", "RAError",
+    "Status", "DType", "Op", "Variant", "Barrier", "Protocol", "Option", "DeviceError", "RAError",
     "load_library", "library_path", "ra_create", "ra_destroy", "ra_reduce_scatter",
     "ra_all_gather", "ra_allreduce", "ra_allreduce_host", "ra_reduce_scatter_compact", "ra_all_gather_compact", "ra_chunk_plan", "ra_owned_chunk", "ra_set_option",
     "ra_get_option", "ra_get_device_status", "ra_read_signals", "ra_read_shadows", "ra_seed_signals",
@@ -63,6 +63,11 @@ class Barrier(enum.IntEnum):
     CLUSTER = 2
 
 
+class Protocol(enum.IntEnum):
+    SIMPLE = 0
+    LL = 1
+
+
 class Option(enum.IntEnum):
     VARIANT = 1
     TIMEOUT_NS = 2
@@ -77,6 +82,8 @@ class Option(enum.IntEnum):
     DEBUG_SHRINK = 11
     WINDOW = 12
     SIGNAL_BITS = 14
+    PROTOCOL = 15
+    LL_FLAG = 16
 
 
 class DeviceError(ctypes.Structure):

@@ -29,7 +29,7 @@ DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
 DEBUG_LIB_PATH = os.path.join(HERE, "libra_gb300_debug.so")
 
 SOURCES = ["ra_host.cpp", "ra_direct.cu", "ra_round.cu", "ra_persistent.cu", "ra_pipelined.cu", "ra_compact.cu",
-           "ra_bcast.cu", "ra_static.cu", "ra_local.cu"]
+           "ra_bcast.cu", "ra_static.cu", "ra_local.cu", "ra_ll.cu"]
 # (source, object stem, preprocessor definitions): ra_direct_inst.cu is
 # compiled once per dtype so its instantiations build in parallel
 DTYPES = ["RA_F32", "RA_BF16", "RA_I32", "RA_F16", "RA_F64", "RA_I64"]
@@ -64,6 +64,7 @@ KERNEL_SOURCES = {
     "compact": ["ra_compact.cu", "ra_device.cuh", "ra_internal.h"],
     "bcast": ["ra_bcast.cu", "ra_device.cuh", "ra_internal.h"],
     "local": ["ra_local.cu", "ra_device.cuh", "ra_internal.h"],
+    "ll": ["ra_ll.cu", "ra_ll.h", "ra_device.cuh", "ra_internal.h"],
 }
 
 

@@ -16,6 +16,7 @@
 
 #include "ra.h"
 #include "ra_internal.h"
+#include "ra_ll.h"
 
 namespace {
 
@@ -106,6 +107,13 @@ struct ra_ctx {
   int variant = RA_VARIANT_AUTO;
   long long timeout_ns = 1000000000LL;
   int signal_bits = 64;   // RA_OPT_SIGNAL_BITS
+  int protocol = RA_PROTOCOL_SIMPLE;   // RA_OPT_PROTOCOL
+  int ll_blocks_per_sm = 0;
+  // RA_PROTOCOL_LL: the inbox (allocated on first use) and the flag the next
+  // call's first message carries
+  uint64_t* ll_inbox = nullptr;
+  size_t ll_inbox_words = 0;
+  uint64_t ll_flag = 1;
   int ctas = 0;
   int check_pointers = 1;
   long long skip = -1;
@@ -677,6 +685,7 @@ void debug_begin(const ra_ctx* h) {
     for (auto& reg : row)
       if (reg.d) debug_add(reg.d, region_words(reg) * sizeof(uint64_t));
   debug_add(h->d_err, sizeof(ra_device_error));
+  if (h->ll_inbox) debug_add(h->ll_inbox, h->ll_inbox_words * sizeof(uint64_t));
   if (h->host_dev) debug_add(h->host_dev, 4 * (size_t)h->R * h->host_n_pad * elem_bytes(h->dtype));
 }
 
@@ -766,12 +775,29 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "cluster kernel launch");
 }
 
+// Launches whose per-call state the host passes in as a kernel parameter
+// (the per-peer barrier's epoch, the pipelined variant's shadow start and
+// message flags) would replay that value unchanged from a CUDA graph, and a
+// replay would take an earlier call's progress for its own: they refuse a
+// stream that is being captured.
+ra_status refuse_capture(cudaStream_t st, const char* what) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "stream capture status");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(RA_ERR_UNSUPPORTED, "%s cannot be captured into a CUDA graph (its per-call state comes from the host)",
+                what);
+  return RA_OK;
+}
+
 ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                          cudaStream_t st) {
   if (h->barrier == RA_BARRIER_CLUSTER) return run_persistent_cluster(h, kind, mode, in, out, st);
   const int sync = h->barrier == RA_BARRIER_PER_PEER ? ra::kSyncPerPeer : ra::kSyncCounting;
+  ra_status s = sync == ra::kSyncPerPeer ? refuse_capture(st, "the per-peer barrier") : RA_OK;
+  if (s != RA_OK) return s;
   SlotRegion* reg = nullptr;
-  ra_status s = ensure_region(h, sync, kind, &reg);
+  s = ensure_region(h, sync, kind, &reg);
   if (s != RA_OK) return s;
   ra::PersistArgs a;
   a.p = make_ptrs(h, in, out);
@@ -815,10 +841,80 @@ int pipeline_window(const ra_ctx* h, int J) {
   return 1;
 }
 
+constexpr size_t kLLInboxBytes = (size_t)64 << 20;   // most bytes of the RA_PROTOCOL_LL inbox
+
+// The pipelined variant with flag-in-data messages (ra_ll.cu).
+ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
+                           cudaStream_t st) {
+  ra::LLArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.rounds = h->region[ra::kSyncFlags][kind].rounds;
+  const int64_t C = a.plan.C;
+  const int wpe = ra::ll_words_per_element((int)elem_bytes(h->dtype));
+  // rows: the most messages a call sends (AllReduce: 2R-3) x receiving ranks
+  const size_t words = (size_t)(2 * h->R - 3) * (size_t)h->R * (size_t)C * (size_t)wpe;
+  if (words > kLLInboxBytes / sizeof(uint64_t))
+    return fail(RA_ERR_UNSUPPORTED, "LL protocol: chunks of %lld elements need a %zu-byte inbox (at most %zu)",
+                (long long)C, words * sizeof(uint64_t), kLLInboxBytes);
+  // threads per CTA, positions per thread (E) and channels (G): one position
+  // per thread while the channels can be co-resident
+  const int threads = (int)std::min<int64_t>(ra::kLLThreads, std::max<int64_t>(32, (C + 31) / 32 * 32));
+  const int cap = h->ll_blocks_per_sm * h->num_sms;
+  if (h->ctas > 0) {
+    a.G = h->ctas;
+    a.E = (int)std::max<int64_t>(1, (C + (int64_t)a.G * threads - 1) / ((int64_t)a.G * threads));
+  } else {
+    const int64_t gmax = std::max(1, cap / h->R);
+    a.E = (int)std::max<int64_t>(1, (C + gmax * threads - 1) / (gmax * threads));
+    a.G = (int)std::max<int64_t>(1, (C + (int64_t)threads * a.E - 1) / ((int64_t)threads * a.E));
+  }
+  if (a.E > ra::kLLMaxE)
+    return fail(RA_ERR_UNSUPPORTED, "LL protocol: %d channels of %d threads cannot carry %lld-element chunks", a.G,
+                threads, (long long)C);
+  if ((long long)a.G * h->R > cap)
+    return fail(RA_ERR_UNSUPPORTED, "LL grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
+  if (!h->ll_inbox) {
+    cudaError_t e = cudaMalloc(&h->ll_inbox, words * sizeof(uint64_t));
+    if (e == cudaSuccess) e = cudaMemset(h->ll_inbox, 0, words * sizeof(uint64_t));
+    if (e != cudaSuccess) {
+      if (h->ll_inbox) cudaFree(h->ll_inbox);
+      h->ll_inbox = nullptr;
+      return cuda_fail(e, "LL inbox allocation");
+    }
+    h->ll_inbox_words = words;
+    h->ll_flag = 1;
+    debug_add(h->ll_inbox, words * sizeof(uint64_t));
+  }
+  // flags never wrap: a call whose flags would pass 2^32 - 1 starts again
+  // at 1 on a zeroed inbox (0 marks a word never written)
+  if (h->ll_flag + (uint64_t)a.rounds > 0xFFFFFFFFull) {
+    const cudaError_t e = cudaMemsetAsync(h->ll_inbox, 0, h->ll_inbox_words * sizeof(uint64_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "LL inbox reset");
+    h->ll_flag = 1;
+  }
+  a.inbox = h->ll_inbox;
+  a.flag_base = (uint32_t)h->ll_flag;
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
+  a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
+  const cudaError_t e = ra::launch_ll(h->dtype, h->op, a, threads, st);
+  if (e != cudaSuccess) return cuda_fail(e, "LL kernel launch");
+  h->ll_flag += (uint64_t)a.rounds;
+  return RA_OK;
+}
+
 ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                         cudaStream_t st) {
+  ra_status s = refuse_capture(st, "the pipelined variant");
+  if (s != RA_OK) return s;
+  if (h->protocol == RA_PROTOCOL_LL) return run_pipelined_ll(h, kind, mode, in, out, st);
   SlotRegion* reg = nullptr;
-  ra_status s = ensure_region(h, ra::kSyncFlags, kind, &reg);
+  s = ensure_region(h, ra::kSyncFlags, kind, &reg);
   if (s != RA_OK) return s;
   ra::PersistArgs a;
   a.p = make_ptrs(h, in, out);
@@ -925,9 +1021,10 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   int coop = 0;
   e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  int bps = 0, pbps = 0;
+  int bps = 0, pbps = 0, llbps = 0;
   e = ra::persistent_blocks_per_sm(dtype, op, ra::kPersistThreads, &bps);
   if (e == cudaSuccess) e = ra::pipelined_blocks_per_sm(dtype, op, ra::kPipeThreads, &pbps);
+  if (e == cudaSuccess) e = ra::ll_blocks_per_sm(dtype, op, ra::kLLThreads, &llbps);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   e = ra::prepare_ag_round();
   if (e == cudaSuccess) e = ra::prepare_bcast();
@@ -953,6 +1050,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   h->use_graphs = 0;   // the bounds table is uploaded before every launch
 #endif
   h->pipe_blocks_per_sm = coop ? pbps : 0;
+  h->ll_blocks_per_sm = coop ? llbps : 0;
   h->local_blocks_per_sm = lbps;
 
   // counting-barrier slots: per kind, the most channels that can be
@@ -1011,6 +1109,7 @@ ra_status ra_destroy(ra_handle h) {
       if (reg.owned && reg.d) cudaFree(reg.d);
   if (h->d_slots) cudaFree(h->d_slots);
   if (h->d_err) cudaFree(h->d_err);
+  if (h->ll_inbox) cudaFree(h->ll_inbox);
   if (h->host_dev) cudaFree(h->host_dev);
   if (h->host_s_in) cudaStreamDestroy(h->host_s_in);
   if (h->host_s_out) cudaStreamDestroy(h->host_s_out);
@@ -1350,6 +1449,17 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       if (value < 0 || value > kMaxSlices) return fail(RA_ERR_INVALID, "window %lld outside [0, %d]", value, kMaxSlices);
       h->window = (int)value;
       return RA_OK;
+    case RA_OPT_PROTOCOL:
+      if (value != RA_PROTOCOL_SIMPLE && value != RA_PROTOCOL_LL)
+        return fail(RA_ERR_INVALID, "unknown protocol %lld", value);
+      if (value == RA_PROTOCOL_LL && h->ll_blocks_per_sm == 0)
+        return fail(RA_ERR_UNSUPPORTED, "device has no cooperative launch");
+      h->protocol = (int)value;
+      return RA_OK;
+    case RA_OPT_LL_FLAG:
+      if (value < 1 || value > 0xFFFFFFFFLL) return fail(RA_ERR_INVALID, "LL flag %lld outside [1, 2^32-1]", value);
+      h->ll_flag = (uint64_t)value;
+      return RA_OK;
     case RA_OPT_SIGNAL_BITS:
       if (value < 16 || value > 64) return fail(RA_ERR_INVALID, "signal bits %lld outside [16, 64]", value);
       h->signal_bits = (int)value;
@@ -1396,6 +1506,8 @@ ra_status ra_get_option(ra_handle h, int key, long long* value) {
     case RA_OPT_SLICES: *value = h->slices; return RA_OK;
     case RA_OPT_WINDOW: *value = h->window; return RA_OK;
     case RA_OPT_SIGNAL_BITS: *value = h->signal_bits; return RA_OK;
+    case RA_OPT_PROTOCOL: *value = h->protocol; return RA_OK;
+    case RA_OPT_LL_FLAG: *value = (long long)h->ll_flag; return RA_OK;
     case RA_OPT_GATHER: *value = h->gather; return RA_OK;
     case RA_OPT_HOST_WINDOWS: *value = h->host_windows; return RA_OK;
     case RA_OPT_DEBUG_SHRINK: *value = h->debug_shrink; return RA_OK;
@@ -1437,6 +1549,12 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) 
   if (rec.code == 0) return RA_OK;
   ra_status s = reset_device_state(h, st);
   if (s != RA_OK) return s;
+  if (rec.code == 5)
+    return fail(RA_ERR_TIMEOUT,
+                "device wait gave up: LL message, round %d, rank %d, channel %d, peer %d, flag observed %llu, "
+                "expected %llu",
+                rec.round, rec.rank, rec.channel, rec.peer, (unsigned long long)rec.observed,
+                (unsigned long long)rec.expected);
   const char* what = rec.code == 1 ? "counting barrier"
                      : rec.code == 2 ? "bulk copy"
                      : rec.code == 3 ? "per-peer barrier"

@@ -127,6 +127,11 @@ def main():
             run(R, n, "f32", "sum", "persistent", "allreduce", options=[(ra.Option.BARRIER, ra.Barrier.CLUSTER)])
         run(R, n, "f32", "sum", "pipelined", "allreduce", options=[(ra.Option.SLICES, 3)])
         run(R, n, "bf16", "sum", "pipelined", "allreduce", options=[(ra.Option.SLICES, 5), (ra.Option.WINDOW, 2)])
+        # flag-in-data messages: the inbox rows and the positions past a ragged chunk's end
+        for kind in ("allreduce", "reduce_scatter", "all_gather"):
+            run(R, n, "bf16", "sum", "pipelined", kind, options=[(ra.Option.PROTOCOL, ra.Protocol.LL)])
+        run(R, n, "f64", "sum", "pipelined", "allreduce", options=[(ra.Option.PROTOCOL, ra.Protocol.LL)])
+        calls += 4
         # passes: every round on one part of every chunk (slice) before the next part
         for kind in ("allreduce", "reduce_scatter", "all_gather"):
             run(R, n, "bf16", "sum", "ring", kind, options=[(ra.Option.SLICES, 3)])

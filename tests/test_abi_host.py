@@ -89,3 +89,18 @@ def test_null_handle_calls_are_rejected(lib):
 def test_status_strings(lib):
     for s in lib.Status:
         assert lib.ra_status_string(s) == "RA_" + s.name
+
+
+def _header_enum(prefix):
+    """{NAME: value} of the enumerators of ra.h that start with `prefix`."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(rf"\b{prefix}(\w+)\s*=\s*(\d+)", text)}
+
+
+@pytest.mark.parametrize("prefix,cls", [("RA_OPT_", "Option"), ("RA_VARIANT_", "Variant"),
+                                        ("RA_BARRIER_", "Barrier"), ("RA_PROTOCOL_", "Protocol")])
+def test_binding_enums_match_the_header(lib, prefix, cls):
+    want = _header_enum(prefix)
+    assert want, prefix
+    got = {e.name: int(e) for e in getattr(lib, cls)}
+    assert got == want

@@ -1,0 +1,267 @@
+"""The pipelined variant with flag-in-data messages (RA_PROTOCOL_LL) against
+the oracle, bitwise, through the C ABI: every dtype and op, the three
+collectives, in place, launch shapes, calls that follow one another on one
+inbox, the restart of the flags before they would wrap, a withheld message
+that must time out rather than be taken from an earlier call's words, and
+the inbox limit."""
+
+import numpy as np
+import pytest
+
+from oracle import elementops, ring
+from ring_allreduce_gb300 import inputs
+from rahelpers import DeviceRanks, assert_bitwise_equal
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+DTYPE_OPS = [("f32", "sum"), ("f32", "max"), ("bf16", "sum"), ("bf16", "max"),
+             ("i32", "sum"), ("i32", "max"), ("f16", "sum"), ("f16", "max"),
+             ("f64", "sum"), ("f64", "max"), ("i64", "sum"), ("i64", "max")]
+# (R, n): degenerate, n < R, ragged tails, chunks of one CTA and of several
+SHAPES = [(2, 1), (3, 2), (4, 4096), (5, 1001), (8, 1024), (8, 8 * 1024 + 13), (13, 7777), (16, 2**14 + 3),
+          (32, 4097), (8, 2**16 + 5)]
+
+
+@pytest.fixture(scope="module")
+def ra():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_allreduce_gb300 import build
+    build.build()
+    from ring_allreduce_gb300 import binding
+    return binding
+
+
+def _dist(dtype):
+    return {"f32": "normal", "bf16": "grad", "i32": "int20", "f16": "grad", "f64": "normal", "i64": "int40"}[dtype]
+
+
+def _run(ra, h, kind, inp, out):
+    if kind == "allreduce":
+        h.allreduce(inp.views, out.views)
+    elif kind == "reduce_scatter":
+        h.reduce_scatter(inp.views, out.views)
+    else:
+        h.all_gather(inp.views)
+
+
+def run_ll(ra, x, dtype, op, kind="allreduce", inplace=False, ctas=0):
+    R, n = len(x), len(x[0])
+    st = inputs.storage_dtype(dtype)
+    inp = DeviceRanks(R, n, st, host=x)
+    out = inp if inplace else DeviceRanks(R, n, st)
+    with ra.RingAllReduce(R, n, dtype, op, variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        if ctas:
+            h.set_option(ra.Option.CTAS, ctas)
+        _run(ra, h, kind, inp, out)
+        status, err = h.device_status()
+        assert status == ra.Status.OK, err.as_dict()
+    torch.cuda.synchronize()
+    assert inp.guards_intact(), "write outside an input buffer"
+    assert out.guards_intact(), "write outside an output buffer"
+    return out.host()
+
+
+def _owned(R, n, got, want, what):
+    plan = ring.chunk_plan(R, n)
+    for r in range(R):
+        off, L = plan[ring.owned_chunk(R, r)]
+        assert_bitwise_equal(got[r][off:off + L], want[r][off:off + L], f"{what} rank {r}")
+
+
+@pytest.mark.parametrize("dtype,op", DTYPE_OPS)
+def test_ll_allreduce_matches_oracle(ra, dtype, op):
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=700 + i)
+        want = ring.ring_allreduce(x, o)
+        got = run_ll(ra, x, dtype, op)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"LL {dtype}/{op} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "sum"), ("i32", "max"), ("f16", "sum"),
+                                      ("f64", "sum"), ("i64", "max")])
+def test_ll_reduce_scatter_owned_chunk(ra, dtype, op):
+    o = elementops.get_op(dtype, op)
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=800 + i)
+        _owned(R, n, run_ll(ra, x, dtype, op, kind="reduce_scatter"), ring.ring_reduce_scatter(x, o),
+               f"LL RS {dtype} R={R} n={n}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16", "f64", "i64"])
+def test_ll_all_gather_from_reduce_scatter_layout(ra, dtype):
+    """Only chunk (r+1) of buf[r] matters; the junk elsewhere is overwritten."""
+    o = elementops.get_op(dtype, "sum")
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, dtype, _dist(dtype), seed=900 + i)
+        rs = ring.ring_reduce_scatter(x, o)
+        junk = inputs.generate(R, n, dtype, _dist(dtype), seed=999)
+        plan = ring.chunk_plan(R, n)
+        buf = []
+        for r in range(R):
+            b = junk[r].copy()
+            off, L = plan[ring.owned_chunk(R, r)]
+            b[off:off + L] = rs[r][off:off + L]
+            buf.append(b)
+        want = ring.ring_all_gather(buf, o)
+        got = run_ll(ra, buf, dtype, "sum", kind="all_gather", inplace=True)
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"LL AG {dtype} R={R} n={n} rank {r}")
+
+
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter"])
+def test_ll_in_place(ra, kind):
+    o = elementops.get_op("f32", "sum")
+    for i, (R, n) in enumerate(SHAPES):
+        x = inputs.generate(R, n, "f32", "normal", seed=1000 + i)
+        got = run_ll(ra, x, "f32", "sum", kind=kind, inplace=True)
+        if kind == "allreduce":
+            want = ring.ring_allreduce(x, o)
+            for r in range(R):
+                assert_bitwise_equal(got[r], want[r], f"LL in place R={R} n={n}")
+        else:
+            _owned(R, n, got, ring.ring_reduce_scatter(x, o), f"LL RS in place R={R} n={n}")
+
+
+@pytest.mark.parametrize("R,n,ctas", [(8, 1000, 1), (8, 8 * 1024 + 13, 3), (4, 4096, 64), (5, 5 * 4 * 256, 1)])
+def test_ll_launch_shapes(ra, R, n, ctas):
+    """Channels given: one CTA carries up to 4 positions per thread (n = 1000
+    and 5120 at one channel); 64 channels leave most threads without a
+    position."""
+    x = inputs.generate(R, n, "bf16", "grad", seed=11 + ctas)
+    want = ring.ring_allreduce(x, elementops.get_op("bf16", "sum"))
+    got = run_ll(ra, x, "bf16", "sum", ctas=ctas)
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r], f"LL ctas={ctas} R={R} n={n} rank {r}")
+
+
+def test_ll_too_few_channels_is_unsupported(ra):
+    # chunks of 4101 elements: more than 4 channels of 256 threads carry at
+    # 4 positions per thread (4096)
+    R, n = 8, 8 * 4101
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        h.set_option(ra.Option.CTAS, 4)
+        inp, out = DeviceRanks(R, n, np.float32), DeviceRanks(R, n, np.float32)
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.views, out.views)
+        assert e.value.status == ra.Status.ERR_UNSUPPORTED
+
+
+def test_ll_calls_in_a_row_and_mixed_collectives(ra):
+    """One handle, one inbox: AllReduce, ReduceScatter, AllGather and
+    AllReduce again on other inputs.  Every call's flags are new, so no word
+    an earlier call left behind is taken for this call's message."""
+    R, n = 6, 6 * 777 + 5
+    o = elementops.get_op("f32", "sum")
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        flag0 = h.get_option(ra.Option.LL_FLAG)
+        assert flag0 == 1
+        for seed, kind in enumerate(["allreduce", "allreduce", "reduce_scatter", "all_gather", "allreduce"]):
+            x = inputs.generate(R, n, "f32", "normal", seed=40 + seed)
+            inp, out = DeviceRanks(R, n, np.float32, host=x), DeviceRanks(R, n, np.float32)
+            _run(ra, h, kind, inp, out)
+            status, err = h.device_status()
+            assert status == ra.Status.OK, err.as_dict()
+            if kind == "allreduce":
+                want, got = ring.ring_allreduce(x, o), out.host()
+                for r in range(R):
+                    assert_bitwise_equal(got[r], want[r], f"call {seed} rank {r}")
+            elif kind == "reduce_scatter":
+                _owned(R, n, out.host(), ring.ring_reduce_scatter(x, o), f"call {seed}")
+            else:
+                want, got = ring.ring_all_gather(x, o), inp.host()
+                for r in range(R):
+                    assert_bitwise_equal(got[r], want[r], f"AG call {seed} rank {r}")
+        rounds = 2 * (R - 1)
+        assert h.get_option(ra.Option.LL_FLAG) == flag0 + 3 * rounds + 2 * (R - 1)
+
+
+def test_ll_flags_restart_before_they_wrap(ra):
+    """A call whose flags would pass 2^32 - 1 zeroes the inbox and starts
+    again at 1; the call whose last message carries 2^32 - 3 (and leaves
+    2^32 - 1 for the next) does not."""
+    R, n = 4, 4 * 1500 + 3
+    rounds = 2 * (R - 1)
+    o = elementops.get_op("i32", "sum")
+    with ra.RingAllReduce(R, n, "i32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        for bad in (0, 2**32):
+            with pytest.raises(ra.RAError):
+                h.set_option(ra.Option.LL_FLAG, bad)
+        x = inputs.generate(R, n, "i32", "int20", seed=3)
+        inp, out = DeviceRanks(R, n, np.int32, host=x), DeviceRanks(R, n, np.int32)
+        want = ring.ring_allreduce(x, o)
+        h.allreduce(inp.views, out.views)           # fills the inbox with low flags
+        start = 2**32 - 1 - rounds                  # messages carry start .. 2^32 - 3
+        h.set_option(ra.Option.LL_FLAG, start)
+        for expect_after in (2**32 - 1, 1 + rounds, 1 + 2 * rounds):
+            out = DeviceRanks(R, n, np.int32)
+            h.allreduce(inp.views, out.views)
+            status, err = h.device_status()
+            assert status == ra.Status.OK, err.as_dict()
+            assert h.get_option(ra.Option.LL_FLAG) == expect_after
+            got = out.host()
+            for r in range(R):
+                assert_bitwise_equal(got[r], want[r], f"flag {expect_after} rank {r}")
+
+
+def test_ll_withheld_message_times_out(ra):
+    """After a good call has filled the inbox, a rank that sends nothing from
+    the next-to-last round on leaves exactly its successor waiting in the
+    last round -- on a word that holds the previous call's message, whose
+    flag is the awaited one less the call's rounds.  The next call is
+    correct."""
+    R, n = 4, 4 * 4096
+    rounds = 2 * (R - 1)
+    x = inputs.generate(R, n, "f32", "normal", 8)
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    inp = DeviceRanks(R, n, np.float32, host=x)
+    out = DeviceRanks(R, n, np.float32)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        h.set_option(ra.Option.TIMEOUT_NS, 20_000_000)
+        h.allreduce(inp.views, out.views)
+        assert h.device_status()[0] == ra.Status.OK
+        h.set_option(ra.Option.SKIP_ARRIVAL, (2 << 16) | (rounds - 2))
+        h.allreduce(inp.views, out.views)
+        status, err = h.device_status()
+        assert status == ra.Status.ERR_TIMEOUT
+        assert err.code == 5 and err.rank == 3 and err.peer == 2 and err.round == rounds - 1, err.as_dict()
+        assert err.expected == 1 + rounds + (rounds - 2)
+        assert err.observed == err.expected - rounds
+        assert "LL message" in ra.ra_last_error()
+        h.set_option(ra.Option.SKIP_ARRIVAL, -1)
+        out = DeviceRanks(R, n, np.float32)
+        h.allreduce(inp.views, out.views)
+        assert h.device_status()[0] == ra.Status.OK
+    got = out.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
+
+
+def test_ll_inbox_limit(ra):
+    """(2R-3) x R x C words of 8 bytes at most 64 MiB: R = 32 with 2^22
+    elements per rank needs more and is refused before any launch."""
+    R, n = 32, 2**22
+    with ra.RingAllReduce(R, n, "f32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        inp = DeviceRanks(R, n, np.float32)
+        with pytest.raises(ra.RAError) as e:
+            h.allreduce(inp.views, inp.views)
+        assert e.value.status == ra.Status.ERR_UNSUPPORTED
+        assert "inbox" in ra.ra_last_error()
+
+
+def test_protocol_option_values(ra):
+    with ra.RingAllReduce(4, 1024, "f32", "sum") as h:
+        assert h.get_option(ra.Option.PROTOCOL) == ra.Protocol.SIMPLE
+        with pytest.raises(ra.RAError) as e:
+            h.set_option(ra.Option.PROTOCOL, 2)
+        assert e.value.status == ra.Status.ERR_INVALID
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        assert h.get_option(ra.Option.PROTOCOL) == ra.Protocol.LL

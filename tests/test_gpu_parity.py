@@ -403,15 +403,20 @@ def test_ring_graph_replay_and_rebuild(ra, kind):
             assert outs[out].guards_intact()
 
 
-@pytest.mark.parametrize("variant", ["direct", "ring"])
-def test_calls_inside_a_caller_graph(ra, variant):
+@pytest.mark.parametrize("variant,options", [("direct", ()), ("ring", ()), ("persistent", ()),
+                                             ("persistent", (("BARRIER", "CLUSTER"),)), ("local", ())])
+def test_calls_inside_a_caller_graph(ra, variant, options):
     """A caller may capture ra_allreduce into its own CUDA graph (after one
-    call on the same buffers outside it) and replay it on new data."""
+    call on the same buffers outside it) and replay it on new data, several
+    times: the counting barrier keeps its waiters' shadows in device memory,
+    so every replay moves them on."""
     R, n = 4, 100003
     o = elementops.get_op("f32", "sum")
     inp = DeviceRanks(R, n, np.float32, host=inputs.generate(R, n, "f32", "normal", 1))
     out = DeviceRanks(R, n, np.float32)
     h = ra.RingAllReduce(R, n, "f32", "sum", variant=variant)
+    for key, value in options:
+        h.set_option(ra.Option[key], ra.Barrier[value])
     try:
         side = torch.cuda.Stream()
         with torch.cuda.stream(side):
@@ -420,7 +425,7 @@ def test_calls_inside_a_caller_graph(ra, variant):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
             h.allreduce(inp.views, out.views, side)
-        for seed in (7, 8):
+        for seed in (7, 8, 9):
             x = inputs.generate(R, n, "f32", "normal", seed)
             inp.big.copy_(DeviceRanks(R, n, np.float32, host=x).big)
             g.replay()
@@ -433,6 +438,37 @@ def test_calls_inside_a_caller_graph(ra, variant):
     finally:
         h.close()
 
+
+
+@pytest.mark.parametrize("variant,key,value", [("pipelined", None, None), ("pipelined", "PROTOCOL", "LL"),
+                                               ("persistent", "BARRIER", "PER_PEER")])
+def test_host_state_launches_refuse_capture(ra, variant, key, value):
+    """The per-peer barrier's epoch and the pipelined variant's flag starts
+    are kernel parameters a graph would replay unchanged: those calls refuse
+    a capturing stream (before any launch), and work again outside it."""
+    R, n = 4, 4096
+    x = inputs.generate(R, n, "f32", "normal", 2)
+    inp, out = DeviceRanks(R, n, np.float32, host=x), DeviceRanks(R, n, np.float32)
+    with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
+        if key:
+            h.set_option(ra.Option[key], (ra.Protocol if key == "PROTOCOL" else ra.Barrier)[value])
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            h.allreduce(inp.views, out.views, side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with pytest.raises(ra.RAError) as e:
+            with torch.cuda.graph(g, stream=side):
+                h.allreduce(inp.views, out.views, side)
+        assert e.value.status == ra.Status.ERR_UNSUPPORTED
+        assert "captured" in ra.ra_last_error()
+        out2 = DeviceRanks(R, n, np.float32)
+        h.allreduce(inp.views, out2.views)
+        assert h.device_status()[0] == ra.Status.OK
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = out2.host()
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r])
 
 
 @pytest.mark.parametrize("dtype,op", DTYPE_OPS)
