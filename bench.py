@@ -669,6 +669,7 @@ SWEEP_VARIANTS = [
     ("persistent_cluster", "persistent", lambda ra: [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
     ("pipelined", "pipelined", lambda ra: []),
     ("pipelined_ll", "pipelined", lambda ra: [(ra.Option.PROTOCOL, ra.Protocol.LL)]),
+    ("pipelined_ll_cluster", "pipelined", lambda ra: [(ra.Option.PROTOCOL, ra.Protocol.LL_CLUSTER)]),
     ("local", "local", lambda ra: []),
 ]
 
@@ -692,8 +693,10 @@ def run_barriers(args):
                               ("per_peer", "persistent", [(ra.Option.BARRIER, ra.Barrier.PER_PEER)]),
                               ("cluster", "persistent", [(ra.Option.BARRIER, ra.Barrier.CLUSTER)]),
                               ("pipelined", "pipelined", []),
-                              ("pipelined_ll", "pipelined", [(ra.Option.PROTOCOL, ra.Protocol.LL)])):
-            if name == "cluster" and R > 16:
+                              ("pipelined_ll", "pipelined", [(ra.Option.PROTOCOL, ra.Protocol.LL)]),
+                              ("pipelined_ll_cluster", "pipelined",
+                               [(ra.Option.PROTOCOL, ra.Protocol.LL_CLUSTER)])):
+            if name in ("cluster", "pipelined_ll_cluster") and R > 16:
                 line[name] = None
                 continue
             h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)
@@ -802,7 +805,7 @@ def run_sweep(args):
         _, outs = _device_ranks(torch, R, n, inputs.storage_dtype("f32"))
         line = {"sweep": "r8_f32_n" if R == 8 else "f32_R", "R": R, "n_per_rank": n}
         for name, v, opts in SWEEP_VARIANTS:
-            if name == "persistent_cluster" and R > 16:
+            if name in ("persistent_cluster", "pipelined_ll_cluster") and R > 16:
                 line[name] = None
                 continue
             h = ra.RingAllReduce(R, n, "f32", "sum", variant=v)

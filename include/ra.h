@@ -156,7 +156,7 @@ typedef enum ra_protocol {
                                  then a progress flag is published (a release
                                  fence and a SignalAdd) that the successor
                                  polls before reading the partial */
-  RA_PROTOCOL_LL = 1          /* flag-in-data messages for small chunks: each
+  RA_PROTOCOL_LL = 1,         /* flag-in-data messages for small chunks: each
                                  8-byte word carries 32 bits of data and a
                                  32-bit flag naming the call and the round,
                                  written by one store into the successor's row
@@ -168,6 +168,15 @@ typedef enum ra_protocol {
                                  store and one poll, with no fence and no
                                  separate flag.  Twice the bytes per element
                                  (four times for 16-bit elements). */
+  RA_PROTOCOL_LL_CLUSTER = 2  /* the same words, stored straight into the
+                                 successor's shared memory: the R CTAs of a
+                                 channel form one thread-block cluster (R <=
+                                 16, else RA_ERR_UNSUPPORTED) and each polls
+                                 its own shared memory, so a hop stays inside
+                                 one GPC.  No inbox and no state kept between
+                                 calls (capturable into a CUDA graph); a
+                                 CTA's rows take (2R-3) x 8 x w bytes per
+                                 position it carries, at most 200 KiB. */
 } ra_protocol;
 
 typedef enum ra_option {
@@ -236,10 +245,11 @@ typedef enum ra_option {
                                 whose signals are 56-bit counters would use 56.
                                 ra_read_signals returns the low bits too. */
   RA_OPT_PROTOCOL = 15,      /* ra_protocol of the pipelined variant, default
-                                RA_PROTOCOL_SIMPLE.  With RA_PROTOCOL_LL,
-                                RA_OPT_CTAS is the channels per rank (0:
-                                chosen), RA_OPT_SKIP_ARRIVAL names a rank that
-                                sends nothing from that round on, and
+                                RA_PROTOCOL_SIMPLE.  With RA_PROTOCOL_LL and
+                                RA_PROTOCOL_LL_CLUSTER, RA_OPT_CTAS is the
+                                channels per rank (0: chosen),
+                                RA_OPT_SKIP_ARRIVAL names a rank that sends
+                                nothing from that round on, and
                                 RA_OPT_SLICES, RA_OPT_WINDOW and
                                 RA_OPT_SIGNAL_BITS do not apply. */
   RA_OPT_LL_FLAG = 16,       /* the flag the next RA_PROTOCOL_LL call's first

@@ -66,6 +66,7 @@ class Barrier(enum.IntEnum):
 class Protocol(enum.IntEnum):
     SIMPLE = 0
     LL = 1
+    LL_CLUSTER = 2
 
 
 class Option(enum.IntEnum):

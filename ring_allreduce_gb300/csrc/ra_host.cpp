@@ -852,9 +852,10 @@ ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in,
   a.plan = make_plan(h->R, h->n);
   a.R = h->R;
   a.mode = mode;
+  a.elem_bytes = (int)elem_bytes(h->dtype);
   a.rounds = h->region[ra::kSyncFlags][kind].rounds;
   const int64_t C = a.plan.C;
-  const int wpe = ra::ll_words_per_element((int)elem_bytes(h->dtype));
+  const int wpe = ra::ll_words_per_element(a.elem_bytes);
   // rows: the most messages a call sends (AllReduce: 2R-3) x receiving ranks
   const size_t words = (size_t)(2 * h->R - 3) * (size_t)h->R * (size_t)C * (size_t)wpe;
   if (words > kLLInboxBytes / sizeof(uint64_t))
@@ -908,8 +909,54 @@ ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in,
   return RA_OK;
 }
 
+// The pipelined variant with flag-in-data messages through distributed
+// shared memory (ra_ll.cu): one cluster of R CTAs per channel.
+ra_status run_pipelined_ll_cluster(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
+                                   cudaStream_t st) {
+  if (h->R > 16) return fail(RA_ERR_UNSUPPORTED, "LL_CLUSTER protocol needs R <= 16 (R=%d)", h->R);
+  ra::LLArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = make_ptrs(h, in, out);
+  a.plan = make_plan(h->R, h->n);
+  a.R = h->R;
+  a.mode = mode;
+  a.elem_bytes = (int)elem_bytes(h->dtype);
+  a.rounds = h->region[ra::kSyncFlags][kind].rounds;
+  const int64_t C = a.plan.C;
+  const int threads = (int)std::min<int64_t>(ra::kLLThreads, std::max<int64_t>(32, (C + 31) / 32 * 32));
+  if (h->ctas > 0) {
+    a.G = h->ctas;
+    a.E = (int)std::max<int64_t>(1, (C + (int64_t)a.G * threads - 1) / ((int64_t)a.G * threads));
+  } else {
+    // one position per thread; channels are independent clusters, so any
+    // number of them may run one wave after another
+    a.E = 1;
+    a.G = (int)std::max<int64_t>(1, (C + threads - 1) / threads);
+  }
+  if (a.E > ra::kLLMaxE)
+    return fail(RA_ERR_UNSUPPORTED, "LL_CLUSTER protocol: %d channels of %d threads cannot carry %lld-element chunks",
+                a.G, threads, (long long)C);
+  if ((int64_t)a.G * h->R > 2147483647LL) return fail(RA_ERR_UNSUPPORTED, "too many clusters");
+  const size_t smem = ra::ll_cluster_smem_bytes(a, threads, a.elem_bytes);
+  if (smem > (size_t)ra::kLLClusterMaxSmem)
+    return fail(RA_ERR_UNSUPPORTED, "LL_CLUSTER protocol: %zu bytes of rows per CTA (at most %d)", smem,
+                ra::kLLClusterMaxSmem);
+  int clusters = 0;
+  cudaError_t e = ra::ll_cluster_capacity(h->dtype, h->op, a, threads, smem, &clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "cluster occupancy query");
+  if (clusters < 1) return fail(RA_ERR_UNSUPPORTED, "a cluster of %d CTAs with %zu bytes each does not fit", h->R, smem);
+  a.timeout_ns = h->timeout_ns;
+  a.err = h->d_err;
+  a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
+  a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
+  e = ra::launch_ll_cluster(h->dtype, h->op, a, threads, smem, st);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "LL_CLUSTER kernel launch");
+}
+
 ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
                         cudaStream_t st) {
+  // nothing of the cluster form is kept between calls: a graph may replay it
+  if (h->protocol == RA_PROTOCOL_LL_CLUSTER) return run_pipelined_ll_cluster(h, kind, mode, in, out, st);
   ra_status s = refuse_capture(st, "the pipelined variant");
   if (s != RA_OK) return s;
   if (h->protocol == RA_PROTOCOL_LL) return run_pipelined_ll(h, kind, mode, in, out, st);
@@ -1030,6 +1077,7 @@ ra_status ra_create(int R, size_t n, ra_dtype dtype, ra_op op, ra_handle* out) {
   if (e == cudaSuccess) e = ra::prepare_bcast();
   if (e == cudaSuccess) e = ra::prepare_persistent_cluster();
   if (e == cudaSuccess) e = ra::prepare_local();
+  if (e == cudaSuccess) e = ra::prepare_ll_cluster();
   if (e != cudaSuccess) return cuda_fail(e, "kernel set-up");
   int lbps = 0;
   if (R >= 2) {
@@ -1450,7 +1498,7 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       h->window = (int)value;
       return RA_OK;
     case RA_OPT_PROTOCOL:
-      if (value != RA_PROTOCOL_SIMPLE && value != RA_PROTOCOL_LL)
+      if (value != RA_PROTOCOL_SIMPLE && value != RA_PROTOCOL_LL && value != RA_PROTOCOL_LL_CLUSTER)
         return fail(RA_ERR_INVALID, "unknown protocol %lld", value);
       if (value == RA_PROTOCOL_LL && h->ll_blocks_per_sm == 0)
         return fail(RA_ERR_UNSUPPORTED, "device has no cooperative launch");

@@ -1,6 +1,7 @@
 // ra_ll.cu -- the pipelined variant with flag-in-data messages
-// (RA_OPT_PROTOCOL = RA_PROTOCOL_LL), for chunks small enough that a ring
-// round is a chain of memory latencies rather than a stream of bytes.
+// (RA_OPT_PROTOCOL = RA_PROTOCOL_LL or RA_PROTOCOL_LL_CLUSTER), for chunks
+// small enough that a ring round is a chain of memory latencies rather than
+// a stream of bytes.
 //
 // "Why AllReduce = ReduceScatter + AllGather -- NCCL Ring AllReduce",
 // sections 4 to 8: in every round a rank receives one chunk's partial from
@@ -15,32 +16,46 @@
 // fence and a signal the receiver polls), so every hop costs a store, a
 // fence that waits for the store to be acknowledged, the signal's trip and
 // the receiver's poll, then a load of the data.  Here each message word
-// carries 32 bits of data together with a 32-bit flag naming the call and
-// the round, written by one 8-byte store (single-copy atomic): the receiver
-// polls the data words themselves, and a word whose flag is the expected
-// one holds the expected data.  A hop is then one store and the poll that
-// sees it, with no fence, no separate signal and no CTA barrier: thread k
-// of a receiving CTA depends only on thread k of the sending CTA, which
-// carries the same positions of the same chunk.  This is the low-latency
-// message form of NCCL's ring (flags inside the data), which the pages do
-// not describe.  The price is twice the bytes per element (four times for
-// 16-bit elements), so it is for small chunks only.
+// carries 32 bits of data together with a 32-bit flag naming the message,
+// written by one 8-byte store (single-copy atomic): the receiver polls the
+// data words themselves, and a word whose flag is the expected one holds the
+// expected data.  A hop is then one store and the poll that sees it, with no
+// fence, no separate signal and no CTA barrier: thread k of a receiving CTA
+// depends only on thread k of the sending CTA, which carries the same
+// positions of the same chunk.  This is the low-latency message form of
+// NCCL's ring (flags inside the data), which the pages do not describe.  The
+// price is twice the bytes per element (four times for 16-bit elements), so
+// it is for small chunks only.
 //
-// Messages live in an inbox of the handle, one row per (message, receiving
-// rank), each row written once per call, so no word is overwritten while
-// someone may still read it.  Flags grow by one per message and by the
-// call's rounds per call (the host restarts them, zeroing the inbox, before
-// they would wrap), so a word left from any earlier call or round never
-// carries the flag being waited for.  Outputs are written only with complete
-// values (the owner's chunk after the last reduce round, every chunk in the
-// copy rounds), and each is written by the thread that read the same
-// element of the same rank's input earlier, or (a rank's chunk r read by its
-// successor in the first round) at the end of a chain of messages each of
-// which carries a value computed from that read: in place calls are safe.
+// Two transports:
+//  * LL: rows of an inbox in device memory, one per (message, receiving
+//    rank), each written once per call, so no word is overwritten while
+//    someone may still read it.  Flags grow by one per message and by the
+//    call's rounds per call (the host restarts them, zeroing the inbox,
+//    before they would wrap), so a word left from any earlier call or round
+//    never carries the flag being waited for.  One cooperative launch (every
+//    channel's CTAs wait on each other's messages).
+//  * LL_CLUSTER: the R CTAs of a channel form one thread-block cluster, and
+//    a message word is stored straight into the successor's shared memory
+//    (distributed shared memory, st.relaxed.cluster), which the successor
+//    polls locally: the hop stays inside one GPC instead of going through
+//    L2.  Each CTA zeroes its rows and the cluster meets once before any
+//    message is sent, so message m carries flag m + 1 in every launch and
+//    nothing is kept between calls (a CUDA graph may replay the launch); the
+//    cluster meets again before any CTA exits, so no store reaches the
+//    shared memory of a CTA that has left.  Channels are independent
+//    clusters: no cooperative launch.
+//
+// Outputs are written only with complete values (the owner's chunk after
+// the last reduce round, every chunk in the copy rounds), and each is
+// written by the thread that read the same element of the same rank's input
+// earlier, or (a rank's chunk r read by its successor in the first round) at
+// the end of a chain of messages each of which carries a value computed from
+// that read: in place calls are safe.
 //
 // Waits are bounded (timeout_ns, two clocks); one that runs out records code
 // 5 (round, rank, channel, predecessor, flag seen, flag expected) and the
-// thread returns; every other waiter returns once it sees the record.
+// thread stops; every other waiter stops once it sees the record.
 #include "ra_device.cuh"
 #include "ra_ll.h"
 
@@ -63,20 +78,81 @@ __device__ __forceinline__ T from_raw(uint64_t b) {
 
 __device__ __forceinline__ uint32_t word_flag(uint64_t w) { return (uint32_t)(w >> 32); }
 
-// Poll the words of this thread's positions in `box` until each carries
-// `flag`; the data into val[].  False when the thread must stop.
-template <class T, int WPE>
-__device__ __forceinline__ bool ll_receive(const LLArgs& a, const uint64_t* box, int64_t pos0, int64_t len,
+// ------------------------------------------------------------ transports
+// A transport gives the row a rank receives message m in (already at this
+// channel's first position) and stores a word into the successor's row.
+
+struct GlobalInbox {
+  uint64_t* inbox;
+  int64_t row;        // words of one (message, rank) row: C * wpe
+  int64_t chan;       // this channel's first word in a row
+  int R, r, q;
+  uint32_t flag_base;
+  __device__ __forceinline__ const uint64_t* recv_row(int m) const {
+    return inbox + ((int64_t)m * R + r) * row + chan;
+  }
+  __device__ __forceinline__ uint64_t load(const uint64_t* w) const { return signal_load_relaxed(w); }
+  __device__ __forceinline__ void store(int m, int64_t word, uint64_t v) const {
+    signal_store_relaxed(inbox + ((int64_t)m * R + q) * row + chan + word, v);
+  }
+  __device__ __forceinline__ uint32_t flag(int m) const { return flag_base + (uint32_t)m; }
+  // polls between looks at the clocks and the error record; polls after
+  // which each one sleeps (a poll is a round trip through L2)
+  static constexpr uint32_t kCheckEvery = 8;
+  static constexpr uint32_t kSleepAfter = 64;
+};
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(v));
+  return v;
+}
+
+// Every thread of the cluster; not .aligned: threads may arrive from
+// different points of a loop they left early.
+__device__ __forceinline__ void cluster_meet() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+struct ClusterInbox {
+  uint64_t* box;      // this CTA's rows in shared memory: [message][P * wpe]
+  int64_t row;        // words of one row
+  uint32_t q;         // the successor's rank in the cluster
+  __device__ __forceinline__ const uint64_t* recv_row(int m) const { return box + (int64_t)m * row; }
+  __device__ __forceinline__ uint64_t load(const uint64_t* w) const {
+    uint64_t v;
+    asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_addr(w)) : "memory");
+    return v;
+  }
+  // the same word of the successor's rows (every CTA lays its rows out alike)
+  __device__ __forceinline__ void store(int m, int64_t word, uint64_t v) const {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(box + (int64_t)m * row + word)),
+                 "r"(q));
+    asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+  }
+  __device__ __forceinline__ uint32_t flag(int m) const { return (uint32_t)m + 1u; }
+  // a poll of shared memory is short next to a look at the clocks or a load
+  // of the error record, and occupies nothing but this SM: no sleeping
+  static constexpr uint32_t kCheckEvery = 32;
+  static constexpr uint32_t kSleepAfter = 0;
+};
+
+// Poll the words of this thread's positions (local k*blockDim.x + tid, valid
+// below `lim`) in `row` until each carries `flag`; the data into val[].
+// False when the thread must stop.
+template <class T, int WPE, class Tr>
+__device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const uint64_t* row, int64_t lim,
                                            uint32_t flag, T* val, int t, int r, int g, int p) {
   uint64_t w[kLLMaxE * WPE];
   uint32_t pending = 0;
 #pragma unroll
   for (int k = 0; k < kLLMaxE; ++k) {
-    const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-    if (k < a.E && pos < len) {
+    const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+    if (k < a.E && loc < lim) {
 #pragma unroll
       for (int h = 0; h < WPE; ++h) {
-        w[k * WPE + h] = signal_load_relaxed(box + pos * WPE + h);
+        w[k * WPE + h] = tr.load(row + loc * WPE + h);
         if (word_flag(w[k * WPE + h]) != flag) pending |= 1u << (k * WPE + h);
       }
     }
@@ -84,17 +160,18 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const uint64_t* box,
   if (pending) {
     const Deadline limit(a.timeout_ns);
     for (uint32_t it = 0;; ++it) {
-      if (it >= 64) __nanosleep(64);
+      if (Tr::kSleepAfter && it >= Tr::kSleepAfter) __nanosleep(64);
 #pragma unroll
       for (int i = 0; i < kLLMaxE * WPE; ++i) {
         if (pending & (1u << i)) {
-          const int64_t pos = pos0 + (int64_t)(i / WPE) * blockDim.x;
-          w[i] = signal_load_relaxed(box + pos * WPE + (i % WPE));
+          const int64_t loc = (int64_t)(i / WPE) * blockDim.x + threadIdx.x;
+          w[i] = tr.load(row + loc * WPE + (i % WPE));
           if (word_flag(w[i]) == flag) pending &= ~(1u << i);
         }
       }
       if (!pending) break;
-      if ((it & 7u) == 7u && load_relaxed_u32(&a.err->code) != 0u) return false;
+      if (it % Tr::kCheckEvery != Tr::kCheckEvery - 1) continue;
+      if (load_relaxed_u32(&a.err->code) != 0u) return false;
       if (limit.passed()) {
         uint32_t seen = 0;
 #pragma unroll
@@ -107,8 +184,8 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const uint64_t* box,
   }
 #pragma unroll
   for (int k = 0; k < kLLMaxE; ++k) {
-    const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-    if (k < a.E && pos < len) {
+    const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+    if (k < a.E && loc < lim) {
       uint64_t b = (uint32_t)w[k * WPE];
       if (WPE == 2) b |= (uint64_t)(uint32_t)w[k * WPE + WPE - 1] << 32;
       val[k] = from_raw<T>(b);
@@ -117,17 +194,15 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const uint64_t* box,
   return true;
 }
 
-template <class D, int OP>
-__global__ void __launch_bounds__(kLLThreads, 4) ll_kernel(const LLArgs a) {
+// Every ring round of rank r, channel g, over this thread's positions
+// chan0 + k*blockDim.x + tid of each chunk; false if a wait gave up.
+template <class D, int OP, class Tr>
+__device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, int g) {
   using T = typename D::T;
   constexpr int WPE = sizeof(T) == 8 ? 2 : 1;
   const int R = a.R, E = a.E;
-  const int r = blockIdx.x % R;
-  const int g = blockIdx.x / R;
   const int p = (r == 0) ? R - 1 : r - 1;
-  const int q = (r == R - 1) ? 0 : r + 1;
-  const int64_t row = a.plan.C * WPE;
-  const int64_t pos0 = (int64_t)g * blockDim.x * E + threadIdx.x;
+  const int64_t chan0 = (int64_t)g * blockDim.x * E;
   const T* in_r = static_cast<const T*>(a.p.in[r]);
   T* out_r = static_cast<T*>(a.p.out[r]);
   for (int t = 0; t < a.rounds; ++t) {
@@ -146,16 +221,17 @@ __global__ void __launch_bounds__(kLLThreads, 4) ll_kernel(const LLArgs a) {
     int c = reduce ? (r - s) : (r + 1 - s);
     c %= R;
     if (c < 0) c += R;
-    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n);
-    const int64_t len = min(off + a.plan.C, a.plan.n) - off;
+    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n) + chan0;
+    // positions of this channel in the chunk: local < lim
+    const int64_t lim = min((int64_t)c * a.plan.C + a.plan.C, a.plan.n) - off;
     T own[kLLMaxE];
     T val[kLLMaxE];
     // the local piece first: it does not wait for the predecessor
     if (reduce) {
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-        if (k < E && pos < len) own[k] = ld_l2_scalar(in_r + off + pos);
+        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+        if (k < E && loc < lim) own[k] = ld_l2_scalar(in_r + off + loc);
       }
     }
     if (t == 0) {
@@ -163,33 +239,31 @@ __global__ void __launch_bounds__(kLLThreads, 4) ll_kernel(const LLArgs a) {
       const T* src = static_cast<const T*>(reduce ? a.p.in[p] : a.p.out[p]);
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-        if (k < E && pos < len) val[k] = ld_l2_scalar(src + off + pos);
+        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+        if (k < E && loc < lim) val[k] = ld_l2_scalar(src + off + loc);
       }
-    } else {
-      const uint64_t* box = a.inbox + ((int64_t)(t - 1) * R + r) * row;
-      if (!ll_receive<T, WPE>(a, box, pos0, len, a.flag_base + (uint32_t)(t - 1), val, t, r, g, p)) return;
+    } else if (!ll_receive<T, WPE>(a, tr, tr.recv_row(t - 1), lim, tr.flag(t - 1), val, t, r, g, p)) {
+      return false;
     }
     if (reduce) {
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-        if (k < E && pos < len) val[k] = Op<D, OP>::apply(val[k], own[k]);
+        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+        if (k < E && loc < lim) val[k] = Op<D, OP>::apply(val[k], own[k]);
       }
     }
     // send before writing the output: the successor is waiting for it.
     // Failure injection: a rank that is to fall silent sends nothing from
     // round skip_round on.
     if (t + 1 < a.rounds && !(r == a.skip_rank && t >= a.skip_round)) {
-      uint64_t* box = a.inbox + ((int64_t)t * R + q) * row;
-      const uint64_t f = (uint64_t)(a.flag_base + (uint32_t)t) << 32;
+      const uint64_t f = (uint64_t)tr.flag(t) << 32;
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-        if (k < E && pos < len) {
+        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+        if (k < E && loc < lim) {
           const uint64_t b = raw_bits(val[k]);
-          signal_store_relaxed(box + pos * WPE, f | (b & 0xFFFFFFFFull));
-          if (WPE == 2) signal_store_relaxed(box + pos * WPE + WPE - 1, f | (b >> 32));
+          tr.store(t, loc * WPE, f | (b & 0xFFFFFFFFull));
+          if (WPE == 2) tr.store(t, loc * WPE + WPE - 1, f | (b >> 32));
         }
       }
     }
@@ -198,14 +272,50 @@ __global__ void __launch_bounds__(kLLThreads, 4) ll_kernel(const LLArgs a) {
     if (!reduce || s == R - 1) {
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t pos = pos0 + (int64_t)k * blockDim.x;
-        if (k < E && pos < len) st_g(out_r + off + pos, val[k]);
+        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
+        if (k < E && loc < lim) st_g(out_r + off + loc, val[k]);
       }
     }
   }
+  return true;
 }
 
-const void* ll_select(int dtype, int op) {
+template <class D, int OP>
+__global__ void __launch_bounds__(kLLThreads, 3) ll_kernel(const LLArgs a) {
+  constexpr int WPE = sizeof(typename D::T) == 8 ? 2 : 1;
+  const int r = blockIdx.x % a.R;
+  const int g = blockIdx.x / a.R;
+  GlobalInbox tr;
+  tr.inbox = a.inbox;
+  tr.row = a.plan.C * WPE;
+  tr.chan = (int64_t)g * blockDim.x * a.E * WPE;
+  tr.R = a.R;
+  tr.r = r;
+  tr.q = (r == a.R - 1) ? 0 : r + 1;
+  tr.flag_base = a.flag_base;
+  ll_rounds<D, OP>(a, tr, r, g);
+}
+
+template <class D, int OP>
+__global__ void __launch_bounds__(kLLThreads, 1) ll_cluster_kernel(const LLArgs a) {
+  constexpr int WPE = sizeof(typename D::T) == 8 ? 2 : 1;
+  extern __shared__ __align__(16) uint64_t ll_box[];
+  const int r = (int)cluster_cta_rank();   // blockIdx.x = g R + r
+  const int g = blockIdx.x / a.R;
+  ClusterInbox tr;
+  tr.box = ll_box;
+  tr.row = (int64_t)blockDim.x * a.E * WPE;
+  tr.q = (uint32_t)((r == a.R - 1) ? 0 : r + 1);
+  // zero this CTA's rows, then meet: no peer stores into them before
+  const int64_t words = (int64_t)(a.rounds - 1) * tr.row;
+  for (int64_t i = threadIdx.x; i < words; i += blockDim.x) ll_box[i] = 0;
+  cluster_meet();
+  ll_rounds<D, OP>(a, tr, r, g);
+  // nobody leaves while a peer may still store into its rows
+  cluster_meet();
+}
+
+const void* ll_fn(int dtype, int op) {
   const void* fn = nullptr;
   with_dtype_op(dtype, op, [&](auto d, auto o) {
     fn = reinterpret_cast<const void*>(&ll_kernel<decltype(d), decltype(o)::value>);
@@ -214,24 +324,92 @@ const void* ll_select(int dtype, int op) {
   return fn;
 }
 
+const void* ll_cluster_fn(int dtype, int op) {
+  const void* fn = nullptr;
+  with_dtype_op(dtype, op, [&](auto d, auto o) {
+    fn = reinterpret_cast<const void*>(&ll_cluster_kernel<decltype(d), decltype(o)::value>);
+    return cudaSuccess;
+  });
+  return fn;
+}
+
+bool ll_shape_ok(const LLArgs& a, int threads) {
+  return a.R >= 2 && a.R <= kMaxRanks && a.G >= 1 && a.E >= 1 && a.E <= kLLMaxE && threads >= 32 &&
+         threads <= kLLThreads && threads % 32 == 0 && a.rounds >= 1 && a.err &&
+         (int64_t)a.G * threads * a.E >= a.plan.C;
+}
+
+cudaLaunchConfig_t ll_cluster_config(const LLArgs& a, int threads, size_t smem, cudaStream_t st,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.R * a.G);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.R;   // CTA (r, g) = blockIdx.x = g R + r: rank r of cluster g
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 }  // namespace
 
 cudaError_t ll_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
-  const void* fn = ll_select(dtype, op);
+  const void* fn = ll_fn(dtype, op);
   if (!fn) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
 }
 
 cudaError_t launch_ll(int dtype, int op, const LLArgs& a, int threads, cudaStream_t st) {
-  const void* fn = ll_select(dtype, op);
-  if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.E < 1 || a.E > kLLMaxE || threads < 32 ||
-      threads > kLLThreads || threads % 32 != 0 || a.rounds < 1 || !a.inbox || !a.err ||
-      (int64_t)a.G * threads * a.E < a.plan.C)
-    return cudaErrorInvalidValue;
+  const void* fn = ll_fn(dtype, op);
+  if (!fn || !ll_shape_ok(a, threads) || !a.inbox) return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<LLArgs*>(&a)};
   return cudaLaunchCooperativeKernel(fn, dim3(a.R * a.G), dim3(threads), args, 0, st);
+}
+
+size_t ll_cluster_smem_bytes(const LLArgs& a, int threads, int elem_bytes) {
+  const size_t rows = a.rounds > 1 ? (size_t)(a.rounds - 1) : 1;
+  return rows * (size_t)threads * (size_t)a.E * (size_t)ll_words_per_element(elem_bytes) * sizeof(uint64_t);
+}
+
+cudaError_t prepare_ll_cluster() {
+  cudaError_t err = cudaSuccess;
+  for (int dt = RA_F32; dt <= RA_I64 && err == cudaSuccess; ++dt)
+    for (int op = RA_SUM; op <= RA_MAX && err == cudaSuccess; ++op) {
+      const void* fn = ll_cluster_fn(dt, op);
+      err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kLLClusterMaxSmem);
+    }
+  return err;
+}
+
+cudaError_t ll_cluster_capacity(int dtype, int op, const LLArgs& a, int threads, size_t smem, int* clusters) {
+  const void* fn = ll_cluster_fn(dtype, op);
+  if (!fn || a.R < 2 || a.R > 16) return cudaErrorInvalidValue;
+  LLArgs one = a;
+  one.G = 1;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = ll_cluster_config(one, threads, smem, 0, attr);
+  return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
+}
+
+cudaError_t launch_ll_cluster(int dtype, int op, const LLArgs& a, int threads, size_t smem, cudaStream_t st) {
+  const void* fn = ll_cluster_fn(dtype, op);
+  if (!fn || !ll_shape_ok(a, threads) || a.R > 16 || smem > (size_t)kLLClusterMaxSmem ||
+      smem < ll_cluster_smem_bytes(a, threads, a.elem_bytes))
+    return cudaErrorInvalidValue;
+  const cudaError_t e = debug_upload(st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = ll_cluster_config(a, threads, smem, st, attr);
+  void* args[] = {const_cast<LLArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace ra

@@ -132,6 +132,11 @@ def main():
             run(R, n, "bf16", "sum", "pipelined", kind, options=[(ra.Option.PROTOCOL, ra.Protocol.LL)])
         run(R, n, "f64", "sum", "pipelined", "allreduce", options=[(ra.Option.PROTOCOL, ra.Protocol.LL)])
         calls += 4
+        if R <= 16:
+            for kind in ("allreduce", "reduce_scatter", "all_gather"):
+                run(R, n, "bf16", "sum", "pipelined", kind, options=[(ra.Option.PROTOCOL, ra.Protocol.LL_CLUSTER)])
+            run(R, n, "f64", "sum", "pipelined", "allreduce", options=[(ra.Option.PROTOCOL, ra.Protocol.LL_CLUSTER)])
+            calls += 4
         # passes: every round on one part of every chunk (slice) before the next part
         for kind in ("allreduce", "reduce_scatter", "all_gather"):
             run(R, n, "bf16", "sum", "ring", kind, options=[(ra.Option.SLICES, 3)])
