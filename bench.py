@@ -271,6 +271,8 @@ def run_gpu_arm(args):
     big_in, ins = _device_ranks(torch, R, n, st_dtype, host)
     big_out, outs = _device_ranks(torch, R, n, st_dtype)
     h = ra.RingAllReduce(R, n, dtype, op, variant=args.variant)
+    if args.protocol != "simple":
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol[args.protocol.upper()])
     variant_name = args.variant
 
     # ---- timed region: K steps, barrier + synchronize on both sides
@@ -414,6 +416,7 @@ def workload_config(args, R, n, op, b, ws):
         "workload": WORKLOAD_TEXT.get(args.workload, args.workload) if args.n is None
         else f"{args.workload} with n={n}",
         "R": R, "n_per_rank": n, "op": op, "variant": args.variant,
+        **({"protocol": args.protocol} if args.protocol != "simple" else {}),
         "l2": f"inputs larger than L2: {R * n * b / 2**20:.0f} MiB of inputs, "
               f"{R * n * b / 2**20:.0f} MiB of outputs per step, no flush",
         "parallelism": f"replicas x{ws} (each GPU runs its own {R}-rank ring)",
@@ -790,6 +793,49 @@ def run_extras(args):
         torch.cuda.empty_cache()
 
 
+def run_l2(args):
+    """Copy bandwidth through L2: a device copy (torch) of one buffer into
+    another, both small enough to stay in the 129 MB L2, replayed 64 times
+    from a CUDA graph so that launches do not count; bytes = read + write.
+    The last line is a copy far larger than L2 (DRAM).  One JSON line per
+    size: what a plain copy reaches when its data never leaves L2 -- the
+    scale for the L2 traffic of the variants that pass their partials
+    through memory."""
+    import torch
+    peak, _ = measured_peaks()
+    for mib in (4, 8, 16, 24, 32, 48, 1024):
+        nbytes = mib << 20
+        src = torch.ones(nbytes // 4, dtype=torch.float32, device="cuda")
+        dst = torch.empty_like(src)
+        copies = 64 if mib <= 64 else 4
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                dst.copy_(src)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(copies):
+                dst.copy_(src)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3 / copies)
+        t = statistics.median(times)
+        print(json.dumps({"l2_copy_mib": mib, "us_per_copy": round(t * 1e6, 2),
+                          "tb_per_s": round(2 * nbytes / t / 1e12, 2),
+                          "of_measured_hbm": round(2 * nbytes / t / 1e9 / peak, 3)}), flush=True)
+        del src, dst, g
+        torch.cuda.empty_cache()
+
+
 def run_sweep(args):
     """Latency/bandwidth sweep (R=8 fp32 sum over n, and R over 2..32 at
     n=2^24), every variant; one JSON line per point on stdout."""
@@ -877,7 +923,11 @@ def main():
     ap.add_argument("--workload", default="r8_f32", choices=["r8_f32", "r8_bf16", "r16_i32", "r4_small"])
     ap.add_argument("--n", type=int, default=None, help="override n per rank (profiling of a smaller case)")
     ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined", "local"])
+    ap.add_argument("--protocol", default="simple", choices=["simple", "ll", "ll_cluster"],
+                    help="message protocol of the pipelined variant")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--l2", action="store_true",
+                    help="copy bandwidth through L2: a device copy over buffers that stay in L2, by size")
     ap.add_argument("--barriers", action="store_true", help="barrier cost vs R, counting vs per-peer")
     ap.add_argument("--extras", action="store_true", help="other dtypes and collectives (direct kernel)")
     ap.add_argument("--no-cpu", action="store_true")
@@ -895,6 +945,8 @@ def main():
         run_reference_arm(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.l2:
+        run_l2(args)
     elif args.barriers:
         run_barriers(args)
     elif args.extras:

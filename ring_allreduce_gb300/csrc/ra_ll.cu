@@ -158,7 +158,11 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
     }
   }
   if (pending) {
-    const Deadline limit(a.timeout_ns);
+    // Off the fast path: the clocks start at the first look, not the first
+    // poll, and the error record is loaded one look ahead of its test, so
+    // its trip overlaps polls.  The bound is the limit plus one look.
+    uint64_t t0 = 0, c0 = 0;
+    uint32_t stop = 0;
     for (uint32_t it = 0;; ++it) {
       if (Tr::kSleepAfter && it >= Tr::kSleepAfter) __nanosleep(64);
 #pragma unroll
@@ -171,8 +175,15 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
       }
       if (!pending) break;
       if (it % Tr::kCheckEvery != Tr::kCheckEvery - 1) continue;
-      if (load_relaxed_u32(&a.err->code) != 0u) return false;
-      if (limit.passed()) {
+      if (stop != 0u) return false;
+      stop = load_relaxed_u32(&a.err->code);
+      if (it == Tr::kCheckEvery - 1) {
+        t0 = globaltimer_ns();
+        c0 = sm_cycles();
+        continue;
+      }
+      const int64_t cycles = a.timeout_ns > ((int64_t)1 << 60) ? ((int64_t)1 << 62) : 3 * a.timeout_ns;
+      if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || (int64_t)(sm_cycles() - c0) > cycles) {
         uint32_t seen = 0;
 #pragma unroll
         for (int i = kLLMaxE * WPE - 1; i >= 0; --i)
@@ -205,25 +216,21 @@ __device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, 
   const int64_t chan0 = (int64_t)g * blockDim.x * E;
   const T* in_r = static_cast<const T*>(a.p.in[r]);
   T* out_r = static_cast<T*>(a.p.out[r]);
-  for (int t = 0; t < a.rounds; ++t) {
-    bool reduce;
-    int s;
-    if (a.mode == kModeAllGather) {
-      reduce = false;
-      s = t + 1;
-    } else if (t < R - 1) {
-      reduce = true;
-      s = t + 1;
-    } else {
-      reduce = false;
-      s = t - (R - 1) + 1;
-    }
-    int c = reduce ? (r - s) : (r + 1 - s);
-    c %= R;
-    if (c < 0) c += R;
-    const int64_t off = min((int64_t)c * a.plan.C, a.plan.n) + chan0;
+  const bool gather = a.mode == kModeAllGather;
+  // The chunk of round t steps back round the ring by one every round:
+  // ReduceScatter round s = t + 1 takes chunk r - s and the copy rounds that
+  // follow it chunk r + 1 - s' (s' = t - R + 2), i.e. r - 1 - t throughout;
+  // an AllGather on its own (s = t + 1) takes r - t.  Kept by one decrement
+  // a round: the time between a send and the next poll is on the ring's
+  // critical path.
+  int c = gather ? r : (r == 0 ? R - 1 : r - 1);
+  for (int t = 0; t < a.rounds; ++t, c = (c == 0 ? R - 1 : c - 1)) {
+    const bool reduce = !gather && t < R - 1;
+    const bool complete = !reduce || t == R - 2;   // the owner's chunk after the last reduce round
+    const int64_t base = (int64_t)c * a.plan.C;
+    const int64_t off = min(base, a.plan.n) + chan0;
     // positions of this channel in the chunk: local < lim
-    const int64_t lim = min((int64_t)c * a.plan.C + a.plan.C, a.plan.n) - off;
+    const int64_t lim = min(base + a.plan.C, a.plan.n) - off;
     T own[kLLMaxE];
     T val[kLLMaxE];
     // the local piece first: it does not wait for the predecessor
@@ -269,7 +276,7 @@ __device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, 
     }
     // complete values: the owner's chunk after the last reduce round, every
     // chunk of the copy rounds
-    if (!reduce || s == R - 1) {
+    if (complete) {
 #pragma unroll
       for (int k = 0; k < kLLMaxE; ++k) {
         const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
