@@ -60,7 +60,7 @@ KERNEL_SOURCES = {
     "direct": ["ra_direct.cu", "ra_direct.cuh", "ra_direct_inst.cu", "ra_device.cuh", "ra_internal.h"],
     "round": ["ra_round.cu", "ra_device.cuh", "ra_internal.h"],
     "persistent": ["ra_persistent.cu", "ra_signal.cuh", "ra_device.cuh", "ra_internal.h"],
-    "pipelined": ["ra_pipelined.cu", "ra_device.cuh", "ra_internal.h"],
+    "pipelined": ["ra_pipelined.cu", "ra_signal.cuh", "ra_device.cuh", "ra_internal.h"],
     "compact": ["ra_compact.cu", "ra_device.cuh", "ra_internal.h"],
     "bcast": ["ra_bcast.cu", "ra_device.cuh", "ra_internal.h"],
     "local": ["ra_local.cu", "ra_device.cuh", "ra_internal.h"],

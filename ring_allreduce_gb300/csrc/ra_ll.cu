@@ -138,18 +138,25 @@ struct ClusterInbox {
   static constexpr uint32_t kSleepAfter = 0;
 };
 
-// Poll the words of this thread's positions (local k*blockDim.x + tid, valid
-// below `lim`) in `row` until each carries `flag`; the data into val[].
-// False when the thread must stop.
-template <class T, int WPE, class Tr>
-__device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const uint64_t* row, int64_t lim,
+// Positions a thread carries: local k*blockDim.x + tid for k < EM (a
+// compile-time bound, 1 or kLLMaxE) and k < a.E, valid below `lim` (at most
+// EM*blockDim.x, so 32 bits hold every local position).
+template <int EM>
+__device__ __forceinline__ bool carries(const LLArgs& a, int k, int lim) {
+  return (EM == 1 || k < a.E) && k * (int)blockDim.x + (int)threadIdx.x < lim;
+}
+
+// Poll the words of this thread's positions in `row` until each carries
+// `flag`; the data into val[].  False when the thread must stop.
+template <class T, int WPE, int EM, class Tr>
+__device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const uint64_t* row, int lim,
                                            uint32_t flag, T* val, int t, int r, int g, int p) {
-  uint64_t w[kLLMaxE * WPE];
+  uint64_t w[EM * WPE];
   uint32_t pending = 0;
 #pragma unroll
-  for (int k = 0; k < kLLMaxE; ++k) {
-    const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-    if (k < a.E && loc < lim) {
+  for (int k = 0; k < EM; ++k) {
+    if (carries<EM>(a, k, lim)) {
+      const int loc = k * (int)blockDim.x + (int)threadIdx.x;
 #pragma unroll
       for (int h = 0; h < WPE; ++h) {
         w[k * WPE + h] = tr.load(row + loc * WPE + h);
@@ -166,9 +173,9 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
     for (uint32_t it = 0;; ++it) {
       if (Tr::kSleepAfter && it >= Tr::kSleepAfter) __nanosleep(64);
 #pragma unroll
-      for (int i = 0; i < kLLMaxE * WPE; ++i) {
+      for (int i = 0; i < EM * WPE; ++i) {
         if (pending & (1u << i)) {
-          const int64_t loc = (int64_t)(i / WPE) * blockDim.x + threadIdx.x;
+          const int loc = (i / WPE) * (int)blockDim.x + (int)threadIdx.x;
           w[i] = tr.load(row + loc * WPE + (i % WPE));
           if (word_flag(w[i]) == flag) pending &= ~(1u << i);
         }
@@ -186,7 +193,7 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
       if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns || (int64_t)(sm_cycles() - c0) > cycles) {
         uint32_t seen = 0;
 #pragma unroll
-        for (int i = kLLMaxE * WPE - 1; i >= 0; --i)
+        for (int i = EM * WPE - 1; i >= 0; --i)
           if (pending & (1u << i)) seen = word_flag(w[i]);
         record_wait_error(a.err, 5u, t, r, g, p, seen, flag);
         return false;
@@ -194,9 +201,8 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
     }
   }
 #pragma unroll
-  for (int k = 0; k < kLLMaxE; ++k) {
-    const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-    if (k < a.E && loc < lim) {
+  for (int k = 0; k < EM; ++k) {
+    if (carries<EM>(a, k, lim)) {
       uint64_t b = (uint32_t)w[k * WPE];
       if (WPE == 2) b |= (uint64_t)(uint32_t)w[k * WPE + WPE - 1] << 32;
       val[k] = from_raw<T>(b);
@@ -207,13 +213,15 @@ __device__ __forceinline__ bool ll_receive(const LLArgs& a, const Tr& tr, const 
 
 // Every ring round of rank r, channel g, over this thread's positions
 // chan0 + k*blockDim.x + tid of each chunk; false if a wait gave up.
-template <class D, int OP, class Tr>
+template <class D, int OP, int EM, class Tr>
 __device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, int g) {
   using T = typename D::T;
   constexpr int WPE = sizeof(T) == 8 ? 2 : 1;
-  const int R = a.R, E = a.E;
+  const int R = a.R;
   const int p = (r == 0) ? R - 1 : r - 1;
-  const int64_t chan0 = (int64_t)g * blockDim.x * E;
+  const int span = EM == 1 ? (int)blockDim.x : a.E * (int)blockDim.x;   // positions of a channel
+  const int64_t chan0 = (int64_t)g * span;
+  const int64_t C = a.plan.C, n = a.plan.n;
   const T* in_r = static_cast<const T*>(a.p.in[r]);
   T* out_r = static_cast<T*>(a.p.out[r]);
   const bool gather = a.mode == kModeAllGather;
@@ -221,43 +229,39 @@ __device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, 
   // ReduceScatter round s = t + 1 takes chunk r - s and the copy rounds that
   // follow it chunk r + 1 - s' (s' = t - R + 2), i.e. r - 1 - t throughout;
   // an AllGather on its own (s = t + 1) takes r - t.  Kept by one decrement
-  // a round: the time between a send and the next poll is on the ring's
-  // critical path.
+  // a round, as is the channel's first element in it: the time between a
+  // send and the next poll is on the ring's critical path.
   int c = gather ? r : (r == 0 ? R - 1 : r - 1);
-  for (int t = 0; t < a.rounds; ++t, c = (c == 0 ? R - 1 : c - 1)) {
+  int64_t first = (int64_t)c * C + chan0;
+  for (int t = 0; t < a.rounds; ++t) {
     const bool reduce = !gather && t < R - 1;
     const bool complete = !reduce || t == R - 2;   // the owner's chunk after the last reduce round
-    const int64_t base = (int64_t)c * a.plan.C;
-    const int64_t off = min(base, a.plan.n) + chan0;
-    // positions of this channel in the chunk: local < lim
-    const int64_t lim = min(base + a.plan.C, a.plan.n) - off;
-    T own[kLLMaxE];
-    T val[kLLMaxE];
+    // positions of this channel in chunk c: local < lim (chunk end - first,
+    // clamped to the channel's span)
+    const int64_t left = min((int64_t)(c + 1) * C, n) - first;
+    const int lim = left <= 0 ? 0 : (left < span ? (int)left : span);
+    T own[EM];
+    T val[EM];
     // the local piece first: it does not wait for the predecessor
     if (reduce) {
+      const T* src = in_r + first;
 #pragma unroll
-      for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-        if (k < E && loc < lim) own[k] = ld_l2_scalar(in_r + off + loc);
-      }
+      for (int k = 0; k < EM; ++k)
+        if (carries<EM>(a, k, lim)) own[k] = ld_l2_scalar(src + k * (int)blockDim.x + (int)threadIdx.x);
     }
     if (t == 0) {
       // round 1 reads the predecessor's input (its owned chunk in AllGather)
-      const T* src = static_cast<const T*>(reduce ? a.p.in[p] : a.p.out[p]);
+      const T* src = static_cast<const T*>(reduce ? a.p.in[p] : a.p.out[p]) + first;
 #pragma unroll
-      for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-        if (k < E && loc < lim) val[k] = ld_l2_scalar(src + off + loc);
-      }
-    } else if (!ll_receive<T, WPE>(a, tr, tr.recv_row(t - 1), lim, tr.flag(t - 1), val, t, r, g, p)) {
+      for (int k = 0; k < EM; ++k)
+        if (carries<EM>(a, k, lim)) val[k] = ld_l2_scalar(src + k * (int)blockDim.x + (int)threadIdx.x);
+    } else if (!ll_receive<T, WPE, EM>(a, tr, tr.recv_row(t - 1), lim, tr.flag(t - 1), val, t, r, g, p)) {
       return false;
     }
     if (reduce) {
 #pragma unroll
-      for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-        if (k < E && loc < lim) val[k] = Op<D, OP>::apply(val[k], own[k]);
-      }
+      for (int k = 0; k < EM; ++k)
+        if (carries<EM>(a, k, lim)) val[k] = Op<D, OP>::apply(val[k], own[k]);
     }
     // send before writing the output: the successor is waiting for it.
     // Failure injection: a rank that is to fall silent sends nothing from
@@ -265,29 +269,35 @@ __device__ __forceinline__ bool ll_rounds(const LLArgs& a, const Tr& tr, int r, 
     if (t + 1 < a.rounds && !(r == a.skip_rank && t >= a.skip_round)) {
       const uint64_t f = (uint64_t)tr.flag(t) << 32;
 #pragma unroll
-      for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-        if (k < E && loc < lim) {
+      for (int k = 0; k < EM; ++k) {
+        if (carries<EM>(a, k, lim)) {
+          const int loc = k * (int)blockDim.x + (int)threadIdx.x;
           const uint64_t b = raw_bits(val[k]);
-          tr.store(t, loc * WPE, f | (b & 0xFFFFFFFFull));
-          if (WPE == 2) tr.store(t, loc * WPE + WPE - 1, f | (b >> 32));
+          tr.store(t, (int64_t)loc * WPE, f | (b & 0xFFFFFFFFull));
+          if (WPE == 2) tr.store(t, (int64_t)loc * WPE + WPE - 1, f | (b >> 32));
         }
       }
     }
     // complete values: the owner's chunk after the last reduce round, every
     // chunk of the copy rounds
     if (complete) {
+      T* dst = out_r + first;
 #pragma unroll
-      for (int k = 0; k < kLLMaxE; ++k) {
-        const int64_t loc = (int64_t)k * blockDim.x + threadIdx.x;
-        if (k < E && loc < lim) st_g(out_r + off + loc, val[k]);
-      }
+      for (int k = 0; k < EM; ++k)
+        if (carries<EM>(a, k, lim)) st_g(dst + k * (int)blockDim.x + (int)threadIdx.x, val[k]);
+    }
+    if (c == 0) {
+      c = R - 1;
+      first += (int64_t)(R - 1) * C;
+    } else {
+      --c;
+      first -= C;
     }
   }
   return true;
 }
 
-template <class D, int OP>
+template <class D, int OP, int EM>
 __global__ void __launch_bounds__(kLLThreads, 3) ll_kernel(const LLArgs a) {
   constexpr int WPE = sizeof(typename D::T) == 8 ? 2 : 1;
   const int r = blockIdx.x % a.R;
@@ -295,15 +305,15 @@ __global__ void __launch_bounds__(kLLThreads, 3) ll_kernel(const LLArgs a) {
   GlobalInbox tr;
   tr.inbox = a.inbox;
   tr.row = a.plan.C * WPE;
-  tr.chan = (int64_t)g * blockDim.x * a.E * WPE;
+  tr.chan = (int64_t)g * blockDim.x * (EM == 1 ? 1 : a.E) * WPE;
   tr.R = a.R;
   tr.r = r;
   tr.q = (r == a.R - 1) ? 0 : r + 1;
   tr.flag_base = a.flag_base;
-  ll_rounds<D, OP>(a, tr, r, g);
+  ll_rounds<D, OP, EM>(a, tr, r, g);
 }
 
-template <class D, int OP>
+template <class D, int OP, int EM>
 __global__ void __launch_bounds__(kLLThreads, 1) ll_cluster_kernel(const LLArgs a) {
   constexpr int WPE = sizeof(typename D::T) == 8 ? 2 : 1;
   extern __shared__ __align__(16) uint64_t ll_box[];
@@ -311,30 +321,38 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_cluster_kernel(const LLArgs 
   const int g = blockIdx.x / a.R;
   ClusterInbox tr;
   tr.box = ll_box;
-  tr.row = (int64_t)blockDim.x * a.E * WPE;
+  tr.row = (int64_t)blockDim.x * (EM == 1 ? 1 : a.E) * WPE;
   tr.q = (uint32_t)((r == a.R - 1) ? 0 : r + 1);
   // zero this CTA's rows, then meet: no peer stores into them before
   const int64_t words = (int64_t)(a.rounds - 1) * tr.row;
   for (int64_t i = threadIdx.x; i < words; i += blockDim.x) ll_box[i] = 0;
   cluster_meet();
-  ll_rounds<D, OP>(a, tr, r, g);
+  ll_rounds<D, OP, EM>(a, tr, r, g);
   // nobody leaves while a peer may still store into its rows
   cluster_meet();
 }
 
-const void* ll_fn(int dtype, int op) {
+// The instantiation for E positions per thread: one position (the usual
+// small call) has code of its own, without the loops over positions.
+const void* ll_fn(int dtype, int op, int E) {
   const void* fn = nullptr;
   with_dtype_op(dtype, op, [&](auto d, auto o) {
-    fn = reinterpret_cast<const void*>(&ll_kernel<decltype(d), decltype(o)::value>);
+    using D = decltype(d);
+    constexpr int OP = decltype(o)::value;
+    fn = E == 1 ? reinterpret_cast<const void*>(&ll_kernel<D, OP, 1>)
+                : reinterpret_cast<const void*>(&ll_kernel<D, OP, kLLMaxE>);
     return cudaSuccess;
   });
   return fn;
 }
 
-const void* ll_cluster_fn(int dtype, int op) {
+const void* ll_cluster_fn(int dtype, int op, int E) {
   const void* fn = nullptr;
   with_dtype_op(dtype, op, [&](auto d, auto o) {
-    fn = reinterpret_cast<const void*>(&ll_cluster_kernel<decltype(d), decltype(o)::value>);
+    using D = decltype(d);
+    constexpr int OP = decltype(o)::value;
+    fn = E == 1 ? reinterpret_cast<const void*>(&ll_cluster_kernel<D, OP, 1>)
+                : reinterpret_cast<const void*>(&ll_cluster_kernel<D, OP, kLLMaxE>);
     return cudaSuccess;
   });
   return fn;
@@ -365,13 +383,13 @@ cudaLaunchConfig_t ll_cluster_config(const LLArgs& a, int threads, size_t smem, 
 }  // namespace
 
 cudaError_t ll_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
-  const void* fn = ll_fn(dtype, op);
+  const void* fn = ll_fn(dtype, op, kLLMaxE);   // the larger register count of the two
   if (!fn) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
 }
 
 cudaError_t launch_ll(int dtype, int op, const LLArgs& a, int threads, cudaStream_t st) {
-  const void* fn = ll_fn(dtype, op);
+  const void* fn = ll_fn(dtype, op, a.E);
   if (!fn || !ll_shape_ok(a, threads) || !a.inbox) return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
@@ -387,17 +405,18 @@ size_t ll_cluster_smem_bytes(const LLArgs& a, int threads, int elem_bytes) {
 cudaError_t prepare_ll_cluster() {
   cudaError_t err = cudaSuccess;
   for (int dt = RA_F32; dt <= RA_I64 && err == cudaSuccess; ++dt)
-    for (int op = RA_SUM; op <= RA_MAX && err == cudaSuccess; ++op) {
-      const void* fn = ll_cluster_fn(dt, op);
-      err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kLLClusterMaxSmem);
-    }
+    for (int op = RA_SUM; op <= RA_MAX && err == cudaSuccess; ++op)
+      for (int E : {1, kLLMaxE}) {
+        const void* fn = ll_cluster_fn(dt, op, E);
+        if (err == cudaSuccess) err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err == cudaSuccess)
+          err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kLLClusterMaxSmem);
+      }
   return err;
 }
 
 cudaError_t ll_cluster_capacity(int dtype, int op, const LLArgs& a, int threads, size_t smem, int* clusters) {
-  const void* fn = ll_cluster_fn(dtype, op);
+  const void* fn = ll_cluster_fn(dtype, op, a.E);
   if (!fn || a.R < 2 || a.R > 16) return cudaErrorInvalidValue;
   LLArgs one = a;
   one.G = 1;
@@ -407,7 +426,7 @@ cudaError_t ll_cluster_capacity(int dtype, int op, const LLArgs& a, int threads,
 }
 
 cudaError_t launch_ll_cluster(int dtype, int op, const LLArgs& a, int threads, size_t smem, cudaStream_t st) {
-  const void* fn = ll_cluster_fn(dtype, op);
+  const void* fn = ll_cluster_fn(dtype, op, a.E);
   if (!fn || !ll_shape_ok(a, threads) || a.R > 16 || smem > (size_t)kLLClusterMaxSmem ||
       smem < ll_cluster_smem_bytes(a, threads, a.elem_bytes))
     return cudaErrorInvalidValue;
