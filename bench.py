@@ -130,6 +130,82 @@ def profile_traffic(workload, units_full):
     return int(m_bytes.group(1)) * units_full / int(m_units.group(1)), path
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, by ctypes; read-only queries) about every millisecond on a
+    thread, so that even a timed region of a few milliseconds holds several
+    samples.  Same interface and result as ClockSampler; start() returns
+    None where NVML cannot be loaded or the GPU not found."""
+
+    SM = 1   # NVML_CLOCK_SM
+    # clock-event reason bits of NVML's public API
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, gpu_uuid, period_s=0.001, lib=None):
+        self.uuid = gpu_uuid
+        self.period = period_s
+        self.lib = lib
+        self.rows = []
+        self.t_begin = self.t_end = None
+        self._stop = threading.Event()
+
+    def _open(self):
+        import ctypes
+        lib = self.lib or ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            return False
+        self._read_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(h, self.SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.h, self.ctypes, self.nvml = h, ctypes, lib
+        return True
+
+    def start(self):
+        try:
+            if not self._open():
+                return None
+        except (OSError, AttributeError):
+            return None
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        return self
+
+    def sample_now(self):
+        c, m = self.ctypes.c_uint(0), self.ctypes.c_ulonglong(0)
+        ok = self.nvml.nvmlDeviceGetClockInfo(self.h, self.SM, self.ctypes.byref(c)) == 0
+        ok = ok and self._read_reasons(self.h, self.ctypes.byref(m)) == 0
+        if ok:
+            self.rows.append((time.monotonic(), float(c.value), int(m.value)))
+
+    def _read(self):
+        while not self._stop.is_set():
+            self.sample_now()
+            time.sleep(self.period)
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
+
+    def stop(self):
+        self._stop.set()
+        self.th.join(timeout=2)
+        inside = [r for r in self.rows if self.t_begin <= r[0] <= self.t_end]
+        if not inside:
+            return None
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside),
+                "note": "NVML samples inside the timed region (a thread about every millisecond, and the "
+                        "timing thread itself while the device runs the enqueued steps)"}
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while a region runs."""
 
@@ -282,7 +358,9 @@ def run_gpu_arm(args):
         gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     except Exception:
         pass
-    clocks = ClockSampler(gpu_id).start() if (rank == 0 and not args.no_clocks) else None
+    clocks = None
+    if rank == 0 and not args.no_clocks:
+        clocks = NvmlClockSampler(gpu_id).start() or ClockSampler(gpu_id).start()
     stream = torch.cuda.current_stream()
     call = h.prepare("allreduce", ins, outs, stream)
     for _ in range(args.warmup):
@@ -302,6 +380,13 @@ def run_gpu_arm(args):
         call()
         ev[i][1].record(stream)
     t1.record(stream)
+    if clocks and hasattr(clocks, "sample_now"):
+        # the device is still running the enqueued steps: sample from this
+        # thread until it is done (a sampling thread may not get the
+        # interpreter in a region of a few milliseconds)
+        while not t1.query():
+            clocks.sample_now()
+            time.sleep(0.0005)
     torch.cuda.synchronize()
     if clocks:
         clocks.end()

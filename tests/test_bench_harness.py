@@ -91,3 +91,61 @@ def test_threaded_cpu_baseline_catches_a_wrong_start_rank():
     assert np.all(ring.ring_allreduce(x, op)[0] == 0.0)
     rotated = [x[(r + 1) % R] for r in range(R)]   # every element's fold starts one rank later
     assert np.all(bench.oracle_threaded_allreduce(rotated, op, 3)[0] == 2.0)
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: an SM clock and a clock-event reason mask
+    that a test sets, read through the same calls and pointers."""
+
+    def __init__(self, mhz, mask, max_mhz=2070):
+        self.mhz, self.mask, self.max_mhz = mhz, mask, max_mhz
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlDeviceGetHandleByUUID(self, uuid, handle):
+        assert uuid.startswith(b"GPU-")
+        handle._obj.value = 1
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, out):
+        out._obj.value = self.max_mhz
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        assert kind == 1   # SM clock
+        out._obj.value = self.mhz
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+        out._obj.value = self.mask
+        return 0
+
+
+def test_nvml_clock_sampler_reads_clocks_and_reasons():
+    import time
+    import bench
+    fake = _FakeNvml(1980, 0x4 | 0x1)   # power cap, plus an idle bit that is not reported
+    s = bench.NvmlClockSampler("GPU-0000", lib=fake).start()
+    assert s is not None
+    s.begin()
+    time.sleep(0.03)
+    s.end()
+    r = s.stop()
+    assert r["sm_mhz"] == 1980 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"]
+    assert r["samples"] >= 3          # about one per millisecond
+    fake2 = _FakeNvml(2070, 0x8 | 0x40)
+    s = bench.NvmlClockSampler("GPU-0000", lib=fake2).start()
+    s.begin()
+    time.sleep(0.01)
+    s.end()
+    assert s.stop()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_nvml_clock_sampler_without_nvml_falls_back():
+    import bench
+    class NoInit(_FakeNvml):
+        def nvmlInit_v2(self):
+            return 9
+    assert bench.NvmlClockSampler("GPU-0000", lib=NoInit(0, 0)).start() is None
