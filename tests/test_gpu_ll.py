@@ -332,3 +332,17 @@ def test_protocol_option_values(ra):
         assert e.value.status == ra.Status.ERR_INVALID
         h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
         assert h.get_option(ra.Option.PROTOCOL) == ra.Protocol.LL
+
+
+@pytest.mark.parametrize("protocol,R,n", [("LL", 8, 8 * 58000 + 3), ("LL_CLUSTER", 8, 2**20 + 3),
+                                          ("LL_CLUSTER", 16, 16 * 40000 + 1)])
+def test_ll_largest_default_shapes(ra, protocol, R, n):
+    """LL near its co-residency limit (chunks of 58001 elements: four positions
+    per thread over some 57 channels of one cooperative launch) and
+    LL_CLUSTER with hundreds of independent clusters running in waves: both
+    bitwise the oracle's ring."""
+    x = inputs.generate(R, n, "f32", "normal", seed=R + n % 97)
+    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
+    got = run_ll(ra, x, "f32", "sum", protocol=protocol)
+    for r in range(R):
+        assert_bitwise_equal(got[r], want[r], f"{protocol} R={R} n={n} rank {r}")
