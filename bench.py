@@ -339,7 +339,10 @@ def run_gpu_arm(args):
     w = dict(inputs.WORKLOADS[args.workload])
     R = w["R"]
     n = args.n or w["n"]
-    dtype, op = w["dtype"], w["ops"][0]
+    dtype = w["dtype"]
+    op = args.op or w["ops"][0]
+    if op not in w["ops"]:
+        raise SystemExit(f"workload {args.workload} runs ops {w['ops']}, not {op}")
     b = inputs.itemsize(dtype)
     st_dtype = inputs.storage_dtype(dtype)
 
@@ -478,7 +481,7 @@ def run_gpu_arm(args):
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1
     if rank == 0 and ws == 1 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds, op_name=op)
 
     h.close()
     if rank == 0:
@@ -498,7 +501,7 @@ def workload_config(args, R, n, op, b, ws):
     """The `config` of a bench line: the workload, identical for the GPU arm
     and the reference arm (which times the oracle on a sample of it)."""
     return {
-        "workload": WORKLOAD_TEXT.get(args.workload, args.workload) if args.n is None
+        "workload": WORKLOAD_TEXT.get(args.workload, args.workload).replace(", sum,", f", {op},") if args.n is None
         else f"{args.workload} with n={n}",
         "R": R, "n_per_rank": n, "op": op, "variant": args.variant,
         **({"protocol": args.protocol} if args.protocol != "simple" else {}),
@@ -591,12 +594,12 @@ def link_floor(torch, pin_in, pin_out, dev_in, dev_out, steps):
 
 # ------------------------------------------------------------- CPU oracle
 
-def _oracle_step_seconds(workload, n_sample):
+def _oracle_step_seconds(workload, n_sample, op_name=None):
     from oracle import elementops, ring
     from ring_allreduce_gb300 import inputs
     w = inputs.WORKLOADS[workload]
     x = inputs.generate(w["R"], n_sample, w["dtype"], w["dist"], w["seed"])
-    op = elementops.get_op(w["dtype"], w["ops"][0])
+    op = elementops.get_op(w["dtype"], op_name or w["ops"][0])
     t = time.perf_counter()
     ring.ring_allreduce(x, op)
     return time.perf_counter() - t, x, op
@@ -672,7 +675,7 @@ def _timed_calls(fn, budget_s):
     return times
 
 
-def cpu_baseline(workload, budget_s=15.0, n_sample=None):
+def cpu_baseline(workload, budget_s=15.0, n_sample=None, op_name=None):
     """Time the oracle, as it stands, on R ranks of a sample of the
     workload, on one thread (value) and split over element ranges on every
     core this process may use (`threaded`); values are algbw on the sample."""
@@ -681,7 +684,7 @@ def cpu_baseline(workload, budget_s=15.0, n_sample=None):
     w = inputs.WORKLOADS[workload]
     b = inputs.itemsize(w["dtype"])
     n_sample = n_sample or w["n"]
-    _, x, op = _oracle_step_seconds(workload, n_sample)
+    _, x, op = _oracle_step_seconds(workload, n_sample, op_name)
     cores = host_cores()
     times = _timed_calls(lambda: ring.ring_allreduce(x, op), budget_s * 2 / 3)
     times_mt = _timed_calls(lambda: oracle_threaded_allreduce(x, op, cores), budget_s / 3)
@@ -710,7 +713,7 @@ def run_reference_arm(args):
     # minutes (25 calls of the R = 8 x 2^24 fp32 headline: ~4 s), else the
     # largest power-of-two sample that does, named in `config`
     budget = 180.0 / max(1, args.steps + args.warmup)
-    t_full, x, op = _oracle_step_seconds(args.workload, n_full)
+    t_full, x, op = _oracle_step_seconds(args.workload, n_full, args.op)
     n_sample = n_full
     if t_full > budget:
         n_sample = 2**12
@@ -719,7 +722,7 @@ def run_reference_arm(args):
             if t > budget:
                 break
             n_sample *= 2
-        _, x, op = _oracle_step_seconds(args.workload, n_sample)
+        _, x, op = _oracle_step_seconds(args.workload, n_sample, args.op)
     from oracle import ring
     for _ in range(args.warmup):
         ring.ring_allreduce(x, op)
@@ -740,7 +743,7 @@ def run_reference_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
         "data": "synthetic",
-        "config": workload_config(cfg_args, w["R"], n_sample, w["ops"][0], b, ws),
+        "config": workload_config(cfg_args, w["R"], n_sample, args.op or w["ops"][0], b, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
                          "host_cores": host_cores()},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1006,6 +1009,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="r8_f32", choices=["r8_f32", "r8_bf16", "r16_i32", "r4_small"])
+    ap.add_argument("--op", default=None, choices=["sum", "max"],
+                    help="reduction of the workload (default: its first; r16_i32 runs sum and max)")
     ap.add_argument("--n", type=int, default=None, help="override n per rank (profiling of a smaller case)")
     ap.add_argument("--variant", default="auto", choices=["auto", "direct", "ring", "persistent", "pipelined", "local"])
     ap.add_argument("--protocol", default="simple", choices=["simple", "ll", "ll_cluster"],
