@@ -48,14 +48,45 @@ def ra():
     return binding
 
 
+def _ll_configs(count=80, seed=20261203):
+    """The pipelined variant's flag-in-data protocols: LL (R up to 32) and
+    LL_CLUSTER (R up to 16), n within their limits (the LL inbox, the
+    cluster's shared memory), every collective but host buffers."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(count):
+        protocol = ["LL", "LL_CLUSTER"][int(rng.integers(2))]
+        Rs = [2, 3, 4, 5, 7, 8, 11, 16] + ([23, 32] if protocol == "LL" else [])
+        R = int(rng.choice(Rs))
+        n = int(rng.choice([1, 2, R - 1, R, 3 * R + 1, int(rng.integers(1, 5000)), int(rng.integers(5000, 60000))]))
+        n = max(n, 1)
+        dtype, op = DTYPE_OPS[int(rng.integers(len(DTYPE_OPS)))]
+        kind = KINDS[int(rng.integers(3))]
+        inplace = bool(rng.integers(2)) and kind in ("allreduce", "reduce_scatter")
+        out.append((1000 + i, R, n, dtype, op, "pipelined-" + protocol, kind, inplace))
+    return out
+
+
 @pytest.mark.parametrize("cfg", _configs(), ids=lambda c: "-".join(str(v) for v in c))
 def test_random_configuration(ra, cfg):
+    _run_configuration(ra, cfg)
+
+
+@pytest.mark.parametrize("cfg", _ll_configs(), ids=lambda c: "-".join(str(v) for v in c))
+def test_random_ll_configuration(ra, cfg):
+    _run_configuration(ra, cfg)
+
+
+def _run_configuration(ra, cfg):
     i, R, n, dtype, op, variant, kind, inplace = cfg
     o = elementops.get_op(dtype, op)
     x = inputs.generate(R, n, dtype, DIST[dtype], seed=7000 + i)
     st = inputs.storage_dtype(dtype)
     plan = ring.chunk_plan(R, n)
+    variant, _, protocol = variant.partition("-")
     with ra.RingAllReduce(R, n, dtype, op, variant=variant) as h:
+        if protocol:
+            h.set_option(ra.Option.PROTOCOL, ra.Protocol[protocol])
         if kind == "allreduce_host":
             ins = [torch.from_numpy(v.view(f"i{v.dtype.itemsize}").copy()).pin_memory() for v in x]
             outs = [torch.zeros_like(t).pin_memory() for t in ins]
