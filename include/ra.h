@@ -117,12 +117,14 @@ typedef enum ra_variant {
                                  finished the previous round on it
                                  (per-predecessor progress flags; rounds of
                                  different sub-slices overlap; RA_OPT_PROTOCOL
-                                 chooses how the messages travel).  Not
-                                 capturable into a CUDA graph: each call
-                                 passes the kernel where its flags start, and
-                                 a replay would reuse that value
-                                 (RA_ERR_UNSUPPORTED while the stream
-                                 captures) */
+                                 chooses how the messages travel).  Each call
+                                 is handed where its flags start; every CTA
+                                 also keeps that in device memory, and a call
+                                 made while its stream is being captured into
+                                 a CUDA graph -- and every call after it
+                                 until ra_get_device_status resets the handle
+                                 -- takes it from there, so replays continue
+                                 the count (a few percent slower at large n) */
   RA_VARIANT_LOCAL = 5        /* one launch, each CTA running every ring round
                                  for one slice of every chunk: the ranks'
                                  messages pass through shared memory, the
@@ -139,11 +141,11 @@ typedef enum ra_barrier {
                                  barrier a counting barrier", section "Fix") */
   RA_BARRIER_PER_PEER = 1,    /* one signal per (channel, round, waiter, peer),
                                  the design that page replaced; a wait that runs
-                                 out can name the missing peer.  Each call
-                                 passes the kernel its epoch, so it is not
-                                 capturable into a CUDA graph
-                                 (RA_ERR_UNSUPPORTED while the stream
-                                 captures) */
+                                 out can name the missing peer.  Each call is
+                                 handed its epoch; every CTA also keeps it in
+                                 device memory, and calls captured into a
+                                 CUDA graph (and the calls after them, until
+                                 a reset) take it from there */
   RA_BARRIER_CLUSTER = 2      /* the R CTAs of a channel form one thread-block
                                  cluster and meet at the hardware cluster
                                  barrier (R <= 16, else RA_ERR_UNSUPPORTED);
@@ -167,7 +169,14 @@ typedef enum ra_protocol {
                                  the words themselves, so a ring hop is one
                                  store and one poll, with no fence and no
                                  separate flag.  Twice the bytes per element
-                                 (four times for 16-bit elements). */
+                                 (four times for 16-bit elements).  Every CTA
+                                 keeps the flag its next call starts at in
+                                 device memory; calls captured into a CUDA
+                                 graph (and the calls after them, until a
+                                 reset) start from there, and a replayed call
+                                 whose flags would pass 2^32 - 1 does nothing
+                                 and reports error code 6 (the status call
+                                 zeroes the inbox). */
   RA_PROTOCOL_LL_CLUSTER = 2  /* the same words, stored straight into the
                                  successor's shared memory: the R CTAs of a
                                  channel form one thread-block cluster (R <=
@@ -273,7 +282,7 @@ typedef struct ra_device_error {
   uint32_t code;      /* 0 = none; 1 = counting-barrier wait ran out; 2 = bulk-copy wait
                          ran out; 3 = per-peer barrier wait ran out; 4 = pipelined
                          flag wait ran out; 5 = RA_PROTOCOL_LL message wait ran
-                         out */
+                         out; 6 = a replayed RA_PROTOCOL_LL call ran out of flags */
   int32_t round;      /* barrier round (0-based), ring round (codes 4, 5) or AllGather round (code 2) */
   int32_t rank;       /* waiting rank */
   int32_t channel;    /* channel: the CTA index within its rank */

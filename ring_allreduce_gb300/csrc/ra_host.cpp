@@ -78,6 +78,10 @@ struct SlotRegion {
   // (0 after a reset, the seeded value after ra_seed_signals, moved by the
   // ring rounds with every call)
   uint64_t shadow_base = 0;
+  // per-peer and flags: a launch of this region was captured into a CUDA
+  // graph, so the host's epoch / shadow start no longer follow the device:
+  // every launch takes them from the CTAs' own copies until the next reset
+  bool from_memory = false;
 };
 
 enum Kind { kKindAllReduce = 0, kKindReduceScatter = 1, kKindAllGather = 2 };
@@ -112,8 +116,10 @@ struct ra_ctx {
   // RA_PROTOCOL_LL: the inbox (allocated on first use) and the flag the next
   // call's first message carries
   uint64_t* ll_inbox = nullptr;
-  size_t ll_inbox_words = 0;
+  size_t ll_inbox_words = 0;   // the inbox's words, then one flag-base word per co-resident CTA
+  size_t ll_alloc_words = 0;
   uint64_t ll_flag = 1;
+  bool ll_from_memory = false;   // an LL launch was captured: bases come from the CTAs' copies
   int ctas = 0;
   int check_pointers = 1;
   long long skip = -1;
@@ -635,8 +641,10 @@ ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
   if (!reg.d) {
     const int bps = sync == ra::kSyncFlags ? h->pipe_blocks_per_sm : h->persist_blocks_per_sm;
     const size_t cap = region_entries(h, sync, reg.rounds, gmax_channels(h, bps), kMaxSlices);
-    // the pipelined flags come with their waiters' shadows, laid out as the flags
-    const size_t words = sync == ra::kSyncFlags ? 2 * cap : cap;
+    // the pipelined flags come with their waiters' shadows, laid out as the
+    // flags; the per-peer slots with each CTA's copy of its epoch ([G][R],
+    // well within cap words)
+    const size_t words = 2 * cap;
     if (cap > 0) {
       cudaError_t e = cudaMalloc(&reg.d, words * sizeof(uint64_t));
       if (e == cudaSuccess) e = cudaMemset(reg.d, 0, words * sizeof(uint64_t));
@@ -645,7 +653,7 @@ ra_status ensure_region(ra_ctx* h, int sync, int kind, SlotRegion** out) {
         reg.d = nullptr;
         return cuda_fail(e, "signal slot allocation");
       }
-      if (sync == ra::kSyncFlags) reg.shadows = reg.d + cap;
+      reg.shadows = reg.d + cap;
     }
     reg.cap = cap;
     reg.owned = true;
@@ -685,7 +693,7 @@ void debug_begin(const ra_ctx* h) {
     for (auto& reg : row)
       if (reg.d) debug_add(reg.d, region_words(reg) * sizeof(uint64_t));
   debug_add(h->d_err, sizeof(ra_device_error));
-  if (h->ll_inbox) debug_add(h->ll_inbox, h->ll_inbox_words * sizeof(uint64_t));
+  if (h->ll_inbox) debug_add(h->ll_inbox, h->ll_alloc_words * sizeof(uint64_t));
   if (h->host_dev) debug_add(h->host_dev, 4 * (size_t)h->R * h->host_n_pad * elem_bytes(h->dtype));
 }
 
@@ -734,6 +742,7 @@ ra_status prepare_region(SlotRegion& reg, int G, int J, cudaStream_t st) {
     cudaError_t e = reset_region(reg, st);
     if (e != cudaSuccess) return cuda_fail(e, "signal slot reset");
     reg.shadow_base = 0;
+    reg.from_memory = false;
     reg.G = G;
     reg.J = J;
     reg.calls = 0;
@@ -777,16 +786,15 @@ ra_status run_persistent_cluster(ra_ctx* h, int kind, int mode, const void* cons
 
 // Launches whose per-call state the host passes in as a kernel parameter
 // (the per-peer barrier's epoch, the pipelined variant's shadow start and
-// message flags) would replay that value unchanged from a CUDA graph, and a
-// replay would take an earlier call's progress for its own: they refuse a
-// stream that is being captured.
-ra_status refuse_capture(cudaStream_t st, const char* what) {
+// LL flag base) would replay that value unchanged from a CUDA graph.  Their
+// CTAs also keep that state in device memory, each its own copy; a launch
+// made on a stream that is being captured -- and every launch of the same
+// state after it, until a reset -- takes it from there instead.
+ra_status stream_capturing(cudaStream_t st, bool* capturing) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   const cudaError_t e = cudaStreamIsCapturing(st, &cs);
   if (e != cudaSuccess) return cuda_fail(e, "stream capture status");
-  if (cs != cudaStreamCaptureStatusNone)
-    return fail(RA_ERR_UNSUPPORTED, "%s cannot be captured into a CUDA graph (its per-call state comes from the host)",
-                what);
+  *capturing = cs != cudaStreamCaptureStatusNone;
   return RA_OK;
 }
 
@@ -794,7 +802,8 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
                          cudaStream_t st) {
   if (h->barrier == RA_BARRIER_CLUSTER) return run_persistent_cluster(h, kind, mode, in, out, st);
   const int sync = h->barrier == RA_BARRIER_PER_PEER ? ra::kSyncPerPeer : ra::kSyncCounting;
-  ra_status s = sync == ra::kSyncPerPeer ? refuse_capture(st, "the per-peer barrier") : RA_OK;
+  bool capturing = false;
+  ra_status s = sync == ra::kSyncPerPeer ? stream_capturing(st, &capturing) : RA_OK;
   if (s != RA_OK) return s;
   SlotRegion* reg = nullptr;
   s = ensure_region(h, sync, kind, &reg);
@@ -819,6 +828,8 @@ ra_status run_persistent(ra_ctx* h, int kind, int mode, const void* const* in, v
   a.shadows = reg->shadows;
   a.epoch = (uint64_t)(reg->calls + 1);
   a.shadow_base = 0;
+  if (capturing) reg->from_memory = true;
+  a.from_memory = reg->from_memory ? 1 : 0;
   a.bits = h->signal_bits;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -845,7 +856,7 @@ constexpr size_t kLLInboxBytes = (size_t)64 << 20;   // most bytes of the RA_PRO
 
 // The pipelined variant with flag-in-data messages (ra_ll.cu).
 ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
-                           cudaStream_t st) {
+                           bool capturing, cudaStream_t st) {
   ra::LLArgs a;
   std::memset(&a, 0, sizeof(a));
   a.p = make_ptrs(h, in, out);
@@ -879,25 +890,34 @@ ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in,
   if ((long long)a.G * h->R > cap)
     return fail(RA_ERR_UNSUPPORTED, "LL grid of %d x %d CTAs cannot be co-resident (%d fit)", h->R, a.G, cap);
   if (!h->ll_inbox) {
-    cudaError_t e = cudaMalloc(&h->ll_inbox, words * sizeof(uint64_t));
-    if (e == cudaSuccess) e = cudaMemset(h->ll_inbox, 0, words * sizeof(uint64_t));
+    // the inbox, then each co-resident CTA's copy of its next flag base
+    const size_t all = words + (size_t)std::max(cap, 1);
+    cudaError_t e = cudaMalloc(&h->ll_inbox, all * sizeof(uint64_t));
+    if (e == cudaSuccess) e = cudaMemset(h->ll_inbox, 0, all * sizeof(uint64_t));
     if (e != cudaSuccess) {
       if (h->ll_inbox) cudaFree(h->ll_inbox);
       h->ll_inbox = nullptr;
       return cuda_fail(e, "LL inbox allocation");
     }
     h->ll_inbox_words = words;
-    h->ll_flag = 1;
-    debug_add(h->ll_inbox, words * sizeof(uint64_t));
+    h->ll_alloc_words = all;
+    h->ll_from_memory = false;   // any flag (1 by default, or as RA_OPT_LL_FLAG set it) suits a zeroed inbox
+    debug_add(h->ll_inbox, all * sizeof(uint64_t));
   }
-  // flags never wrap: a call whose flags would pass 2^32 - 1 starts again
-  // at 1 on a zeroed inbox (0 marks a word never written)
-  if (h->ll_flag + (uint64_t)a.rounds > 0xFFFFFFFFull) {
-    const cudaError_t e = cudaMemsetAsync(h->ll_inbox, 0, h->ll_inbox_words * sizeof(uint64_t), st);
+  if (capturing) h->ll_from_memory = true;
+  // flags never wrap: a call from the host whose flags would pass 2^32 - 1
+  // starts again at 1 on a zeroed inbox (0 marks a word never written); a
+  // replayed call whose flags would wrap gives up (code 6) and the status
+  // call that reports it zeroes the inbox
+  if (!h->ll_from_memory && h->ll_flag + (uint64_t)a.rounds > 0xFFFFFFFFull) {
+    const cudaError_t e = cudaMemsetAsync(h->ll_inbox, 0, h->ll_alloc_words * sizeof(uint64_t), st);
     if (e != cudaSuccess) return cuda_fail(e, "LL inbox reset");
     h->ll_flag = 1;
   }
   a.inbox = h->ll_inbox;
+  a.bases = h->ll_inbox + h->ll_inbox_words;
+  a.nbases = (int)(h->ll_alloc_words - h->ll_inbox_words);
+  a.from_memory = h->ll_from_memory ? 1 : 0;
   a.flag_base = (uint32_t)h->ll_flag;
   a.timeout_ns = h->timeout_ns;
   a.err = h->d_err;
@@ -957,9 +977,10 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
                         cudaStream_t st) {
   // nothing of the cluster form is kept between calls: a graph may replay it
   if (h->protocol == RA_PROTOCOL_LL_CLUSTER) return run_pipelined_ll_cluster(h, kind, mode, in, out, st);
-  ra_status s = refuse_capture(st, "the pipelined variant");
+  bool capturing = false;
+  ra_status s = stream_capturing(st, &capturing);
   if (s != RA_OK) return s;
-  if (h->protocol == RA_PROTOCOL_LL) return run_pipelined_ll(h, kind, mode, in, out, st);
+  if (h->protocol == RA_PROTOCOL_LL) return run_pipelined_ll(h, kind, mode, in, out, capturing, st);
   SlotRegion* reg = nullptr;
   s = ensure_region(h, ra::kSyncFlags, kind, &reg);
   if (s != RA_OK) return s;
@@ -994,6 +1015,8 @@ ra_status run_pipelined(ra_ctx* h, int kind, int mode, const void* const* in, vo
   a.skip_rank = h->skip >= 0 ? (int)(h->skip >> 16) : -1;
   a.skip_round = h->skip >= 0 ? (int)(h->skip & 0xFFFF) : -1;
   a.shadow_base = reg->shadow_base;
+  if (capturing) reg->from_memory = true;
+  a.from_memory = reg->from_memory ? 1 : 0;
   cudaError_t e = ra::launch_pipelined(h->dtype, h->op, a, ra::kPipeThreads, st);
   if (e != cudaSuccess) return cuda_fail(e, "pipelined kernel launch");
   reg->calls += 1;
@@ -1015,7 +1038,16 @@ ra_status reset_device_state(ra_ctx* h, cudaStream_t st) {
     for (auto& reg : row) {
       reg.calls = 0;
       reg.shadow_base = 0;
+      reg.from_memory = false;
     }
+  if (h->ll_inbox) {
+    // the LL inbox and the CTAs' flag bases start again too (after a
+    // replayed call ran out of flags, the only way back)
+    e = cudaMemset(h->ll_inbox, 0, h->ll_alloc_words * sizeof(uint64_t));
+    if (e != cudaSuccess) return cuda_fail(e, "LL inbox reset");
+    h->ll_flag = 1;
+    h->ll_from_memory = false;
+  }
   return RA_OK;
 }
 
@@ -1597,6 +1629,11 @@ ra_status ra_get_device_status(ra_handle h, void* stream, ra_device_error* err) 
   if (rec.code == 0) return RA_OK;
   ra_status s = reset_device_state(h, st);
   if (s != RA_OK) return s;
+  if (rec.code == 6)
+    return fail(RA_ERR_TIMEOUT,
+                "LL flags exhausted in a call replayed from a CUDA graph (rank %d, channel %d, next flag %llu): "
+                "the inbox is zeroed and the flags start again at 1",
+                rec.rank, rec.channel, (unsigned long long)rec.observed);
   if (rec.code == 5)
     return fail(RA_ERR_TIMEOUT,
                 "device wait gave up: LL message, round %d, rank %d, channel %d, peer %d, flag observed %llu, "

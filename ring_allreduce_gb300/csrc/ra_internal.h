@@ -145,9 +145,13 @@ struct PersistArgs {
   uint64_t* slots;      // counting: [G][rounds-1][R]; per-peer: [G][rounds-1][R][R];
                         // flags: [G][R][J]
   uint64_t* shadows;    // counting: each waiter's shadow, laid out as slots; flags: rank r's
-                        // shadows of its predecessor's flags, [G][R][J] by waiter
+                        // shadows of its predecessor's flags, [G][R][J] by waiter; per-peer:
+                        // each CTA's copy of the epoch of its last call, [G][R]
   uint64_t epoch;       // calls on this slot array since it was zeroed, this one included
   uint64_t shadow_base; // flags: the value every waiter's shadow starts this call at
+  int from_memory;      // per-peer and flags: take the call's epoch / shadow start from the
+                        // CTA's own copy in device memory (moved on by every launch) instead
+                        // of epoch / shadow_base -- for launches a CUDA graph replays
   int bits;             // width of the signal comparisons (rolling order on the low bits), <= 64
   int64_t timeout_ns;
   ra_device_error* err;

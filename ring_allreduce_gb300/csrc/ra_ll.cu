@@ -55,7 +55,8 @@
 //
 // Waits are bounded (timeout_ns, two clocks); one that runs out records code
 // 5 (round, rank, channel, predecessor, flag seen, flag expected) and the
-// thread stops; every other waiter stops once it sees the record.
+// thread stops; every other waiter stops once it sees the record.  A
+// replayed LL launch whose flags would wrap records code 6 and does nothing.
 #include "ra_device.cuh"
 #include "ra_ll.h"
 
@@ -302,6 +303,41 @@ __global__ void __launch_bounds__(kLLThreads, 3) ll_kernel(const LLArgs a) {
   constexpr int WPE = sizeof(typename D::T) == 8 ? 2 : 1;
   const int r = blockIdx.x % a.R;
   const int g = blockIdx.x / a.R;
+  // The flag base.  Each CTA keeps its own copy of the flag its next call
+  // starts at, in device memory, and moves it on itself (no other CTA reads
+  // it): a launch from the host is handed the base and writes the next one
+  // down; a launch a CUDA graph replays (from_memory) takes its base from
+  // there -- 0, never written, is 1 on the inbox zeroed when it was made --
+  // and gives up with code 6, touching nothing, when its flags would pass
+  // 2^32 - 1 (every CTA holds the same value, so every CTA gives up).
+  uint32_t base = a.flag_base;
+  if (a.from_memory) {
+    __shared__ uint32_t s_base;
+    if (threadIdx.x == 0) {
+      uint64_t next = (uint64_t)ld_l2_scalar(reinterpret_cast<const int64_t*>(a.bases + blockIdx.x));
+      if (next == 0) next = 1;
+      if (next + (uint64_t)a.rounds > 0xFFFFFFFFull) {
+        record_wait_error(a.err, 6u, 0, r, g, -1, next, 0xFFFFFFFFull);
+        next = 0;
+      }
+      s_base = (uint32_t)next;
+    }
+    __syncthreads();
+    base = s_base;
+    if (base == 0) return;
+  }
+  {
+    // the next base: this CTA's copy; a launch from the host also sets the
+    // copies of the CTAs beyond its grid (CTA 0's threads), so that every
+    // copy agrees whatever grid a later launch has
+    const unsigned long long nb = (unsigned long long)base + (unsigned long long)a.rounds;
+    auto put = [&](int i) {
+      if (RA_ACCESS_OK(a.bases + i, 8u, 2u)) __stcg(reinterpret_cast<unsigned long long*>(a.bases + i), nb);
+    };
+    if (threadIdx.x == 0) put((int)blockIdx.x);
+    if (!a.from_memory && blockIdx.x == 0)
+      for (int i = (int)gridDim.x + (int)threadIdx.x; i < a.nbases; i += (int)blockDim.x) put(i);
+  }
   GlobalInbox tr;
   tr.inbox = a.inbox;
   tr.row = a.plan.C * WPE;
@@ -309,7 +345,7 @@ __global__ void __launch_bounds__(kLLThreads, 3) ll_kernel(const LLArgs a) {
   tr.R = a.R;
   tr.r = r;
   tr.q = (r == a.R - 1) ? 0 : r + 1;
-  tr.flag_base = a.flag_base;
+  tr.flag_base = base;
   ll_rounds<D, OP, EM>(a, tr, r, g);
 }
 
@@ -390,7 +426,7 @@ cudaError_t ll_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
 
 cudaError_t launch_ll(int dtype, int op, const LLArgs& a, int threads, cudaStream_t st) {
   const void* fn = ll_fn(dtype, op, a.E);
-  if (!fn || !ll_shape_ok(a, threads) || !a.inbox) return cudaErrorInvalidValue;
+  if (!fn || !ll_shape_ok(a, threads) || !a.inbox || !a.bases || a.R * a.G > a.nbases) return cudaErrorInvalidValue;
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<LLArgs*>(&a)};

@@ -30,6 +30,9 @@ struct LLArgs {
   int rounds;           // ring rounds this call runs; messages 0 .. rounds-2
   uint64_t* inbox;      // LL: [message][receiving rank][plan.C * wpe] words
   uint32_t flag_base;   // LL: message t of this call carries flag flag_base + t (no wrap within a call)
+  uint64_t* bases;      // LL: each CTA's copy of the flag its next call starts at, [nbases >= R*G]
+  int nbases;
+  int from_memory;      // LL: take the flag base from the CTA's copy (a launch a CUDA graph replays)
   int64_t timeout_ns;
   ra_device_error* err;
   int skip_rank;        // failure injection: this rank sends nothing from round skip_round on

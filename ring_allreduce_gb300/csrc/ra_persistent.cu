@@ -94,7 +94,8 @@ __device__ __forceinline__ bool counting_barrier(const PersistArgs& a, int g, in
 // slots every one holds k (the call's epoch), and the waiter reads all R-1
 // (readSignal, one lane of warp 0 per peer) until each has reached the epoch.
 // A wait that runs out can name the peer that did not arrive.
-__device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, int t, int r, int* s_abort) {
+__device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, const uint64_t* s_epoch, int g, int t,
+                                                 int r, int* s_abort) {
   __syncthreads();
   const int R = a.R;
   uint64_t* round_slots = a.slots + ((int64_t)g * (a.rounds - 1) + t) * R * R;   // [waiter][peer]
@@ -107,6 +108,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
   }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
+    const uint64_t epoch = *s_epoch;
     const uint64_t* mine = round_slots + (int64_t)r * R;
     const bool active = lane < R && lane != r;
     const Deadline limit(a.timeout_ns);
@@ -116,7 +118,7 @@ __device__ __forceinline__ bool per_peer_barrier(const PersistArgs& a, int g, in
       uint64_t v = 0;
       if (active) {
         v = sig::read(mine + lane, a.bits);   // acquire, by the lane that observes the slot
-        ok = sig::reached(v, a.epoch, a.bits);
+        ok = sig::reached(v, epoch, a.bits);
       }
       const unsigned missing = __ballot_sync(0xffffffffu, !ok);
       if (missing == 0u) break;
@@ -223,6 +225,21 @@ persistent_kernel(const PersistArgs a) {
   const int R = a.R, GV = a.G * a.J;
   const int r = blockIdx.x % R;
   const int p = (r == 0) ? R - 1 : r - 1;
+  // The per-peer barrier's epoch: every slot of a waiter holds the number of
+  // calls it took part in.  Each CTA keeps its own copy of that count in
+  // device memory and moves it on itself (no other CTA reads it), so a launch
+  // a CUDA graph replays takes its epoch from there (from_memory); a launch
+  // from the host is handed the count and writes it down.
+  __shared__ uint64_t s_epoch;
+  if (a.sync == kSyncPerPeer && a.rounds > 1) {
+    uint64_t* mine = a.shadows + blockIdx.x;
+    if (threadIdx.x == 0) {
+      const uint64_t e = a.from_memory ? sig::load_shadow(mine).v + 1 : a.epoch;
+      sig::store_shadow(mine, sig::Shadow{e});
+      s_epoch = e;
+    }
+    __syncthreads();
+  }
   // pass j of channel c is virtual channel c J + j of G J (one pass: c)
   for (int g = blockIdx.x / R * a.J, gend = g + a.J; g < gend; ++g) {
     for (int t = 0; t < a.rounds; ++t) {
@@ -263,7 +280,7 @@ persistent_kernel(const PersistArgs a) {
           cluster_barrier();
           continue;
         }
-        const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, g, t, r, &s_abort)
+        const bool go = a.sync == kSyncPerPeer ? per_peer_barrier(a, &s_epoch, g, t, r, &s_abort)
                                                 : counting_barrier(a, g, t, r, shadow, &s_abort);
         if (!go) return;
       }

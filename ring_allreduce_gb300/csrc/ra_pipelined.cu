@@ -132,11 +132,20 @@ pipelined_kernel(const PersistArgs a) {
   // equal -- reset or seeded together, each moved by the call's rounds -- at
   // a value the host keeps with the flags and passes in (a.shadow_base), so
   // the waiter holds its shadow in a register for the launch (reading it
-  // back from device memory here measured 5-12 % slower calls on GB300).
+  // back from device memory here measured 5-12 % slower calls on GB300; a
+  // launch a CUDA graph replays does read it back: from_memory).
   // Thread j keeps the copy of sub-slice j in device memory where it stands
   // after the call -- moved past every round's publication, the last one
   // too, which nobody waits on -- since nothing reads it during the launch.
-  const sig::Shadow start{a.shadow_base};
+  sig::Shadow start{a.shadow_base};
+  if (a.from_memory) {
+    // a launch a CUDA graph replays: the start is where this waiter's own
+    // shadows stand (all J alike; only this CTA writes them)
+    __shared__ uint64_t s_start;
+    if (threadIdx.x == 0) s_start = sig::load_shadow(a.shadows + ((int64_t)g * R + r) * J).v;
+    __syncthreads();
+    start = sig::Shadow{s_start};
+  }
   if (threadIdx.x < J) {
     sig::Shadow s = start;
     sig::increase_shadow(s, (uint64_t)a.rounds);

@@ -150,6 +150,7 @@ extern "C" ra_status ra_allreduce_noalloc(int R, size_t n, ra_dtype dtype, ra_op
     return record_error(RA_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
   }
   PersistArgs a;
+  a.from_memory = 0;
   for (int r = 0; r < kMaxRanks; ++r) {
     a.p.in[r] = r < R ? in[r] : nullptr;
     a.p.out[r] = r < R ? out[r] : nullptr;

@@ -442,13 +442,17 @@ def test_calls_inside_a_caller_graph(ra, variant, options):
 
 @pytest.mark.parametrize("variant,key,value", [("pipelined", None, None), ("pipelined", "PROTOCOL", "LL"),
                                                ("persistent", "BARRIER", "PER_PEER")])
-def test_host_state_launches_refuse_capture(ra, variant, key, value):
-    """The per-peer barrier's epoch and the pipelined variant's flag starts
-    are kernel parameters a graph would replay unchanged: those calls refuse
-    a capturing stream (before any launch), and work again outside it."""
-    R, n = 4, 4096
-    x = inputs.generate(R, n, "f32", "normal", 2)
-    inp, out = DeviceRanks(R, n, np.float32, host=x), DeviceRanks(R, n, np.float32)
+def test_host_state_launches_replay_from_graphs(ra, variant, key, value):
+    """The per-peer barrier's epoch, the pipelined flags' shadow start and the
+    LL flag base are handed to each launch by the host, and every CTA keeps
+    its own copy in device memory.  A call captured into a CUDA graph -- and
+    every call after it -- takes them from there: one call from the host,
+    three replays on new data and one more call from the host are all
+    bitwise the oracle's, and the signals count all five calls."""
+    R, n = 4, 4 * 3001
+    o = elementops.get_op("f32", "sum")
+    inp = DeviceRanks(R, n, np.float32, host=inputs.generate(R, n, "f32", "normal", 2))
+    out = DeviceRanks(R, n, np.float32)
     with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
         if key:
             h.set_option(ra.Option[key], (ra.Protocol if key == "PROTOCOL" else ra.Barrier)[value])
@@ -457,18 +461,69 @@ def test_host_state_launches_refuse_capture(ra, variant, key, value):
             h.allreduce(inp.views, out.views, side)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
-        with pytest.raises(ra.RAError) as e:
-            with torch.cuda.graph(g, stream=side):
-                h.allreduce(inp.views, out.views, side)
-        assert e.value.status == ra.Status.ERR_UNSUPPORTED
-        assert "captured" in ra.ra_last_error()
-        out2 = DeviceRanks(R, n, np.float32)
+        with torch.cuda.graph(g, stream=side):
+            h.allreduce(inp.views, out.views, side)
+        for seed in (7, 8, 9, 10):
+            x = inputs.generate(R, n, "f32", "normal", seed)
+            inp.big.copy_(DeviceRanks(R, n, np.float32, host=x).big)
+            if seed < 10:
+                g.replay()
+            else:
+                h.allreduce(inp.views, out.views)   # from the host again, after the replays
+            torch.cuda.synchronize()
+            status, err = h.device_status()
+            assert status == ra.Status.OK, (seed, err.as_dict())
+            want, got = ring.ring_allreduce(x, o), out.host()
+            for r in range(R):
+                assert_bitwise_equal(got[r], want[r], f"{variant} {value} seed {seed} rank {r}")
+        if key != "PROTOCOL":
+            calls = 5
+            slots = h.read_signals()[0]
+            assert slots
+            if variant == "pipelined":
+                # every flag: 5 calls x 2(R-1) finished rounds
+                assert all(v == calls * 2 * (R - 1) for v in slots), slots[:8]
+            else:
+                # per-peer slots [channel][round][waiter][peer]: each peer added 1 per call;
+                # a waiter's own column is never written
+                for i, v in enumerate(slots):
+                    assert v == (0 if (i // R) % R == i % R else calls), (i, v)
+
+
+def test_replayed_ll_calls_stop_before_their_flags_wrap(ra):
+    """An LL call from the host whose last message carries 2^32 - 3 leaves
+    2^32 - 1 as the next base; a replayed call cannot start the flags again
+    (it cannot zero the inbox), so it does nothing and reports code 6; the
+    status call zeroes the inbox and the next call is correct."""
+    R, n = 4, 4 * 1500 + 3
+    rounds = 2 * (R - 1)
+    o = elementops.get_op("i32", "sum")
+    x = inputs.generate(R, n, "i32", "int20", seed=3)
+    inp, out = DeviceRanks(R, n, np.int32, host=x), DeviceRanks(R, n, np.int32)
+    want = ring.ring_allreduce(x, o)
+    with ra.RingAllReduce(R, n, "i32", "sum", variant="pipelined") as h:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol.LL)
+        h.set_option(ra.Option.LL_FLAG, 2**32 - 1 - rounds)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            h.allreduce(inp.views, out.views, side)
+        torch.cuda.synchronize()
+        assert h.device_status()[0] == ra.Status.OK
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            h.allreduce(inp.views, out.views, side)
+        g.replay()
+        torch.cuda.synchronize()
+        status, err = h.device_status()
+        assert status == ra.Status.ERR_TIMEOUT and err.code == 6, err.as_dict()
+        assert err.observed == 2**32 - 1
+        assert "exhausted" in ra.ra_last_error()
+        out2 = DeviceRanks(R, n, np.int32)
         h.allreduce(inp.views, out2.views)
         assert h.device_status()[0] == ra.Status.OK
-    want = ring.ring_allreduce(x, elementops.get_op("f32", "sum"))
-    got = out2.host()
-    for r in range(R):
-        assert_bitwise_equal(got[r], want[r])
+        got = out2.host()
+        for r in range(R):
+            assert_bitwise_equal(got[r], want[r], f"after the reset rank {r}")
 
 
 @pytest.mark.parametrize("dtype,op", DTYPE_OPS)
