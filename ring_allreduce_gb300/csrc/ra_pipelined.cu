@@ -116,8 +116,14 @@ __device__ __forceinline__ void copy_range(const typename D::T* src, typename D:
   }
 }
 
-template <class D, int OP>
-__global__ void __launch_bounds__(kPipeThreads, 3)
+// FROM_MEMORY: the instantiation for launches a CUDA graph replays, which
+// read the shadow start back from device memory; launches from the host run
+// the other one, whose code does not carry that path at all.  The channels
+// are sized from the host instantiation's co-resident CTAs; the other is
+// held to 4 CTAs of 512 threads per SM (32 registers), at least as many as
+// the host one allows for any element type, so the same grid fits both.
+template <class D, int OP, bool FROM_MEMORY>
+__global__ void __launch_bounds__(kPipeThreads, FROM_MEMORY ? 4 : 3)
 pipelined_kernel(const PersistArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
@@ -138,7 +144,7 @@ pipelined_kernel(const PersistArgs a) {
   // after the call -- moved past every round's publication, the last one
   // too, which nobody waits on -- since nothing reads it during the launch.
   sig::Shadow start{a.shadow_base};
-  if (a.from_memory) {
+  if (FROM_MEMORY) {
     // a launch a CUDA graph replays: the start is where this waiter's own
     // shadows stand (all J alike; only this CTA writes them)
     __shared__ uint64_t s_start;
@@ -198,23 +204,27 @@ pipelined_kernel(const PersistArgs a) {
   }
 }
 
-static const void* pipelined_select(int dtype, int op) {
+static const void* pipelined_select(int dtype, int op, bool from_memory) {
   const void* fn = nullptr;
   with_dtype_op(dtype, op, [&](auto d, auto o) {
-    fn = reinterpret_cast<const void*>(&pipelined_kernel<decltype(d), decltype(o)::value>);
+    using D = decltype(d);
+    constexpr int OP = decltype(o)::value;
+    fn = from_memory ? reinterpret_cast<const void*>(&pipelined_kernel<D, OP, true>)
+                     : reinterpret_cast<const void*>(&pipelined_kernel<D, OP, false>);
     return cudaSuccess;
   });
   return fn;
 }
 
+// Co-resident CTAs of the host instantiation (the replay one fits as many).
 cudaError_t pipelined_blocks_per_sm(int dtype, int op, int threads, int* blocks) {
-  const void* fn = pipelined_select(dtype, op);
+  const void* fn = pipelined_select(dtype, op, false);
   if (!fn) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, 0);
 }
 
 cudaError_t launch_pipelined(int dtype, int op, const PersistArgs& a, int threads, cudaStream_t st) {
-  const void* fn = pipelined_select(dtype, op);
+  const void* fn = pipelined_select(dtype, op, a.from_memory != 0);
   if (!fn || a.R < 2 || a.R > kMaxRanks || a.G < 1 || a.J < 1 || a.J > kPipeMaxSlices || a.W < 1 || a.rounds < 1 ||
       !a.shadows)
     return cudaErrorInvalidValue;
