@@ -268,7 +268,10 @@ typedef enum ra_option {
                                 zeroes the inbox and starts again at 1, so no
                                 word left in the inbox ever carries a flag
                                 being waited for.  Setting it is for tests of
-                                that restart. */
+                                that restart.  It governs calls from the host;
+                                once a call has been captured into a CUDA
+                                graph the CTAs' own copies do, until
+                                ra_get_device_status resets the handle. */
   RA_OPT_DEBUG_SHRINK = 11   /* bounds-checked builds only (see
                                 ra_debug_bounds_report): register each of the
                                 call's buffers this many bytes shorter than it
