@@ -119,18 +119,18 @@ struct ClusterInbox {
   uint64_t* box;      // this CTA's rows in shared memory: [message][P * wpe]
   int64_t row;        // words of one row
   uint32_t q;         // the successor's rank in the cluster
+  uint32_t remote;    // the successor's rows, as a shared::cluster address
   __device__ __forceinline__ const uint64_t* recv_row(int m) const { return box + (int64_t)m * row; }
   __device__ __forceinline__ uint64_t load(const uint64_t* w) const {
     uint64_t v;
     asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_addr(w)) : "memory");
     return v;
   }
-  // the same word of the successor's rows (every CTA lays its rows out alike)
+  // the same word of the successor's rows (every CTA lays its rows out
+  // alike, and a CTA's shared memory maps linearly into the cluster window)
   __device__ __forceinline__ void store(int m, int64_t word, uint64_t v) const {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(box + (int64_t)m * row + word)),
-                 "r"(q));
-    asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+    const uint32_t at = remote + (uint32_t)(((int64_t)m * row + word) * sizeof(uint64_t));
+    asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(at), "l"(v) : "memory");
   }
   __device__ __forceinline__ uint32_t flag(int m) const { return (uint32_t)m + 1u; }
   // a poll of shared memory is short next to a look at the clocks or a load
@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_cluster_kernel(const LLArgs 
   tr.box = ll_box;
   tr.row = (int64_t)blockDim.x * (EM == 1 ? 1 : a.E) * WPE;
   tr.q = (uint32_t)((r == a.R - 1) ? 0 : r + 1);
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(tr.remote) : "r"(smem_addr(ll_box)), "r"(tr.q));
   // zero this CTA's rows, then meet: no peer stores into them before
   const int64_t words = (int64_t)(a.rounds - 1) * tr.row;
   for (int64_t i = threadIdx.x; i < words; i += blockDim.x) ll_box[i] = 0;

@@ -16,10 +16,12 @@
 //     (`increase_shadow`, `wait_meet_shadow`).
 // Who uses what: the counting barrier of the persistent kernel (add; each
 // waiter's shadow read ahead from device memory, increase_shadow by R-1,
-// store_shadow, wait_meet_shadow), the per-peer barrier (add, read), the
+// store_shadow, wait_meet_shadow), the per-peer barrier (add, read; each
+// CTA's copy of its epoch kept with load_shadow / store_shadow), the
 // pipelined kernel's progress flags (add; the waiter's shadow of its
 // predecessor's flag, held in a register for the launch: increase_shadow,
-// wait_meet_shadow), and the handle's signal maintenance kernel (reset, add,
+// wait_meet_shadow; its start read back with load_shadow by launches a CUDA
+// graph replays), and the handle's signal maintenance kernel (reset, add,
 // read, increase_shadow, store_shadow; ra_persistent.cu).  The comparison width `bits`
 // (RA_OPT_SIGNAL_BITS) is 64 unless a call asks for fewer, as a counter of
 // 56 bits would.
