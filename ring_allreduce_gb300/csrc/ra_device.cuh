@@ -445,11 +445,6 @@ __device__ __forceinline__ uint32_t load_relaxed_u32(const uint32_t* p) {
   return v;
 }
 
-// Rolling comparison: observed has reached target even across wrap-around.
-__device__ __forceinline__ bool rolling_reached(uint64_t observed, uint64_t target) {
-  return (int64_t)(observed - target) >= 0;
-}
-
 // The first wait that gives up fills the error record; later ones leave it.
 __device__ __forceinline__ void record_wait_error(ra_device_error* err, uint32_t code, int round, int rank,
                                                   int channel, int peer, uint64_t observed, uint64_t expected) {
