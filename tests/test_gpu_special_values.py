@@ -24,7 +24,17 @@ from rahelpers import DeviceBuffers, DeviceRanks, assert_bitwise_equal
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-VARIANTS = ["direct", "ring", "persistent", "pipelined", "local"]
+# the pipelined variant also with its flag-in-data protocols, whose words
+# split 8-byte elements into two 32-bit halves
+VARIANTS = ["direct", "ring", "persistent", "pipelined", "local", "pipelined-LL", "pipelined-LL_CLUSTER"]
+
+
+def _handle(ra, R, n, dtype, op, variant):
+    v, _, protocol = variant.partition("-")
+    h = ra.RingAllReduce(R, n, dtype, op, variant=v)
+    if protocol:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol[protocol])
+    return h
 FLOAT_DTYPES = ["f32", "bf16", "f16", "f64"]
 SHAPES = [(8, 8192), (5, 4099), (3, 65539)]
 
@@ -83,7 +93,7 @@ def test_allreduce_special_values(ra, dtype, op, variant):
         want = _oracle(ring.ring_allreduce, x, elementops.get_op(dtype, op))
         st = inputs.storage_dtype(dtype)
         inp, out = DeviceRanks(R, n, st, host=x), DeviceRanks(R, n, st)
-        with ra.RingAllReduce(R, n, dtype, op, variant=variant) as h:
+        with _handle(ra, R, n, dtype, op, variant) as h:
             h.allreduce(inp.views, out.views)
             status, err = h.device_status()
             assert status == ra.Status.OK, err.as_dict()
@@ -106,7 +116,7 @@ def test_reduce_scatter_special_values(ra, dtype, variant):
     want = _oracle(ring.ring_reduce_scatter, x, elementops.get_op(dtype, op))
     st = inputs.storage_dtype(dtype)
     inp, out = DeviceRanks(R, n, st, host=x), DeviceRanks(R, n, st)
-    with ra.RingAllReduce(R, n, dtype, op, variant=variant) as h:
+    with _handle(ra, R, n, dtype, op, variant) as h:
         h.reduce_scatter(inp.views, out.views)
         assert h.device_status()[0] == ra.Status.OK
     got = out.host()
