@@ -21,6 +21,16 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
 
 VARIANTS = ["direct", "ring", "persistent", "pipelined", "local"]
+# the pipelined variant's flag-in-data protocols, for the small calls they are for
+SMALL_VARIANTS = VARIANTS + ["pipelined-LL", "pipelined-LL_CLUSTER"]
+
+
+def _handle(ra, R, n, dtype, op, variant):
+    v, _, protocol = variant.partition("-")
+    h = ra.RingAllReduce(R, n, dtype, op, variant=v)
+    if protocol:
+        h.set_option(ra.Option.PROTOCOL, ra.Protocol[protocol])
+    return h
 
 
 @pytest.fixture(scope="module")
@@ -39,7 +49,7 @@ def _check_allreduce(ra, x, dtype, op, variants, want=None):
     inp = DeviceRanks(R, n, st, host=x)
     for v in variants:
         out = DeviceRanks(R, n, st)
-        with ra.RingAllReduce(R, n, dtype, op, variant=v) as h:
+        with _handle(ra, R, n, dtype, op, v) as h:
             h.allreduce(inp.views, out.views)
             status, err = h.device_status()
             assert status == ra.Status.OK, err.as_dict()
@@ -52,7 +62,7 @@ def _check_allreduce(ra, x, dtype, op, variants, want=None):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("variant", SMALL_VARIANTS)
 def test_r4_small_placement_and_allgather(ra, variant):
     x = inputs.workload_inputs("r4_small")
     op = elementops.get_op("f32", "sum")
@@ -60,7 +70,7 @@ def test_r4_small_placement_and_allgather(ra, variant):
     S = ring.ring_allreduce(x, op)[0]
     inp = DeviceRanks(R, n, np.float32, host=x)
     out = DeviceRanks(R, n, np.float32)
-    with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
+    with _handle(ra, R, n, "f32", "sum", variant) as h:
         h.reduce_scatter(inp.views, out.views)
         assert h.device_status()[0] == ra.Status.OK
         rs = out.host()
@@ -97,7 +107,7 @@ def test_r16_i32(ra, op):
 @pytest.mark.parametrize("n", inputs.SWEEP_N)
 def test_sweep_r8_f32(ra, n):
     x = inputs.generate(8, n, "f32", "normal", inputs.SWEEP_SEED)
-    _check_allreduce(ra, x, "f32", "sum", VARIANTS)
+    _check_allreduce(ra, x, "f32", "sum", SMALL_VARIANTS if n <= 2**18 else VARIANTS)
 
 
 @pytest.mark.parametrize("R", [R for R in inputs.SWEEP_R if R != 8])
