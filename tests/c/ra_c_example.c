@@ -2,7 +2,8 @@
  * only include/ra.h and the CUDA runtime.  R ranks of n fp32 elements hold
  * x_r[i] = 1000 r + (i mod 997); every output must hold the closed form
  * S[i] = 1000 R(R-1)/2 + R (i mod 997) exactly (small integers: exact in fp32
- * whatever the order).  Runs every variant, the compact forms and the
+ * whatever the order).  Runs every variant (the pipelined one with each message
+ * protocol too), the compact forms and the
  * host-buffer entry point, checks the chunk plan and the placement of the
  * 4-rank example, and exits non-zero on the first mismatch. */
 #include <stdio.h>
@@ -31,7 +32,8 @@
     }                                                                               \
   } while (0)
 
-static int run(int R, size_t n, int variant) {
+/* protocol: the pipelined variant's RA_OPT_PROTOCOL, or -1 to leave it */
+static int run(int R, size_t n, int variant, int protocol) {
   float* host = (float*)malloc(n * sizeof(float));
   void* in[32];
   void* out[32];
@@ -47,6 +49,7 @@ static int run(int R, size_t n, int variant) {
   }
   CHECK_RA(ra_create(R, n, RA_F32, RA_SUM, &h));
   CHECK_RA(ra_set_option(h, RA_OPT_VARIANT, variant));
+  if (protocol >= 0) CHECK_RA(ra_set_option(h, RA_OPT_PROTOCOL, protocol));
   CHECK_RA(ra_allreduce(h, (const void* const*)in, (void* const*)out, NULL));
   CHECK_RA(ra_get_device_status(h, NULL, NULL));
   for (r = 0; r < R; ++r) {
@@ -54,8 +57,8 @@ static int run(int R, size_t n, int variant) {
     for (i = 0; i < n; ++i) {
       const float want = (float)(1000 * R * (R - 1) / 2 + R * (int)(i % 997));
       if (host[i] != want) {
-        fprintf(stderr, "variant %d R=%d n=%zu rank %d element %zu: %f != %f\n", variant, R, n, r, i,
-                host[i], want);
+        fprintf(stderr, "variant %d protocol %d R=%d n=%zu rank %d element %zu: %f != %f\n", variant, protocol, R,
+                n, r, i, host[i], want);
         return 1;
       }
     }
@@ -128,7 +131,12 @@ int main(void) {
   for (v = 0; v < sizeof(variants) / sizeof(variants[0]); ++v)
     for (a = 0; a < sizeof(ranks) / sizeof(ranks[0]); ++a)
       for (b = 0; b < sizeof(sizes) / sizeof(sizes[0]); ++b)
-        if (run(ranks[a], sizes[b], variants[v])) return 1;
+        if (run(ranks[a], sizes[b], variants[v], -1)) return 1;
+  /* the pipelined variant's flag-in-data protocols */
+  for (k = RA_PROTOCOL_LL; k <= RA_PROTOCOL_LL_CLUSTER; ++k)
+    for (a = 0; a < sizeof(ranks) / sizeof(ranks[0]); ++a)
+      for (b = 0; b < sizeof(sizes) / sizeof(sizes[0]); ++b)
+        if (run(ranks[a], sizes[b], RA_VARIANT_PIPELINED, k)) return 1;
   printf("c example: ok\n");
   return 0;
 }
