@@ -15,17 +15,23 @@
 // Every x_r[c] is read once and every output vector written once: the
 // compulsory 2 R n b bytes, with no synchronisation between CTAs.
 //
-// Loads never stall a round.  Warp 0 streams the operands into a ring of
-// kStages shared-memory stages with TMA bulk copies (cp.async.bulk, one
-// mbarrier per stage counting the bytes; lane r copies rank r's part), in
-// load steps that run ahead of the rounds and across slice boundaries: step
+// Loads never stall a round.  The first P warps stream the operands into a
+// ring of shared-memory stages with TMA bulk copies (cp.async.bulk, one
+// mbarrier per stage counting the bytes; warp w copies the parts of ranks
+// w, w + P, ...), in load steps that run ahead of the rounds and across
+// slice boundaries: step
 // 0 of a slice holds x_r[r] for every r (round 1's incoming messages), step
 // s holds x_r[(r - s) mod R].  Round s writes m_r over x_r[c] in step s's
 // stage, so that stage is round s+1's incoming messages and no other buffer
 // is needed.  The folding warps release a step's stage once the round after
 // it is done (the last step's, once its results are stored) by arriving on
 // the stage's second mbarrier; warp 0 waits on that before refilling it and
-// takes no part in the rounds' barriers, so its copies overlap the folds.
+// the copying warps take no part in the rounds' barriers, so their copies
+// overlap the folds.  One warp's lanes issue their bulk copies one after
+// another (~40 ns each on GB300, whatever the size): 32 parts of 960 bytes
+// a step took 1.25 us from one warp and 0.66 us spread over four.  So P is
+// 1 up to 8 ranks and 4 above (the other warps fold, so more copying warps
+// mean smaller stages: 2 or 4 of them cost R = 8 3-6 %).
 // Every wait is bounded; a wait that runs out records error code 2, the
 // folding warps tell warp 0 to stop, and the CTA leaves once its copies in
 // flight have landed.  The unaligned head and tail elements of the chunks
@@ -36,18 +42,27 @@ namespace ra {
 
 namespace {
 
-constexpr int kLocalThreads = 512;   // one CTA per SM: warp 0 issues the bulk copies, 15 warps fold
-constexpr int kStages = 6;           // load steps in flight or in use per CTA
-constexpr int kSliceItems = 1920;    // R * SV <= 1920 16-byte vectors per stage (30 KiB)
-constexpr int kFolders = kLocalThreads - 32;
-constexpr int kItems = kSliceItems / kFolders;       // (rank, vector) positions per folding thread
-static_assert(kItems * kFolders == kSliceItems, "slice items must split evenly over the folding threads");
+constexpr int kLocalThreads = 512;   // one CTA per SM: P warps issue the bulk copies, the others fold
+constexpr int kMaxStages = 8;        // load steps in flight or in use per CTA
+constexpr int kItems = 4;            // (rank, vector) positions per folding thread
+constexpr int kStageBudget = 200 * 1024;   // shared memory of the stages, at most
+
+// Warps issuing the bulk copies, 16-byte vectors a stage holds (kItems per
+// folding thread) and stages, for R ranks.
+__host__ __device__ constexpr int copy_warps(int R) { return R <= 8 ? 1 : 4; }
+__host__ __device__ constexpr int stage_items(int R) { return kItems * (kLocalThreads - 32 * copy_warps(R)); }
+__host__ __device__ constexpr int stage_count(int R) {
+  return kStageBudget / (stage_items(R) * 16) < kMaxStages ? kStageBudget / (stage_items(R) * 16) : kMaxStages;
+}
+static_assert(stage_count(2) >= 2 && stage_count(kMaxRanks) >= 2, "at least two stages");
+static_assert(32 * copy_warps(kMaxRanks) >= kMaxRanks, "a copying lane for every rank");
 
 struct LocalShared {
-  uint64_t full[kStages];     // the stage holds its step's operands
-  uint64_t empty[kStages];    // the folding warps are done with the stage's step
-  int64_t issued;             // steps warp 0 issued (read on abort)
-  int abort;                  // the folding warps gave up: warp 0 stops
+  uint64_t full[kMaxStages];  // the stage holds its step's operands
+  uint64_t empty[kMaxStages]; // the folding warps are done with the stage's step
+  int64_t issued;             // steps the copying warps issued (read on abort)
+  int abort;                  // the folding warps gave up: the copying warps stop
+  int go[2];                  // warp 0 to the other copying warps: step u goes ahead (slot u & 1)
   int64_t cvb[kMaxRanks];     // chunk c's whole vectors: [cvb, cve)
   int64_t cve[kMaxRanks];
   int64_t base[2][kMaxRanks]; // slice j (index j & 1): first vector of chunk c's part
@@ -71,10 +86,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Named barrier 1: the folding warps only (warp 0 never waits on it).
-__device__ __forceinline__ void folders_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kFolders) : "memory"); }
+// Named barrier 1: the nf folding threads only (the copying warps never
+// wait on it); named barrier 2: the copying warps only.
+__device__ __forceinline__ void folders_sync(int nf) { asm volatile("bar.sync 1, %0;" ::"r"(nf) : "memory"); }
+__device__ __forceinline__ void producers_sync(int np) { asm volatile("bar.sync 2, %0;" ::"r"(np) : "memory"); }
 
-__device__ __forceinline__ bool folders_all(bool pred) {
+__device__ __forceinline__ bool folders_all(bool pred, int nf) {
   uint32_t all;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -82,7 +99,7 @@ __device__ __forceinline__ bool folders_all(bool pred) {
       "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(all)
-      : "r"((uint32_t)pred), "n"(kFolders)
+      : "r"((uint32_t)pred), "r"(nf)
       : "memory");
   return all != 0;
 }
@@ -102,9 +119,10 @@ __global__ void __launch_bounds__(kLocalThreads, 1)
 local_kernel(const LocalArgs a) {
   using T = typename D::T;
   constexpr int V = D::kVec;
-  extern __shared__ __align__(128) uint4 smem[];   // stage[kStages][R][SV]
+  extern __shared__ __align__(128) uint4 smem[];   // stage[NS][R][SV]
   __shared__ LocalShared sh;
-  const int R = a.R, SV = a.SV;
+  const int R = a.R, SV = a.SV, P = copy_warps(a.R), NS = stage_count(a.R);
+  const int nf = kLocalThreads - 32 * P;   // folding threads
   const int items = R * SV;
   const int64_t n = a.plan.n, C = a.plan.C;
   uint4* const stage0 = smem;
@@ -113,7 +131,7 @@ local_kernel(const LocalArgs a) {
   const int64_t G = a.slices;
   const int64_t J = G > blockIdx.x ? (G - 1 - blockIdx.x) / gridDim.x + 1 : 0;   // slices of this CTA
   const int64_t steps = J * T_;
-  const bool producer = threadIdx.x < 32;   // warp 0 issues the copies
+  const bool producer = threadIdx.x < 32 * P;   // warps 0 .. P-1 issue the copies
 
   if (threadIdx.x < R) {
     const int64_t off = min((int64_t)threadIdx.x * C, n);
@@ -122,7 +140,7 @@ local_kernel(const LocalArgs a) {
     sh.cve[threadIdx.x] = sp.ve;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&sh.full[i], 1);    // one arrival: lane 0's expect_tx
       mbar_init(&sh.empty[i], 1);   // one arrival: the releasing folding thread
     }
@@ -132,56 +150,75 @@ local_kernel(const LocalArgs a) {
   }
   __syncthreads();
 
-  auto next = [](int st) { return st + 1 == kStages ? 0 : st + 1; };
+  auto next = [NS](int st) { return st + 1 == NS ? 0 : st + 1; };
   bool ok = true;
 
   if (producer) {
-    // Warp 0 issues load steps in order, each once its stage is free.  Step
-    // u: slice u / T_, s = u % T_, stage u % kStages.  Rank r's operand:
-    // x_r[(r - s) mod R] (step 0: x_r[r], round 1's incoming message);
-    // AllGather alone: x_r[(r + 1) mod R].  Lane r copies rank r's part;
-    // lane 0 announces the step's bytes first.
-    const int lane = threadIdx.x;
-    const uint4* const lane_in = lane < R ? static_cast<const uint4*>(a.p.in[lane]) : nullptr;
+    // The copying warps issue load steps in order, each once its stage is
+    // free.  Step u: slice u / T_, s = u % T_, stage u % NS.  Rank r's
+    // operand: x_r[(r - s) mod R] (step 0: x_r[r], round 1's incoming
+    // message); AllGather alone: x_r[(r + 1) mod R].  Warp 0 alone waits
+    // for the stage and announces the step's bytes (lane r: rank r's part),
+    // then tells the other copying warps whether the step goes ahead, so
+    // every warp issues the same steps; warp w copies ranks w + P j (lane j).
+    const int pw = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = pw + P * lane;
+    const uint4* const rank_in = rank < R ? static_cast<const uint4*>(a.p.in[rank]) : nullptr;
+    auto chunk_of = [&](int r, int s) {
+      int c = reduce ? r - s : r + 1;
+      return c < 0 ? c + R : (c >= R ? c - R : c);
+    };
     int64_t slice = 0;
     int s = 0, st = 0;
-    uint32_t eparity = 0;   // bit i: parity of stage i's next release
+    uint32_t eparity = 0;   // bit i: parity of stage i's next release (warp 0)
     int64_t u = 0;
     for (; u < steps; ++u) {
-      if (u >= kStages) {   // the stage's previous step must be released
-        const bool freed = wait_bounded(&sh.empty[st], (eparity >> st) & 1u, a.timeout_ns, &sh.abort);
-        eparity ^= 1u << st;
-        if (!freed) {
-          if (lane == 0 && !sh.abort)
-            record_wait_error(a.err, 2u, s, -1, blockIdx.x, -1, (uint64_t)u, (uint64_t)steps);
-          break;
-        }
-      }
       const int64_t g = blockIdx.x + slice * gridDim.x;
-      int c = reduce ? lane - s : lane + 1;
-      c = c < 0 ? c + R : (c >= R ? c - R : c);
-      int64_t off = 0;
-      const int len = lane < R ? slice_part(sh, c, g, SV, &off) : 0;
-      const uint32_t bytes = __reduce_add_sync(0xffffffffu, (uint32_t)len * 16u);
-      if (lane == 0) mbar_arrive_expect_tx(&sh.full[st], bytes);
-      __syncwarp();
-      if (len > 0) bulk_load(stage0 + st * items + lane * SV, lane_in + off, (uint32_t)len * 16u, &sh.full[st]);
+      bool go = true;
+      if (pw == 0) {
+        if (u >= NS) {   // the stage's previous step must be released
+          go = wait_bounded(&sh.empty[st], (eparity >> st) & 1u, a.timeout_ns, &sh.abort);
+          // one answer for the warp: a lane that saw the release just before
+          // another saw the folding warps give up must not copy alone
+          go = __all_sync(0xffffffffu, go);
+          eparity ^= 1u << st;
+          if (!go && lane == 0 && !sh.abort)
+            record_wait_error(a.err, 2u, s, -1, blockIdx.x, -1, (uint64_t)u, (uint64_t)steps);
+        }
+        if (go) {
+          int64_t off = 0;
+          const int len = lane < R ? slice_part(sh, chunk_of(lane, s), g, SV, &off) : 0;
+          const uint32_t bytes = __reduce_add_sync(0xffffffffu, (uint32_t)len * 16u);
+          if (lane == 0) mbar_arrive_expect_tx(&sh.full[st], bytes);
+        }
+        if (P > 1 && lane == 0) sh.go[u & 1] = go ? 1 : 0;
+      }
+      if (P > 1) {
+        producers_sync(32 * P);   // the bytes are announced before any of the step's copies
+        go = sh.go[u & 1] != 0;
+      }
+      if (!go) break;
+      if (rank < R) {
+        int64_t off = 0;
+        const int len = slice_part(sh, chunk_of(rank, s), g, SV, &off);
+        if (len > 0) bulk_load(stage0 + st * items + rank * SV, rank_in + off, (uint32_t)len * 16u, &sh.full[st]);
+      }
       if (++s == T_) {
         s = 0;
         ++slice;
       }
       st = next(st);
     }
-    if (lane == 0) sh.issued = u;
+    if (threadIdx.x == 0) sh.issued = u;
   } else {
     // Folding warps.  Positions fixed for the whole launch: rank rk, vector
     // own - rk*SV of the slice.
-    const int ft = threadIdx.x - 32;
+    const int ft = threadIdx.x - 32 * P;
     int rk[kItems], own[kItems], pred[kItems];
     uint4* outp[kItems];
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
-      const int i = ft + k * kFolders;
+      const int i = ft + k * nf;
       const bool on = i < items;
       const int r = on ? i / SV : 0;
       const int v = i - r * SV;
@@ -212,7 +249,7 @@ local_kernel(const LocalArgs a) {
         // slice j-1 reads the other table; slice j-2, the last reader of this one, is past a barrier
         sh.len[tb][ft] = slice_part(sh, ft, g, SV, &sh.base[tb][ft]);
       }
-      folders_sync();   // the slice table; and slice j-1's stores have read its last stage
+      folders_sync(nf);   // the slice table; and slice j-1's stores have read its last stage
       if (held >= 0) {
         release(held);
         held = -1;
@@ -253,7 +290,7 @@ local_kernel(const LocalArgs a) {
             record_wait_error(a.err, 2u, s, -1, blockIdx.x, -1, (uint64_t)(j * T_ + s), (uint64_t)steps);
           }
           fence_proxy_async_smem();   // these shared-memory accesses precede later bulk copies into the stages
-          if (!folders_all(got)) {
+          if (!folders_all(got, nf)) {
             ok = false;
             break;
           }
@@ -268,7 +305,7 @@ local_kernel(const LocalArgs a) {
       } else {
         const bool got = wait_stage(cst);
         if (!got) record_wait_error(a.err, 2u, 0, -1, blockIdx.x, -1, (uint64_t)j, (uint64_t)steps);
-        if (!folders_all(got)) {
+        if (!folders_all(got, nf)) {
           ok = false;
           break;
         }
@@ -307,8 +344,8 @@ local_kernel(const LocalArgs a) {
     // of each stage can still be in flight
     if (threadIdx.x == 0) {
       const int64_t issued = sh.issued;
-      for (int64_t u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
-        wait_bounded(&sh.full[u % kStages], (uint32_t)((u / kStages) & 1), a.timeout_ns);
+      for (int64_t u = issued > NS ? issued - NS : 0; u < issued; ++u)
+        wait_bounded(&sh.full[u % NS], (uint32_t)((u / NS) & 1), a.timeout_ns);
     }
     return;
   }
@@ -356,16 +393,17 @@ const void* local_select(int dtype, int op) {
 
 }  // namespace
 
-int local_slice_vectors(int R) { return R < 1 ? 0 : kSliceItems / R; }
+int local_slice_vectors(int R) { return R < 1 ? 0 : stage_items(R) / R; }
 
-size_t local_smem_bytes(int R) { return (size_t)kStages * R * local_slice_vectors(R) * sizeof(uint4); }
+size_t local_smem_bytes(int R) { return R < 1 ? 0 : (size_t)stage_count(R) * R * local_slice_vectors(R) * sizeof(uint4); }
 
 cudaError_t prepare_local() {
+  size_t most = 0;
+  for (int R = 2; R <= kMaxRanks; ++R) most = std::max(most, local_smem_bytes(R));
   cudaError_t err = cudaSuccess;
   for (int dt = RA_F32; dt <= RA_I64 && err == cudaSuccess; ++dt)
     for (int op = RA_SUM; op <= RA_MAX && err == cudaSuccess; ++op)
-      err = cudaFuncSetAttribute(local_select(dt, op), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)local_smem_bytes(1));
+      err = cudaFuncSetAttribute(local_select(dt, op), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
   return err;
 }
 
@@ -381,7 +419,7 @@ cudaError_t launch_local(int dtype, int op, const LocalArgs& a, int ctas, cudaSt
   const cudaError_t e = debug_upload(st);
   if (e != cudaSuccess) return e;
   return with_dtype_op(dtype, op, [&](auto d, auto o) {
-    const size_t smem = (size_t)kStages * a.R * a.SV * sizeof(uint4);
+    const size_t smem = (size_t)stage_count(a.R) * a.R * a.SV * sizeof(uint4);
     local_kernel<decltype(d), decltype(o)::value><<<ctas, kLocalThreads, smem, st>>>(a);
     return cudaGetLastError();
   });

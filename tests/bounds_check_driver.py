@@ -170,11 +170,12 @@ def main():
     ends = [v.data_ptr() + n * 4 for v in inp.views + out.views]
     shrunk_count, shrunk_first = ra.ra_debug_bounds_report(reset=True)
 
-    # bounded waits run out: the local kernel (AllReduce) and the ring
-    # variant's AllGather rounds wait on bulk copies that the checks skip
+    # bounded waits run out: the local kernel (AllReduce; one copying warp at
+    # R = 8, four at R = 16) and the ring variant's AllGather rounds wait on
+    # bulk copies that the checks skip
     timeouts = {}
-    for variant, kind in (("local", "allreduce"), ("ring", "all_gather")):
-        R, n = 8, 8 * 4096
+    for variant, kind, R in (("local", "allreduce", 8), ("local", "allreduce", 16), ("ring", "all_gather", 8)):
+        n = R * 4096
         x = inputs.generate(R, n, "f32", "normal", seed=7)
         o = elementops.get_op("f32", "sum")
         with ra.RingAllReduce(R, n, "f32", "sum", variant=variant) as h:
@@ -204,7 +205,7 @@ def main():
             first["after"] = status2.name
             first["after_equal"] = all(np.array_equal(got[r].view(np.uint32), want[r].view(np.uint32))
                                        for r in range(R))
-        timeouts[variant] = first
+        timeouts[f"{variant} R={R}"] = first
     ra.ra_debug_bounds_report(reset=True)
     print(json.dumps({
         "timeouts": timeouts,
