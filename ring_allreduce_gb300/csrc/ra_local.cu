@@ -19,9 +19,8 @@
 // ring of shared-memory stages with TMA bulk copies (cp.async.bulk, one
 // mbarrier per stage counting the bytes; warp w copies the parts of ranks
 // w, w + P, ...), in load steps that run ahead of the rounds and across
-// slice boundaries: step
-// 0 of a slice holds x_r[r] for every r (round 1's incoming messages), step
-// s holds x_r[(r - s) mod R].  Round s writes m_r over x_r[c] in step s's
+// slice boundaries: step 0 of a slice holds x_r[r] for every r (round 1's
+// incoming messages), step s holds x_r[(r - s) mod R].  Round s writes m_r over x_r[c] in step s's
 // stage, so that stage is round s+1's incoming messages and no other buffer
 // is needed.  The folding warps release a step's stage once the round after
 // it is done (the last step's, once its results are stored) by arriving on
@@ -350,24 +349,37 @@ local_kernel(const LocalArgs a) {
     return;
   }
 
-  // chunk heads and tails off the 16-byte grid: element by element, same ring order
+  // Chunk heads and tails off the 16-byte grid: element by element, in the
+  // same ring order, every chunk's at once -- CTA 0's threads 2V k .. 2V k +
+  // 2V-1 take chunk k (a chunk with a whole vector has at most 2(V-1) such
+  // elements) -- and an element's R loads issued together before the fold.
+  // Taken one chunk after another, each load after the previous fold, they
+  // held R = 24 x 2^24 fp32 back by tens of microseconds: the words around a
+  // chunk boundary are in no bulk copy, so every one of those loads came
+  // from DRAM.
   if (blockIdx.x == 0) {
-    for (int k = 0; k < R; ++k) {
+    constexpr int S = 2 * V;
+    static_assert(S * kMaxRanks <= kLocalThreads, "a thread group for every chunk");
+    const int k = (int)threadIdx.x / S;
+    if (k < R) {
       const int64_t off = min((int64_t)k * C, n);
       const Span<V> sp(off, min(off + C, n));
       const int64_t ns = sp.scalar_count();
       const int owner = (k == 0) ? R - 1 : k - 1;
-      for (int64_t e = threadIdx.x; e < ns; e += blockDim.x) {
+      for (int64_t e = threadIdx.x % S; e < ns; e += S) {
         const int64_t i = sp.scalar_at(e);
         T acc;
         if (!reduce) {
           acc = ld_g(static_cast<const T*>(a.p.in[owner]) + i);
         } else {
-          acc = ld_g(static_cast<const T*>(a.p.in[k]) + i);
-          for (int jr = 1; jr < R; ++jr) {
-            const int q = (k + jr >= R) ? k + jr - R : k + jr;
-            acc = Op<D, OP>::apply(acc, ld_g(static_cast<const T*>(a.p.in[q]) + i));
-          }
+          T x[kMaxRanks];   // x[j]: rank (k + j) mod R's element
+#pragma unroll
+          for (int j = 0; j < kMaxRanks; ++j)
+            if (j < R) x[j] = ld_g(static_cast<const T*>(a.p.in[k + j >= R ? k + j - R : k + j]) + i);
+          acc = x[0];
+#pragma unroll
+          for (int j = 1; j < kMaxRanks; ++j)
+            if (j < R) acc = Op<D, OP>::apply(acc, x[j]);
         }
         if (a.mode == kModeReduceScatter) {
           st_g(static_cast<T*>(a.p.out[owner]) + i, acc);
