@@ -190,7 +190,8 @@ typedef enum ra_protocol {
 
 typedef enum ra_option {
   RA_OPT_VARIANT = 1,        /* ra_variant, default RA_VARIANT_AUTO */
-  RA_OPT_TIMEOUT_NS = 2,     /* limit of every device-side wait in ns, default 1e9 */
+  RA_OPT_TIMEOUT_NS = 2,     /* limit of every device-side wait in ns, 1e3
+                                (1 us) to 6e10 (60 s), default 1e9 */
   RA_OPT_CTAS = 3,           /* CTAs per rank (ring, persistent) or per chunk
                                 (direct), or in all (local); 0 = chosen
                                 from the SM count */

@@ -853,6 +853,7 @@ int pipeline_window(const ra_ctx* h, int J) {
 }
 
 constexpr size_t kLLInboxBytes = (size_t)64 << 20;   // most bytes of the RA_PROTOCOL_LL inbox
+constexpr long long kMaxTimeoutNs = 60LL * 1000 * 1000 * 1000;   // RA_OPT_TIMEOUT_NS at most (60 s)
 
 // The pipelined variant with flag-in-data messages (ra_ll.cu).
 ra_status run_pipelined_ll(ra_ctx* h, int kind, int mode, const void* const* in, void* const* out,
@@ -1554,7 +1555,10 @@ ra_status ra_set_option(ra_handle h, int key, long long value) {
       h->host_windows = (int)value;
       return RA_OK;
     case RA_OPT_TIMEOUT_NS:
-      if (value < 1000) return fail(RA_ERR_INVALID, "timeout %lld ns below 1 us", value);
+      // at most a minute: a wait that cannot end (a withheld arrival) must
+      // not hold a GPU for longer
+      if (value < 1000 || value > kMaxTimeoutNs)
+        return fail(RA_ERR_INVALID, "timeout %lld ns outside [1 us, 60 s]", value);
       h->timeout_ns = value;
       return RA_OK;
     case RA_OPT_CTAS:

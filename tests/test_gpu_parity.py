@@ -346,7 +346,8 @@ def test_argument_checks_on_device(ra):
         # option values outside their ranges are refused and change nothing
         for key, value in ((ra.Option.SLICES, -1), (ra.Option.SLICES, 65), (ra.Option.WINDOW, -1),
                            (ra.Option.WINDOW, 65), (ra.Option.VARIANT, 99), (ra.Option.BARRIER, 7),
-                           (ra.Option.TIMEOUT_NS, 10), (ra.Option.CTAS, -2), (ra.Option.GATHER, 3),
+                           (ra.Option.TIMEOUT_NS, 10), (ra.Option.TIMEOUT_NS, 60_000_000_001),
+                           (ra.Option.CTAS, -2), (ra.Option.GATHER, 3),
                            (ra.Option.HOST_WINDOWS, 9)):
             before = h.get_option(key)
             with pytest.raises(ra.RAError) as e:
