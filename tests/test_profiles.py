@@ -46,3 +46,28 @@ def test_profile_cites_current_sources(path):
         assert h == build.kernel_source_hash(kernel), (
             f"{os.path.basename(path)} was measured on {kernel} sources {h}; "
             f"they are now {build.kernel_source_hash(kernel)}")
+
+
+def _doc_citations():
+    """Every profiles/<name> a top-level document cites (globs included)."""
+    out = set()
+    for doc in ("DESIGN.md", "README.md", "BASELINE.md"):
+        path = os.path.join(ROOT, doc)
+        if os.path.exists(path):
+            with open(path, encoding="utf-8") as fh:
+                out.update(re.findall(r"profiles/[A-Za-z0-9_*.]+", fh.read()))
+    return sorted(c.rstrip(".") for c in out)
+
+
+@pytest.mark.parametrize("cited", _doc_citations())
+def test_cited_profiles_exist(cited):
+    assert glob.glob(os.path.join(ROOT, cited)), f"{cited} is cited but no such summary is committed"
+
+
+@pytest.mark.parametrize("path", PROFILES, ids=[os.path.basename(p) for p in PROFILES])
+def test_profile_states_its_command(path):
+    """Each summary gives the command that produced its figures."""
+    with open(path, encoding="utf-8") as fh:
+        text = fh.read()
+    assert re.search(r"^Commands?\b", text, re.M), f"{os.path.basename(path)} states no command"
+    assert "python " in text, f"{os.path.basename(path)} names no command line"
