@@ -149,3 +149,41 @@ def test_nvml_clock_sampler_without_nvml_falls_back():
         def nvmlInit_v2(self):
             return 9
     assert bench.NvmlClockSampler("GPU-0000", lib=NoInit(0, 0)).start() is None
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _reference_arm(env_extra, *args):
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *args],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the oracle on the host cores, no GPU) prints one
+    JSON line with the contract's keys, on the config it actually ran."""
+    import json
+    res = _reference_arm({}, "--workload", "r4_small", "--steps", "3", "--warmup", "3")
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["config"]["R"] == 4 and d["config"]["n_per_rank"] == 4096   # the whole small workload ran
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert "n=4096" in d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_nothing_on_other_ranks():
+    res = _reference_arm({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"},
+                         "--gpus", "2", "--workload", "r4_small", "--steps", "1", "--warmup", "3")
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert not [l for l in res.stdout.splitlines() if l.startswith("{")], res.stdout
