@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "ring allreduce algbw GB/s and % of GB300 HBM roofline (R ranks on 1 GPU)"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10**6   # GB300's L2
 
 WORKLOAD_TEXT = {
     "r8_f32": "ring allreduce, R=8 ranks x n=2^24 fp32 per rank (64 MiB/rank), N(0,1), sum, seed 1",
@@ -497,6 +498,17 @@ def ring_passes(round_bytes):
     return max(1, min(8, -(-round_bytes // (32 << 20))))
 
 
+def l2_statement(in_bytes):
+    """How a step's timing stands to the L2: inputs larger than it (each step
+    reads them from DRAM, no flush needed), or a call small enough to live
+    in it, timed back to back as the latency figure it is."""
+    if in_bytes > L2_BYTES:
+        return (f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB of inputs, "
+                f"{in_bytes / 2**20:.0f} MiB of outputs per step, no flush")
+    return (f"inputs in L2 ({in_bytes / 2**10:.0f} KiB of inputs, as much of outputs): calls timed "
+            f"back to back without a flush, a latency figure rather than a bandwidth one")
+
+
 def workload_config(args, R, n, op, b, ws):
     """The `config` of a bench line: the workload, identical for the GPU arm
     and the reference arm (which times the oracle on a sample of it)."""
@@ -505,8 +517,7 @@ def workload_config(args, R, n, op, b, ws):
         else f"{args.workload} with n={n}",
         "R": R, "n_per_rank": n, "op": op, "variant": args.variant,
         **({"protocol": args.protocol} if args.protocol != "simple" else {}),
-        "l2": f"inputs larger than L2: {R * n * b / 2**20:.0f} MiB of inputs, "
-              f"{R * n * b / 2**20:.0f} MiB of outputs per step, no flush",
+        "l2": l2_statement(R * n * b),
         "parallelism": f"replicas x{ws} (each GPU runs its own {R}-rank ring)",
     }
 

@@ -187,3 +187,16 @@ def test_reference_arm_prints_nothing_on_other_ranks():
                          "--gpus", "2", "--workload", "r4_small", "--steps", "1", "--warmup", "3")
     assert res.returncode == 0, res.stderr[-2000:]
     assert not [l for l in res.stdout.splitlines() if l.startswith("{")], res.stdout
+
+
+def test_config_says_how_timing_stands_to_the_l2():
+    """Inputs larger than L2 need no flush between steps; a call that fits in
+    L2 is said to be timed back to back, a latency figure."""
+    import argparse
+    import bench
+    args = argparse.Namespace(workload="r8_f32", n=None, variant="auto", protocol="simple")
+    big = bench.workload_config(args, 8, 2**24, "sum", 4, 1)["l2"]
+    assert big.startswith("inputs larger than L2: 512 MiB of inputs")
+    args = argparse.Namespace(workload="r4_small", n=None, variant="auto", protocol="simple")
+    small = bench.workload_config(args, 4, 4096, "sum", 4, 1)["l2"]
+    assert small.startswith("inputs in L2 (64 KiB of inputs") and "latency" in small
