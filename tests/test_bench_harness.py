@@ -200,3 +200,19 @@ def test_config_says_how_timing_stands_to_the_l2():
     args = argparse.Namespace(workload="r4_small", n=None, variant="auto", protocol="simple")
     small = bench.workload_config(args, 4, 4096, "sum", 4, 1)["l2"]
     assert small.startswith("inputs in L2 (64 KiB of inputs") and "latency" in small
+
+
+def test_roofline_traffic_only_from_a_summary_of_the_current_kernel(monkeypatch):
+    """`roofline.traffic` is the committed ncu summary's DRAM bytes per launch,
+    scaled by the units a launch processes, while the summary names the
+    direct kernel's current source hash; null once the kernel has changed."""
+    import bench
+    from ring_allreduce_gb300 import build
+    t, path = bench.profile_traffic("r8_f32", 2**24)
+    assert path.endswith("direct_kernel_r8_f32.md")
+    assert t is not None and 0.9 * 2**30 < t < 1.2 * 2**30    # about the compulsory 1 GiB
+    t2, _ = bench.profile_traffic("r8_f32", 2**25)
+    assert t2 == 2 * t
+    real = build.kernel_source_hash
+    monkeypatch.setattr(build, "kernel_source_hash", lambda k=None: "0" * 16 if k == "direct" else real(k))
+    assert bench.profile_traffic("r8_f32", 2**24)[0] is None
